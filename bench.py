@@ -1,0 +1,522 @@
+"""Benchmark: one mixed decode step (5 sliding + 1 global layer) on GB300.
+
+Workload (seeded, synthetic; shapes from the pages): 64 requests, 4 speculative
+positions each, context lengths log-uniform in [512, 32768].  A step is the
+whole hot path once: for each of 5 sliding layers, carat_ring_append of the 4
+new K/V rows per request into its 1024-slot ring, then carat_swa_attention read
+in place from the rotated rings; for the global layer, the append into the full
+cache, then carat_global_verify_attention (8 heads x 4 positions = 32 rows per
+KV head, masked key tail).
+
+Metric: algorithmic HBM bytes of the step / step time (GB/s), plus us per call.
+Every layer call streams > 400 MB, more than the 129 MB L2, so no L2 flush is
+needed between steps.  Timed steps repeat the same step at fixed positions (same
+work every step).
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+With --impl reference the fp64 CPU oracle is timed instead, on a bounded
+sample of the same workload (the reference arm).  Under torchrun (N > 1) every
+rank runs an independent replica on its own GPU (the path has no exchange step:
+requests are independent), and the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SWA decode + GQA verify attention: HBM GB/s (% of ~8 TB/s), µs/layer call"
+WORKLOAD = "mixed_decode_step_b64_k4_5swa_1global"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = os.path.join(ROOT, "sliding_window_gqa_ring_gb300", "csrc")
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic bytes (what the method must move at least once per call)
+# ---------------------------------------------------------------------------
+
+def sliding_call_bytes(w, b):
+    """Bytes one request moves in one sliding layer: the K and V rows of the
+    union of its queries' windows, its queries, its fp32 outputs, and the
+    append (new rows read + written, displaced rows read + written)."""
+    k, hkv, d, hq = w.proposal_count, w.kv_heads, w.head_dim, w.q_heads
+    kc = int(w.key_counts[b])
+    ctx = kc - k
+    keys = kc - max(0, ctx - w.window + 1)            # positions [max(0,ctx-W+1), kc)
+    row = hkv * d * 2
+    attn = keys * row * 2 + k * hq * d * 2 + k * hq * d * 4
+    disp = sum(1 for i in range(k - 1) if ctx - w.window + 1 + i >= 0)
+    append = k * row * 2 * 2 + disp * row * 2 * 2
+    return attn, append
+
+
+def global_call_bytes(w, b):
+    k, hkv, d, hq = w.proposal_count, w.kv_heads, w.head_dim, w.q_heads
+    kc = int(w.key_counts[b])
+    row = hkv * d * 2
+    attn = kc * row * 2 + k * hq * d * 2 + k * hq * d * 4
+    append = k * row * 2 * 2
+    return attn, append
+
+
+def step_bytes(sliding, glob):
+    s_attn = sum(sliding_call_bytes(sliding, b)[0] for b in range(sliding.batch))
+    s_app = sum(sliding_call_bytes(sliding, b)[1] for b in range(sliding.batch))
+    g_attn = sum(global_call_bytes(glob, b)[0] for b in range(glob.batch))
+    g_app = sum(global_call_bytes(glob, b)[1] for b in range(glob.batch))
+    return {"swa_attention": s_attn, "swa_append": s_app, "global_attention": g_attn,
+            "global_append": g_app,
+            "step": sliding.layers * (s_attn + s_app) + g_attn + g_app}
+
+
+# ---------------------------------------------------------------------------
+# Helpers
+# ---------------------------------------------------------------------------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(KERNEL_SOURCES)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(KERNEL_SOURCES, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(call):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("source_hash") != kernel_source_hash():
+        return None
+    e = t.get("calls", {}).get(call)
+    return None if e is None else e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+        finally:
+            try:
+                os.unlink(self.path)
+            except OSError:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ---------------------------------------------------------------------------
+# Oracle sample (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_jobs(sliding, glob, requests):
+    """(bytes, args) of oracle calls covering the sampled requests: every
+    sliding layer and the global layer of each.  Inputs come from the seeded
+    generators, exactly as staged on the GPU."""
+    from sliding_window_gqa_ring_gb300 import synth
+    jobs = []
+    for b in requests:
+        for layer in range(sliding.layers):
+            first, kh, vh = synth.last_rows(sliding, layer, b, sliding.window
+                                            + sliding.proposal_count)
+            q = synth.queries(sliding, layer, b)
+            jobs.append((sliding_call_bytes(sliding, b)[0], ("swa", layer, b),
+                         (q, kh, vh, first, int(sliding.context_lengths[b]), sliding.window,
+                          sliding.scale)))
+        kc = int(glob.key_counts[b])
+        kh = synth.history(glob, 0, b, 0, kc, "k")
+        vh = synth.history(glob, 0, b, 0, kc, "v")
+        q = synth.queries(glob, 0, b)
+        jobs.append((global_call_bytes(glob, b)[0], ("global", 0, b),
+                     (q, kh, vh, 0, int(glob.context_lengths[b]), 0, glob.scale)))
+    return jobs
+
+
+def time_oracle(jobs, threads):
+    import oracle
+    orc = oracle.default()
+    t0 = time.perf_counter()
+    outs = orc.attention_batch([j[2] for j in jobs], threads=threads)
+    dt = time.perf_counter() - t0
+    return outs, dt
+
+
+# ---------------------------------------------------------------------------
+# The GPU arm
+# ---------------------------------------------------------------------------
+
+def run_carat(args, world, rank, local):
+    import torch
+
+    from sliding_window_gqa_ring_gb300 import carat, engine, synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sliding, glob = synth.mixed_step()
+    B, k = sliding.batch, sliding.proposal_count
+    nbytes = step_bytes(sliding, glob)
+
+    # --- stage the state: rings and caches written through carat_ring_append
+    t_stage = time.perf_counter()
+    sample = list(range(0, B, max(1, B // args.sample_requests))) if rank == 0 else []
+    layers = []
+    for li in range(sliding.layers):
+        lay = engine.SlidingLayer(B, window=sliding.window, q_heads=sliding.q_heads,
+                                  kv_heads=sliding.kv_heads, head_dim=sliding.head_dim,
+                                  max_proposals=k, scale=sliding.scale, device=dev)
+        inp = engine.stage_sliding(sliding, li, lay)
+        inp.host["hist"] = {}
+        layers.append((lay, inp))
+    glay = engine.GlobalLayer(B, capacity=glob.capacity, q_heads=glob.q_heads,
+                              kv_heads=glob.kv_heads, head_dim=glob.head_dim, max_proposals=k,
+                              scale=glob.scale, device=dev)
+    ginp = engine.stage_global(glob, 0, glay, keep_history=False)
+    outs = [torch.empty(inp.queries.shape, dtype=torch.float32, device=dev) for _, inp in layers]
+    gout = torch.empty(ginp.queries.shape, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+    stage_s = time.perf_counter() - t_stage
+
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for (lay, inp), out in zip(layers, outs):
+            lay.step(inp.queries, inp.k_new, inp.v_new, inp.context_lengths, out=out)
+        glay.step(ginp.queries, ginp.k_new, ginp.v_new, ginp.context_lengths, out=gout)
+
+    # --- first step: its outputs are checked against the oracle sample
+    step()
+    torch.cuda.synchronize()
+    first_outs = [o.cpu().numpy() for o in outs]
+    first_gout = gout.cpu().numpy()
+
+    cpu_baseline = None
+    parity = None
+    if rank == 0 and args.cpu_baseline:
+        jobs = oracle_jobs(sliding, glob, sample)
+        threads = os.cpu_count() or 1
+        refs, dt = time_oracle(jobs, threads)
+        moved = sum(j[0] for j in jobs)
+        worst = 0.0
+        for (nb, (kind, li, b), _), ref in zip(jobs, refs):
+            got = first_outs[li][b] if kind == "swa" else first_gout[b]
+            worst = max(worst, float(np.abs(got - ref).max()))
+        parity = {"requests": len(sample), "max_abs_err": worst, "gate": 2e-2,
+                  "ok": worst <= 2e-2}
+        cpu_baseline = {"value": moved / dt / 1e9, "unit": "GB/s", "cores": threads,
+                        "kind": "oracle",
+                        "sample": (f"fp64 C oracle, all 6 layers' attention for {len(sample)} of "
+                                   f"{B} requests ({moved / 1e9:.3f} GB of algorithmic bytes), "
+                                   f"{dt:.2f} s wall on {threads} threads")}
+
+    # --- warm-up
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # --- timed region
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = carat.kernel_launches()
+    with ClockSampler(local) as clk:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    launches = carat.kernel_launches() - launches0
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+        torch.distributed.barrier()
+    clocks = clk.summary()
+    ms_per_step = ms / args.steps
+    value = world * nbytes["step"] * args.steps / (ms / 1e3) / 1e9
+
+    # --- per-call breakdown (events around each call)
+    calls = {"swa_append": [], "swa_attention": [], "global_append": [],
+             "global_attention": []}
+    reps = max(3, min(args.steps, 50))
+    ev = []
+    for _ in range(reps):
+        for (lay, inp), out in zip(layers, outs):
+            a, bb, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            a.record(stream)
+            lay.append(inp.k_new, inp.v_new, inp.context_lengths)
+            bb.record(stream)
+            lay.attend(inp.queries, inp.context_lengths, out=out)
+            c.record(stream)
+            ev.append(("swa", a, bb, c))
+        a, bb, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a.record(stream)
+        glay.append(ginp.k_new, ginp.v_new, ginp.context_lengths)
+        bb.record(stream)
+        glay.attend(ginp.queries, ginp.context_lengths, out=gout)
+        c.record(stream)
+        ev.append(("global", a, bb, c))
+    torch.cuda.synchronize()
+    for kind, a, bb, c in ev:
+        calls[f"{kind}_append"].append(a.elapsed_time(bb) * 1e3)
+        calls[f"{kind}_attention"].append(bb.elapsed_time(c) * 1e3)
+    per_call = {}
+    for name, us in calls.items():
+        mean_us = statistics.mean(us)
+        per_call[name] = {"us": round(mean_us, 3), "gb_s": round(nbytes[name] / (mean_us * 1e3), 1),
+                          "bytes": nbytes[name],
+                          "launches_per_step": (sliding.layers if name.startswith("swa") else 1)}
+    share = {n: per_call[n]["us"] * per_call[n]["launches_per_step"] for n in per_call}
+    dominant = max(share, key=share.get)
+    peak, peak_kind = measured_peaks()
+    achieved = per_call[dominant]["gb_s"]
+    roofline = {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peak,
+                "peak_source": f"{peak_kind} hbm_gbs", "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": profiled_traffic(dominant),
+                "algorithmic_bytes_per_launch": nbytes[dominant],
+                "timing": "CUDA events around the whole call (split-K kernel + combine)"}
+
+    # --- end to end through the public API with host buffers
+    pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())  # noqa: E731
+    h_in = [(pin(inp.queries), pin(inp.k_new), pin(inp.v_new), pin(inp.context_lengths))
+            for _, inp in layers]
+    g_in = (pin(ginp.queries), pin(ginp.k_new), pin(ginp.v_new), pin(ginp.context_lengths))
+    h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    g_hout = torch.empty(gout.shape, dtype=gout.dtype, pin_memory=True)
+    d_in = [tuple(torch.empty_like(x, device=dev) for x in hi) for hi in h_in]
+    gd_in = tuple(torch.empty_like(x, device=dev) for x in g_in)
+    h2d = sum(x.numel() * x.element_size() for hi in h_in for x in hi) + \
+        sum(x.numel() * x.element_size() for x in g_in)
+    d2h = sum(o.numel() * o.element_size() for o in h_out) + g_hout.numel() * g_hout.element_size()
+
+    def e2e_step():
+        for (lay, _), hi, di, out, ho in zip(layers, h_in, d_in, outs, h_out):
+            for src, dst in zip(hi, di):
+                dst.copy_(src, non_blocking=True)
+            lay.step(di[0], di[1], di[2], di[3], out=out)
+            ho.copy_(out, non_blocking=True)
+        for src, dst in zip(g_in, gd_in):
+            dst.copy_(src, non_blocking=True)
+        glay.step(gd_in[0], gd_in[1], gd_in[2], gd_in[3], out=gout)
+        g_hout.copy_(gout, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 200))
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * nbytes["step"] * e2e_steps / (e2e_ms / 1e3) / 1e9
+
+    status = carat.carat_get_device_status(clear=True)
+    if rank != 0:
+        return None
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16; shapes of the pages' Gemma-4 layers)",
+        "config": {"workload": WORKLOAD, "batch": B, "proposal_count": k,
+                   "sliding_layers": sliding.layers, "global_layers": 1,
+                   "window": sliding.window, "sliding_heads": "16 q / 8 kv x 256",
+                   "global_heads": "16 q / 2 kv x 512", "global_capacity": glob.capacity,
+                   "context_lengths": "log-uniform [512, 32768], seed 1006",
+                   "mean_key_count": float(np.mean(glob.key_counts)),
+                   "step_bytes": nbytes["step"],
+                   "l2": "no flush: every layer call streams more than the 129 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline,
+        "per_call": per_call,
+        "cpu_baseline": cpu_baseline,
+        "parity_sample": parity,
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / e2e_steps, 4),
+                "steps": e2e_steps},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "device_status": status,
+        "stage_seconds": round(stage_s, 1),
+    }
+    return line
+
+
+# ---------------------------------------------------------------------------
+# The reference arm: the oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    from sliding_window_gqa_ring_gb300 import synth
+    sliding, glob = synth.mixed_step()
+    threads = os.cpu_count() or 1
+    # one step = the oracle over a bounded slice of the step's work, sized so
+    # the whole --warmup + --steps run stays within about a minute
+    budget_s = 60.0 / max(1, args.steps + args.warmup)
+    order = list(range(sliding.batch))
+    jobs_all = oracle_jobs(sliding, glob, order[:threads])
+    # estimate cost per job from bytes (global jobs dominate)
+    _, t_one = time_oracle(jobs_all[:1], 1)
+    per_byte = t_one / max(1, jobs_all[0][0])
+    target_bytes = budget_s * threads / per_byte
+    jobs, acc = [], 0
+    for j in sorted(jobs_all, key=lambda j: j[0]):
+        if acc + j[0] > target_bytes and jobs:
+            break
+        jobs.append(j)
+        acc += j[0]
+    for _ in range(args.warmup):
+        time_oracle(jobs, threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        time_oracle(jobs, threads)
+    dt = time.perf_counter() - t0
+    moved = sum(j[0] for j in jobs) * args.steps
+    value = moved / dt / 1e9
+    sample = (f"fp64 C oracle, {len(jobs)} attention calls per step (one request-layer each, "
+              f"{sum(j[0] for j in jobs) / 1e6:.1f} MB algorithmic) on {threads} threads")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch": sliding.batch,
+                       "proposal_count": sliding.proposal_count},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["carat", "reference"], default="carat")
+    ap.add_argument("--sample-requests", type=int, default=16,
+                    help="requests the oracle recomputes for the CPU baseline / parity sample")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    line = run_carat(args, world, rank, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

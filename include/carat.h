@@ -1,0 +1,221 @@
+/*
+ * carat.h -- C ABI of libcarat.so: sliding-window ring-buffer KV cache and
+ * grouped-query attention for Gemma-4-style decoding and speculative verify,
+ * written for one NVIDIA GB300 (sm_103a).
+ *
+ * Two parts, as the pages describe them:
+ *
+ *  1. Sliding-window layers keep each request's K and V history in a fixed
+ *     ring of `window` slots (1024 for Gemma 4).  A token's slot is its
+ *     absolute position modulo the window, and a new token overwrites the
+ *     slot of the token one window older, with nothing shifted
+ *     ("Announcing Carat: An inference engine designed for Gemma 4", section
+ *     "Replacing page lookups with a ring buffer").  K and V are written in
+ *     lockstep, so both rings share one rotation, and attention reads the
+ *     rotated rings in place: attention does not depend on a common
+ *     reordering of K and V ("Improving Decode Throughput on Intel Gaudi 3",
+ *     section "Our approach").
+ *
+ *  2. Global layers keep the full history in a zero-initialised cache.  Their
+ *     speculative-verify attention groups the query heads that share one KV
+ *     head together with all proposal positions into one tile of rows
+ *     (8 heads x 4 positions = 32 rows for Gemma 4), computes QK^T, a causal
+ *     softmax and PV, and masks the key tail past key_count
+ *     ("Announcing Carat ...", sections "More FLOPs can be faster" and
+ *     "Doing it all in one kernel can be slower").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers on the current CUDA device and
+ *    must be 16-byte aligned.  `stream` is a cudaStream_t passed as void*
+ *    (NULL = the legacy default stream).  Every call is asynchronous on that
+ *    stream; nothing synchronises the host.
+ *  - bf16 tensors are raw IEEE bfloat16; outputs are fp32.  Layouts are dense
+ *    row-major in the order written next to each argument.
+ *  - The caller owns every buffer, including the workspace; the library
+ *    allocates no device memory and keeps no state across calls except one
+ *    device status word per GPU (carat_get_device_status).
+ *  - Positions.  For request b, context_lengths[b] tokens are in the cache
+ *    BEFORE this step; the step's proposal_count new tokens sit at positions
+ *    context_lengths[b] + j, j = 0 .. proposal_count-1, and
+ *    key_count = context_length + proposal_count (the "More FLOPs" section's
+ *    key_count).  Query j of request b is the token at position
+ *    context_lengths[b] + j.  Plain decode is proposal_count = 1.
+ *  - Grouping.  Query head h reads KV head h / (q_heads / kv_heads).
+ *  - Errors.  Nothing aborts and nothing throws across the ABI.  Argument
+ *    checks run on the host before any launch and return a status without
+ *    touching the GPU.  Values that live in device memory (context lengths,
+ *    ring ids) are checked by the kernels: a request with a bad value is
+ *    skipped, its outputs are written as NaN, and a bit is set in the device
+ *    status word (CARAT_DEV_*).  A failed launch returns CARAT_ERR_CUDA.
+ *  - batch == 0 is valid and launches nothing.
+ */
+#ifndef CARAT_H
+#define CARAT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum carat_status {
+    CARAT_OK = 0,
+    CARAT_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, inconsistent sizes */
+    CARAT_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim, rows per tile */
+    CARAT_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required */
+    CARAT_ERR_CUDA = 4           /* a CUDA runtime call or launch failed */
+} carat_status;
+
+/* Bits of the device status word. */
+#define CARAT_DEV_BAD_CONTEXT 0x1 /* context_length < 0, or key_count > capacity */
+#define CARAT_DEV_BAD_CACHE_ID 0x2 /* ring/cache id outside [0, num_rings) */
+
+/* Largest proposal_count the attention entry points accept. */
+#define CARAT_MAX_PROPOSALS 16
+/* Largest (q_heads / kv_heads) * proposal_count, the rows of one tile. */
+#define CARAT_MAX_TILE_ROWS 128
+
+/*
+ * carat_ring_append -- write this step's new K and V rows into a ring.
+ *
+ * Source: "Announcing Carat ...", "Replacing page lookups with a ring
+ * buffer" (slot = position mod window; a new token reuses the oldest slot
+ * without shifting); "Improving Decode Throughput on Intel Gaudi 3", "Our
+ * approach" (for each decoded token the new KV is written and the head moves
+ * on by one; K and V in lockstep).
+ *
+ *   k_ring, v_ring   bf16 [num_rings][window][kv_heads][head_dim]; ring r
+ *                    belongs to one request.  Slot s of ring r holds the
+ *                    latest position t with t mod window == s.
+ *   ring_ids         int32 [batch]: ring of request b; NULL = ring b
+ *                    (then num_rings >= batch).
+ *   k_new, v_new     bf16 [batch][proposal_count][kv_heads][head_dim]: rows
+ *                    for positions context_lengths[b] + j.
+ *   context_lengths  int32 [batch]: tokens in the ring before this append.
+ *   displaced        bf16 [batch][proposal_count-1][2][kv_heads][head_dim]
+ *                    (K then V) or NULL.  When proposal_count > 1 the new
+ *                    tokens overwrite slots whose old rows the step's earlier
+ *                    queries still attend to; if `displaced` is given, those
+ *                    rows (positions context_length - window + 1 + i) are
+ *                    copied there first, for carat_swa_attention.  Entries
+ *                    whose position is negative are left untouched.
+ *   window           ring slots (1024 for Gemma 4's sliding layers).  A
+ *                    global-layer cache of `capacity` rows is a ring with
+ *                    window = capacity whose positions never wrap.
+ *
+ * Limits: 1 <= proposal_count <= window; proposal_count <= 16 when
+ * displaced != NULL; kv_heads * head_dim * 2 bytes must be a multiple of 16.
+ * Appending proposal_count up to `window` rows with displaced == NULL is how a
+ * prompt's last `window` tokens are written after prefill.
+ */
+carat_status carat_ring_append(void *k_ring, void *v_ring, int num_rings,
+                               const int32_t *ring_ids,
+                               const void *k_new, const void *v_new,
+                               const int32_t *context_lengths, int proposal_count,
+                               void *displaced,
+                               int batch, int kv_heads, int head_dim, int window,
+                               void *stream);
+
+/*
+ * carat_swa_attention -- sliding-window decode / verify attention read
+ * straight from the rotated rings (no gather, no un-rotation).
+ *
+ * Source: "Improving Decode Throughput on Intel Gaudi 3", "Our approach"
+ * (both ring buffers go straight into one fused attention kernel) and
+ * "Patching sliding window KV allocation" (sliding layers attend to the most
+ * recent 1024 tokens).  Query j at position p attends to positions
+ * [max(0, p - window + 1), p], its own included.
+ *
+ *   out              fp32 [batch][proposal_count][q_heads][head_dim]
+ *   queries          bf16 [batch][proposal_count][q_heads][head_dim], after
+ *                    the positional embedding.
+ *   k_ring, v_ring, num_rings, ring_ids   as in carat_ring_append, AFTER
+ *                    this step's append.
+ *   displaced        as written by carat_ring_append; required (non-NULL)
+ *                    when proposal_count > 1, ignored when it is 1.
+ *   context_lengths  int32 [batch]: tokens before this step.
+ *   scale            softmax scale applied to q.k (e.g. 1/sqrt(head_dim)).
+ *   workspace        device scratch of at least carat_swa_workspace_bytes(...)
+ *                    bytes, owned by the caller; contents need no
+ *                    initialisation and are overwritten.  Calls that overlap on
+ *                    the GPU need separate workspaces.
+ *
+ * Supported: head_dim 256 or 512; (q_heads/kv_heads)*proposal_count <= 128;
+ * proposal_count <= 16 and <= window.
+ */
+carat_status carat_swa_attention(float *out, const void *queries,
+                                 const void *k_ring, const void *v_ring, int num_rings,
+                                 const int32_t *ring_ids, const void *displaced,
+                                 const int32_t *context_lengths, int proposal_count,
+                                 int batch, int q_heads, int kv_heads, int head_dim,
+                                 int window, float scale,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * carat_global_verify_attention -- grouped-head speculative-verify attention
+ * over a full (global-layer) cache.
+ *
+ * Source: "Announcing Carat ...", "More FLOPs can be faster" (key_count =
+ * context_length + proposal_count; QK^T, a causal softmax in which query j
+ * ignores every key after its own position, then PV; the cache tail past key_count is
+ * zero-initialised and masked, so padding the key dimension changes nothing)
+ * and "Doing it all in one kernel can be slower" (the query heads sharing a
+ * KV head and all proposal positions form one set of rows against the same
+ * cached K and V).
+ *
+ *   out              fp32 [batch][proposal_count][q_heads][head_dim]
+ *   queries          bf16 [batch][proposal_count][q_heads][head_dim]
+ *   key_cache, value_cache  bf16 [num_caches][capacity][kv_heads][head_dim]:
+ *                    row t of cache c holds position t.  This step's tokens
+ *                    must already be appended (e.g. carat_ring_append with
+ *                    window = capacity).  Rows past key_count are never read
+ *                    into the result.
+ *   cache_ids        int32 [batch] or NULL (= cache b; num_caches >= batch).
+ *   context_lengths  int32 [batch]; key_count = context_length +
+ *                    proposal_count must be <= capacity (checked on device).
+ *   workspace        >= carat_global_workspace_bytes(...) bytes, as above.
+ *
+ * Supported: head_dim 256 or 512; (q_heads/kv_heads)*proposal_count <= 128;
+ * proposal_count <= 16.
+ */
+carat_status carat_global_verify_attention(float *out, const void *queries,
+                                           const void *key_cache, const void *value_cache,
+                                           int num_caches, const int32_t *cache_ids,
+                                           const int32_t *context_lengths, int proposal_count,
+                                           int batch, int q_heads, int kv_heads, int head_dim,
+                                           int capacity, float scale,
+                                           void *workspace, size_t workspace_bytes,
+                                           void *stream);
+
+/* Workspace bytes the two attention calls need for these sizes (0 if the
+ * sizes are invalid).  Pure host arithmetic; no CUDA call. */
+size_t carat_swa_workspace_bytes(int batch, int proposal_count, int q_heads, int kv_heads,
+                                 int head_dim, int window);
+size_t carat_global_workspace_bytes(int batch, int proposal_count, int q_heads,
+                                    int kv_heads, int head_dim, int capacity);
+
+/*
+ * Read (and, if clear != 0, reset) the current device's status word
+ * (CARAT_DEV_* bits, 0 = nothing seen).  Enqueued on `stream` and
+ * synchronised with it before returning.
+ */
+carat_status carat_get_device_status(int32_t *host_out, int clear, void *stream);
+
+/* Static English text for a status code. */
+const char *carat_status_string(carat_status status);
+
+/* Number of CUDA kernels this library has launched in this process, on any
+ * device (a host-side counter, incremented once per kernel launch). */
+uint64_t carat_kernel_launches(void);
+
+/* ABI version of this header (incremented on incompatible changes). */
+#define CARAT_ABI_VERSION 1
+int carat_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CARAT_H */

@@ -1,0 +1,208 @@
+"""ctypes binding of libcarat.so: the same entry points, torch tensors in.
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  Tensors must already live on the current CUDA device; the calls are
+enqueued on torch's current stream (or the one passed) and return without
+synchronising.  A missing library raises ``CaratError`` -- there is no CPU
+fallback.
+
+Layouts (see include/carat.h for the full contract):
+  queries   bf16 [B][k][Hq][D]          out   fp32 [B][k][Hq][D]
+  rings     bf16 [num_rings][window][Hkv][D]
+  caches    bf16 [num_caches][capacity][Hkv][D]
+  new rows  bf16 [B][k][Hkv][D]         displaced bf16 [B][k-1][2][Hkv][D]
+  context_lengths int32 [B]; ring_ids / cache_ids int32 [B] or None
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(_HERE, "libcarat.so")
+
+CARAT_OK = 0
+CARAT_ERR_INVALID_ARG = 1
+CARAT_ERR_UNSUPPORTED = 2
+CARAT_ERR_WORKSPACE = 3
+CARAT_ERR_CUDA = 4
+CARAT_DEV_BAD_CONTEXT = 0x1
+CARAT_DEV_BAD_CACHE_ID = 0x2
+MAX_PROPOSALS = 16
+MAX_TILE_ROWS = 128
+
+EXPORTED = (
+    "carat_ring_append", "carat_swa_attention", "carat_global_verify_attention",
+    "carat_swa_workspace_bytes", "carat_global_workspace_bytes", "carat_get_device_status",
+    "carat_status_string", "carat_abi_version", "carat_kernel_launches",
+)
+
+
+class CaratError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def _declare(lib):
+    vp, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+    lib.carat_ring_append.restype = i32
+    lib.carat_ring_append.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, vp]
+    lib.carat_swa_attention.restype = i32
+    lib.carat_swa_attention.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, i32, i32, i32, i32, i32,
+                                        i32, f32, vp, sz, vp]
+    lib.carat_global_verify_attention.restype = i32
+    lib.carat_global_verify_attention.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32,
+                                                  i32, i32, f32, vp, sz, vp]
+    lib.carat_swa_workspace_bytes.restype = sz
+    lib.carat_swa_workspace_bytes.argtypes = [i32] * 6
+    lib.carat_global_workspace_bytes.restype = sz
+    lib.carat_global_workspace_bytes.argtypes = [i32] * 6
+    lib.carat_get_device_status.restype = i32
+    lib.carat_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32), i32, vp]
+    lib.carat_status_string.restype = ctypes.c_char_p
+    lib.carat_status_string.argtypes = [i32]
+    lib.carat_abi_version.restype = i32
+    lib.carat_abi_version.argtypes = []
+    lib.carat_kernel_launches.restype = ctypes.c_uint64
+    lib.carat_kernel_launches.argtypes = []
+    return lib
+
+
+def library():
+    """The loaded libcarat.so (raises CaratError if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIBRARY):
+                raise CaratError(CARAT_ERR_CUDA, f"libcarat.so not built ({LIBRARY}); run "
+                                 "python -c 'import __graft_entry__ as g; g.build()'")
+            _lib = _declare(ctypes.CDLL(LIBRARY))
+    return _lib
+
+
+_STATUS_TEXT = {
+    CARAT_OK: "ok",
+    CARAT_ERR_INVALID_ARG: "invalid argument",
+    CARAT_ERR_UNSUPPORTED: "unsupported size",
+    CARAT_ERR_WORKSPACE: "workspace missing or too small",
+    CARAT_ERR_CUDA: "CUDA error",
+}
+
+
+def status_string(status: int) -> str:
+    """Text for a status code (the same strings carat_status_string returns)."""
+    return _STATUS_TEXT.get(status, "unknown status")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor or None")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _expect(t, dtype, name):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _check(status: int, what: str):
+    if status != CARAT_OK:
+        raise CaratError(status, what)
+
+
+def carat_ring_append(k_ring, v_ring, k_new, v_new, context_lengths, *, ring_ids=None,
+                      displaced=None, window=None, stream=None):
+    """Write this step's K/V rows at slot = position mod window (lockstep K, V).
+
+    k_new/v_new: bf16 [B][k][Hkv][D]; rings bf16 [num_rings][window][Hkv][D].
+    """
+    _expect(k_ring, torch.bfloat16, "k_ring")
+    _expect(k_new, torch.bfloat16, "k_new")
+    _expect(context_lengths, torch.int32, "context_lengths")
+    num_rings, ring_window, kv_heads, head_dim = k_ring.shape
+    batch, k = k_new.shape[0], k_new.shape[1]
+    if window is None:
+        window = ring_window
+    _check(library().carat_ring_append(
+        _ptr(k_ring), _ptr(v_ring), num_rings, _ptr(ring_ids), _ptr(k_new), _ptr(v_new),
+        _ptr(context_lengths), k, _ptr(displaced), batch, kv_heads, head_dim, window,
+        _stream(stream)), "carat_ring_append")
+
+
+def swa_workspace_bytes(batch, proposal_count, q_heads, kv_heads, head_dim, window) -> int:
+    return int(library().carat_swa_workspace_bytes(batch, proposal_count, q_heads, kv_heads,
+                                                   head_dim, window))
+
+
+def global_workspace_bytes(batch, proposal_count, q_heads, kv_heads, head_dim, capacity) -> int:
+    return int(library().carat_global_workspace_bytes(batch, proposal_count, q_heads, kv_heads,
+                                                      head_dim, capacity))
+
+
+def carat_swa_attention(out, queries, k_ring, v_ring, context_lengths, *, scale, workspace,
+                        ring_ids=None, displaced=None, stream=None):
+    """Sliding-window attention read in place from the rotated rings.
+
+    out fp32 [B][k][Hq][D]; queries bf16 [B][k][Hq][D]; workspace: a CUDA tensor
+    of at least swa_workspace_bytes(...) bytes.
+    """
+    _expect(queries, torch.bfloat16, "queries")
+    _expect(out, torch.float32, "out")
+    batch, k, q_heads, head_dim = queries.shape
+    num_rings, window, kv_heads, _ = k_ring.shape
+    _check(library().carat_swa_attention(
+        _ptr(out), _ptr(queries), _ptr(k_ring), _ptr(v_ring), num_rings, _ptr(ring_ids),
+        _ptr(displaced), _ptr(context_lengths), k, batch, q_heads, kv_heads, head_dim, window,
+        float(scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "carat_swa_attention")
+
+
+def carat_global_verify_attention(out, queries, key_cache, value_cache, context_lengths, *,
+                                  scale, workspace, cache_ids=None, stream=None):
+    """Grouped-head causal verify attention over a full cache (masked tail)."""
+    _expect(queries, torch.bfloat16, "queries")
+    _expect(out, torch.float32, "out")
+    batch, k, q_heads, head_dim = queries.shape
+    num_caches, capacity, kv_heads, _ = key_cache.shape
+    _check(library().carat_global_verify_attention(
+        _ptr(out), _ptr(queries), _ptr(key_cache), _ptr(value_cache), num_caches,
+        _ptr(cache_ids), _ptr(context_lengths), k, batch, q_heads, kv_heads, head_dim, capacity,
+        float(scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "carat_global_verify_attention")
+
+
+def carat_get_device_status(clear: bool = True, stream=None) -> int:
+    v = ctypes.c_int32(0)
+    _check(library().carat_get_device_status(ctypes.byref(v), 1 if clear else 0, _stream(stream)),
+           "carat_get_device_status")
+    return int(v.value)
+
+
+def kernel_launches() -> int:
+    """Kernels libcarat.so has launched in this process so far."""
+    return int(library().carat_kernel_launches())
+
+
+def workspace_tensor(nbytes: int, device=None) -> torch.Tensor:
+    """A 256-byte aligned uint8 CUDA tensor of at least nbytes (torch owns it)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")

@@ -1,0 +1,300 @@
+// api.cu -- the extern "C" entry points of libcarat.so.
+//
+// Host side only: argument checks (before any CUDA call), the split plan that
+// sizes the caller's workspace, and the launches.  The kernels live in
+// ring_append.cu and attention_*.cu.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "carat_internal.cuh"
+
+namespace carat {
+
+// One status word per device, read back by carat_get_device_status.
+__device__ int g_device_status;
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_status_mutex;
+int *g_status_ptr[kMaxDevices];
+
+// Device address of this device's status word (looked up once per device).
+int *device_status_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_status_mutex);
+    if (!g_status_ptr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int *>(ptr);
+    }
+    return g_status_ptr[dev];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_head_dim(int d) { return d == 256 || d == 512; }
+
+// Occupancy target for the split plan: CTAs wanted in flight.
+constexpr long long kTargetCtas = 8LL * 152;
+
+struct SplitPlan {
+    int chunk = 0;
+    int nchunks = 0;
+    size_t ml_bytes = 0;
+    size_t o_bytes = 0;
+    size_t total = 0;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Choose keys per split: the largest power of two in [64, 4096] that still
+// gives kTargetCtas CTAs over all (request, KV head) pairs.
+SplitPlan make_plan(long long pairs, long long keys, int rows, int head_dim) {
+    SplitPlan p;
+    int chunk = 64;
+    for (int c = 4096; c >= 64; c >>= 1) {
+        long long n = (keys + c - 1) / c;
+        if (pairs * n >= kTargetCtas) {
+            chunk = c;
+            break;
+        }
+    }
+    p.chunk = chunk;
+    p.nchunks = (int)((keys + chunk - 1) / chunk);
+    const size_t parts = (size_t)pairs * p.nchunks * rows;
+    p.ml_bytes = align256(parts * sizeof(float2));
+    p.o_bytes = align256(parts * (size_t)head_dim * sizeof(float));
+    p.total = p.ml_bytes + p.o_bytes;
+    return p;
+}
+
+bool attention_shape_ok(int batch, int proposal_count, int q_heads, int kv_heads, int head_dim) {
+    return batch >= 0 && proposal_count >= 1 && proposal_count <= kMaxProposals && q_heads >= 1 &&
+           kv_heads >= 1 && q_heads % kv_heads == 0 && head_dim >= 1;
+}
+
+carat_status attention_unsupported(int proposal_count, int q_heads, int kv_heads, int head_dim) {
+    if (!supported_head_dim(head_dim)) return CARAT_ERR_UNSUPPORTED;
+    if ((long long)(q_heads / kv_heads) * proposal_count > kMaxTileRows) return CARAT_ERR_UNSUPPORTED;
+    return CARAT_OK;
+}
+
+SplitPlan swa_plan(int batch, int proposal_count, int q_heads, int kv_heads, int head_dim,
+                   int window) {
+    const int rows = (q_heads / kv_heads) * proposal_count;
+    return make_plan((long long)batch * kv_heads,
+                     keys_scanned(KeySource::kRing, window, proposal_count, 0), rows, head_dim);
+}
+
+SplitPlan global_plan(int batch, int proposal_count, int q_heads, int kv_heads, int head_dim,
+                      int capacity) {
+    const int rows = (q_heads / kv_heads) * proposal_count;
+    return make_plan((long long)batch * kv_heads, capacity, rows, head_dim);
+}
+
+carat_status launch_status(cudaError_t e) { return e == cudaSuccess ? CARAT_OK : CARAT_ERR_CUDA; }
+
+}  // namespace
+}  // namespace carat
+
+using namespace carat;
+
+extern "C" {
+
+const char *carat_status_string(carat_status status) {
+    switch (status) {
+        case CARAT_OK: return "ok";
+        case CARAT_ERR_INVALID_ARG: return "invalid argument";
+        case CARAT_ERR_UNSUPPORTED: return "unsupported size";
+        case CARAT_ERR_WORKSPACE: return "workspace missing or too small";
+        case CARAT_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+int carat_abi_version(void) { return CARAT_ABI_VERSION; }
+
+uint64_t carat_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+size_t carat_swa_workspace_bytes(int batch, int proposal_count, int q_heads, int kv_heads,
+                                 int head_dim, int window) {
+    if (!attention_shape_ok(batch, proposal_count, q_heads, kv_heads, head_dim) || window < 1 ||
+        proposal_count > window)
+        return 0;
+    if (attention_unsupported(proposal_count, q_heads, kv_heads, head_dim) != CARAT_OK) return 0;
+    if (batch == 0) return 0;
+    return swa_plan(batch, proposal_count, q_heads, kv_heads, head_dim, window).total;
+}
+
+size_t carat_global_workspace_bytes(int batch, int proposal_count, int q_heads, int kv_heads,
+                                    int head_dim, int capacity) {
+    if (!attention_shape_ok(batch, proposal_count, q_heads, kv_heads, head_dim) ||
+        capacity < proposal_count)
+        return 0;
+    if (attention_unsupported(proposal_count, q_heads, kv_heads, head_dim) != CARAT_OK) return 0;
+    if (batch == 0) return 0;
+    return global_plan(batch, proposal_count, q_heads, kv_heads, head_dim, capacity).total;
+}
+
+carat_status carat_ring_append(void *k_ring, void *v_ring, int num_rings, const int32_t *ring_ids,
+                               const void *k_new, const void *v_new,
+                               const int32_t *context_lengths, int proposal_count,
+                               void *displaced, int batch, int kv_heads, int head_dim, int window,
+                               void *stream) {
+    if (batch < 0 || kv_heads < 1 || head_dim < 1 || window < 1 || proposal_count < 1 ||
+        proposal_count > window || num_rings < 1)
+        return CARAT_ERR_INVALID_ARG;
+    if (((long long)kv_heads * head_dim * 2) % 16 != 0) return CARAT_ERR_INVALID_ARG;
+    if (displaced && proposal_count > kMaxProposals) return CARAT_ERR_INVALID_ARG;
+    if (!ring_ids && num_rings < batch) return CARAT_ERR_INVALID_ARG;
+    if (batch == 0) return CARAT_OK;
+    if (!k_ring || !v_ring || !k_new || !v_new || !context_lengths) return CARAT_ERR_INVALID_ARG;
+    if (!aligned16(k_ring) || !aligned16(v_ring) || !aligned16(k_new) || !aligned16(v_new) ||
+        (displaced && !aligned16(displaced)))
+        return CARAT_ERR_INVALID_ARG;
+    AppendParams p{};
+    p.k_ring = static_cast<uint16_t *>(k_ring);
+    p.v_ring = static_cast<uint16_t *>(v_ring);
+    p.ids = ring_ids;
+    p.k_new = static_cast<const uint16_t *>(k_new);
+    p.v_new = static_cast<const uint16_t *>(v_new);
+    p.context_lengths = context_lengths;
+    p.displaced = (proposal_count > 1) ? static_cast<uint16_t *>(displaced) : nullptr;
+    p.dev_status = device_status_ptr();
+    p.num_ids = num_rings;
+    p.batch = batch;
+    p.k = proposal_count;
+    p.kv_heads = kv_heads;
+    p.head_dim = head_dim;
+    p.window = window;
+    return launch_status(launch_ring_append(p, static_cast<cudaStream_t>(stream)));
+}
+
+static carat_status check_attention_common(float *out, const void *queries, const void *k_base,
+                                           const void *v_base, int num_ids, const int32_t *ids,
+                                           const int32_t *context_lengths, int batch) {
+    if (num_ids < 1 || (!ids && num_ids < batch)) return CARAT_ERR_INVALID_ARG;
+    if (!out || !queries || !k_base || !v_base || !context_lengths) return CARAT_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(queries) || !aligned16(k_base) || !aligned16(v_base))
+        return CARAT_ERR_INVALID_ARG;
+    return CARAT_OK;
+}
+
+carat_status carat_swa_attention(float *out, const void *queries, const void *k_ring,
+                                 const void *v_ring, int num_rings, const int32_t *ring_ids,
+                                 const void *displaced, const int32_t *context_lengths,
+                                 int proposal_count, int batch, int q_heads, int kv_heads,
+                                 int head_dim, int window, float scale, void *workspace,
+                                 size_t workspace_bytes, void *stream) {
+    if (!attention_shape_ok(batch, proposal_count, q_heads, kv_heads, head_dim) || window < 1 ||
+        proposal_count > window || !std::isfinite(scale))
+        return CARAT_ERR_INVALID_ARG;
+    carat_status st = attention_unsupported(proposal_count, q_heads, kv_heads, head_dim);
+    if (st != CARAT_OK) return st;
+    if (batch == 0) return CARAT_OK;
+    st = check_attention_common(out, queries, k_ring, v_ring, num_rings, ring_ids, context_lengths,
+                                batch);
+    if (st != CARAT_OK) return st;
+    if (proposal_count > 1 && (!displaced || !aligned16(displaced))) return CARAT_ERR_INVALID_ARG;
+    const SplitPlan plan = swa_plan(batch, proposal_count, q_heads, kv_heads, head_dim, window);
+    if (!workspace || workspace_bytes < plan.total || !aligned16(workspace))
+        return CARAT_ERR_WORKSPACE;
+
+    AttnParams p{};
+    p.q = static_cast<const uint16_t *>(queries);
+    p.k_base = static_cast<const uint16_t *>(k_ring);
+    p.v_base = static_cast<const uint16_t *>(v_ring);
+    p.ids = ring_ids;
+    p.displaced = proposal_count > 1 ? static_cast<const uint16_t *>(displaced) : nullptr;
+    p.context_lengths = context_lengths;
+    p.out = out;
+    p.part_ml = static_cast<float2 *>(workspace);
+    p.part_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.ml_bytes);
+    p.dev_status = device_status_ptr();
+    p.num_ids = num_rings;
+    p.batch = batch;
+    p.k = proposal_count;
+    p.q_heads = q_heads;
+    p.kv_heads = kv_heads;
+    p.head_dim = head_dim;
+    p.group = q_heads / kv_heads;
+    p.rows = p.group * proposal_count;
+    p.window = window;
+    p.capacity = 0;
+    p.chunk = plan.chunk;
+    p.nchunks = plan.nchunks;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.source = KeySource::kRing;
+    return launch_status(launch_attention_simt(p, static_cast<cudaStream_t>(stream)));
+}
+
+carat_status carat_global_verify_attention(float *out, const void *queries, const void *key_cache,
+                                           const void *value_cache, int num_caches,
+                                           const int32_t *cache_ids,
+                                           const int32_t *context_lengths, int proposal_count,
+                                           int batch, int q_heads, int kv_heads, int head_dim,
+                                           int capacity, float scale, void *workspace,
+                                           size_t workspace_bytes, void *stream) {
+    if (!attention_shape_ok(batch, proposal_count, q_heads, kv_heads, head_dim) ||
+        capacity < proposal_count || !std::isfinite(scale))
+        return CARAT_ERR_INVALID_ARG;
+    carat_status st = attention_unsupported(proposal_count, q_heads, kv_heads, head_dim);
+    if (st != CARAT_OK) return st;
+    if (batch == 0) return CARAT_OK;
+    st = check_attention_common(out, queries, key_cache, value_cache, num_caches, cache_ids,
+                                context_lengths, batch);
+    if (st != CARAT_OK) return st;
+    const SplitPlan plan = global_plan(batch, proposal_count, q_heads, kv_heads, head_dim, capacity);
+    if (!workspace || workspace_bytes < plan.total || !aligned16(workspace))
+        return CARAT_ERR_WORKSPACE;
+
+    AttnParams p{};
+    p.q = static_cast<const uint16_t *>(queries);
+    p.k_base = static_cast<const uint16_t *>(key_cache);
+    p.v_base = static_cast<const uint16_t *>(value_cache);
+    p.ids = cache_ids;
+    p.displaced = nullptr;
+    p.context_lengths = context_lengths;
+    p.out = out;
+    p.part_ml = static_cast<float2 *>(workspace);
+    p.part_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.ml_bytes);
+    p.dev_status = device_status_ptr();
+    p.num_ids = num_caches;
+    p.batch = batch;
+    p.k = proposal_count;
+    p.q_heads = q_heads;
+    p.kv_heads = kv_heads;
+    p.head_dim = head_dim;
+    p.group = q_heads / kv_heads;
+    p.rows = p.group * proposal_count;
+    p.window = 0;
+    p.capacity = capacity;
+    p.chunk = plan.chunk;
+    p.nchunks = plan.nchunks;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.source = KeySource::kLinear;
+    return launch_status(launch_attention_simt(p, static_cast<cudaStream_t>(stream)));
+}
+
+carat_status carat_get_device_status(int32_t *host_out, int clear, void *stream) {
+    if (!host_out) return CARAT_ERR_INVALID_ARG;
+    int *ptr = device_status_ptr();
+    if (!ptr) return CARAT_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t value = 0;
+    if (cudaMemcpyAsync(&value, ptr, sizeof(value), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return CARAT_ERR_CUDA;
+    if (clear && cudaMemsetAsync(ptr, 0, sizeof(int), s) != cudaSuccess) return CARAT_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return CARAT_ERR_CUDA;
+    *host_out = value;
+    return CARAT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,129 @@
+// carat_internal.cuh -- definitions shared by the CUDA translation units of
+// libcarat.so (never installed, never seen by callers).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/carat.h"
+
+namespace carat {
+
+constexpr int kMaxProposals = CARAT_MAX_PROPOSALS;
+constexpr int kMaxTileRows = CARAT_MAX_TILE_ROWS;
+
+// Where the keys of one (request, KV head) come from.
+enum class KeySource : int {
+    kRing = 0,    // sliding layer: `window` ring slots + (proposal_count - 1) displaced rows
+    kLinear = 1,  // global layer: cache row t holds position t, t < key_count
+};
+
+// Everything an attention launch needs; passed by value as a kernel argument.
+struct AttnParams {
+    const uint16_t *q;          // [B][k][Hq][D]
+    const uint16_t *k_base;     // ring or cache, [num][rows][Hkv][D]
+    const uint16_t *v_base;
+    const int32_t *ids;         // ring/cache id per request, or nullptr
+    const uint16_t *displaced;  // [B][k-1][2][Hkv][D] (ring source, k > 1)
+    const int32_t *context_lengths;
+    float *out;                 // [B][k][Hq][D]
+    float2 *part_ml;            // [B][Hkv][nchunks][rows] (running max, sum) in log2 units
+    float *part_o;              // [B][Hkv][nchunks][rows][D] unnormalised
+    int *dev_status;
+    int num_ids;                // rings / caches available
+    int batch, k, q_heads, kv_heads, head_dim, group, rows;
+    int window;                 // ring slots (kRing) -- positions older than p-window+1 hidden
+    int capacity;               // cache rows (kLinear)
+    int chunk;                  // keys per split
+    int nchunks;                // splits per (request, KV head)
+    float scale_log2;           // softmax scale * log2(e)
+    KeySource source;
+};
+
+struct AppendParams {
+    uint16_t *k_ring, *v_ring;
+    const int32_t *ids;
+    const uint16_t *k_new, *v_new;
+    const int32_t *context_lengths;
+    uint16_t *displaced;
+    int *dev_status;
+    int num_ids, batch, k, kv_heads, head_dim, window;
+};
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+
+// bf16 pair packed in a 32-bit word -> two fp32 values (exact: a bf16 is the
+// upper half of an fp32).
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// 2^x with the SFU instruction (about 2 ulp); inputs <= 0 here, -inf -> 0.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// L2 policy that marks lines for early eviction (K/V rows are read once).
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 16-byte global load, no L1 allocation, with an L2 eviction-priority hint.
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p, uint64_t pol) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p), "l"(pol));
+    return r;
+}
+
+__device__ __forceinline__ void set_status(int *status, int bits) {
+    if (status) atomicOr(status, bits);
+}
+
+// Resolve request b: its cache/ring id and context length; false (and a
+// status bit) when either is out of range.
+__device__ __forceinline__ bool request_ok(const AttnParams &p, int b, int *id_out,
+                                           long long *ctx_out) {
+    long long ctx = p.context_lengths[b];
+    int id = p.ids ? p.ids[b] : b;
+    bool ok = true;
+    if (ctx < 0 || (p.source == KeySource::kLinear && ctx + p.k > p.capacity)) ok = false;
+    if (id < 0 || id >= p.num_ids) ok = false;
+    *id_out = id;
+    *ctx_out = ctx;
+    return ok;
+}
+
+// CARAT_DEV_* bits describing why request_ok rejected a request.
+__device__ __forceinline__ int request_error_bits(const AttnParams &p, int id, long long ctx) {
+    int bits = 0;
+    if (ctx < 0 || (p.source == KeySource::kLinear && ctx + p.k > p.capacity))
+        bits |= CARAT_DEV_BAD_CONTEXT;
+    if (id < 0 || id >= p.num_ids) bits |= CARAT_DEV_BAD_CACHE_ID;
+    return bits;
+}
+
+// Number of key slots scanned per (request, KV head).
+__host__ __device__ __forceinline__ long long keys_scanned(KeySource src, int window, int k,
+                                                          long long key_count) {
+    return src == KeySource::kRing ? (long long)window + (k - 1) : key_count;
+}
+
+// Host-side count of kernel launches (carat_kernel_launches).
+void count_launches(int n);
+
+// ---------------------------------------------------------------------------
+// Host-side launchers (defined in the .cu files)
+// ---------------------------------------------------------------------------
+cudaError_t launch_ring_append(const AppendParams &p, cudaStream_t stream);
+cudaError_t launch_attention_simt(const AttnParams &p, cudaStream_t stream);
+
+}  // namespace carat

@@ -1,0 +1,71 @@
+// ring_append.cu -- write a step's new K/V rows into per-request rings.
+//
+// Slot of position t = t mod window ("Announcing Carat: An inference engine
+// designed for Gemma 4", "Replacing page lookups with a ring buffer"); K and
+// V rows are written by the same thread in the same order, so both rings
+// keep one rotation ("Improving Decode Throughput on Intel Gaudi 3", "Our
+// approach").
+//
+// One CTA per (new token j, request b).  Each thread moves 16-byte chunks of
+// the token's [kv_heads][head_dim] row.  When `displaced` is given, the old
+// row in the slot that token j >= 1 overwrites is copied out first by the
+// same thread that then overwrites it, so the read precedes the write in
+// program order and no other thread touches those bytes.
+#include "carat_internal.cuh"
+
+namespace carat {
+
+__global__ void __launch_bounds__(256) ring_append_kernel(const AppendParams p) {
+    const int j = blockIdx.x;
+    const int b = blockIdx.y;
+    const long long ctx = p.context_lengths[b];
+    const int id = p.ids ? p.ids[b] : b;
+    if (ctx < 0 || id < 0 || id >= p.num_ids) {
+        if (threadIdx.x == 0 && j == 0)
+            set_status(p.dev_status, ctx < 0 ? CARAT_DEV_BAD_CONTEXT : CARAT_DEV_BAD_CACHE_ID);
+        return;
+    }
+    const long long t = ctx + j;                 // absolute position of new token j
+    const long long slot = t % p.window;
+    const size_t row_elems = (size_t)p.kv_heads * p.head_dim;
+    const int chunks = (int)(row_elems * 2 / 16);
+
+    uint4 *kdst = reinterpret_cast<uint4 *>(p.k_ring + ((size_t)id * p.window + slot) * row_elems);
+    uint4 *vdst = reinterpret_cast<uint4 *>(p.v_ring + ((size_t)id * p.window + slot) * row_elems);
+    const uint4 *ksrc =
+        reinterpret_cast<const uint4 *>(p.k_new + ((size_t)b * p.k + j) * row_elems);
+    const uint4 *vsrc =
+        reinterpret_cast<const uint4 *>(p.v_new + ((size_t)b * p.k + j) * row_elems);
+
+    // Old occupant of this slot: position t - window.  Token j >= 1 displaces a
+    // row that query 0 .. j-1 of this step still needs, if it exists.
+    const bool save = p.displaced != nullptr && j >= 1 && t - p.window >= 0;
+    uint4 *ddst = nullptr;
+    if (save)
+        ddst = reinterpret_cast<uint4 *>(p.displaced +
+                                         (((size_t)b * (p.k - 1) + (j - 1)) * 2) * row_elems);
+
+    for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+        uint4 kn = ksrc[c];
+        uint4 vn = vsrc[c];
+        if (save) {
+            uint4 ko = kdst[c];
+            uint4 vo = vdst[c];
+            ddst[c] = ko;
+            ddst[chunks + c] = vo;
+        }
+        kdst[c] = kn;
+        vdst[c] = vn;
+    }
+}
+
+cudaError_t launch_ring_append(const AppendParams &p, cudaStream_t stream) {
+    const int chunks = p.kv_heads * p.head_dim * 2 / 16;
+    int threads = chunks < 256 ? ((chunks + 31) / 32) * 32 : 256;
+    dim3 grid(p.k, p.batch);
+    ring_append_kernel<<<grid, threads, 0, stream>>>(p);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace carat

@@ -1,0 +1,189 @@
+"""Per-layer device state and the decode / verify step above the C ABI.
+
+``SlidingLayer`` owns one layer's K and V rings (one ring of ``window`` slots per
+request), the displaced-row buffer and the attention workspace; ``GlobalLayer``
+owns a full cache per request.  ``step()`` is the per-layer hot path: append this
+step's K/V rows, then attend (the order the pages give: the new token's KV is
+written, then attention reads the rotated rings in place).  All compute runs
+in libcarat.so; torch only allocates device memory and supplies the stream.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from . import carat, synth
+
+
+def _bf16_tensor(bits: np.ndarray, device) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.view(torch.bfloat16).to(device)
+
+
+def _i32(values, device) -> torch.Tensor:
+    return torch.as_tensor(np.asarray(values, dtype=np.int32), device=device)
+
+
+class SlidingLayer:
+    """K/V rings of one sliding-window layer."""
+
+    def __init__(self, num_rings: int, *, window: int = 1024, q_heads: int = 16,
+                 kv_heads: int = 8, head_dim: int = 256, max_batch: int | None = None,
+                 max_proposals: int = 1, scale: float | None = None, device="cuda",
+                 fill: float | None = 0.0):
+        self.window, self.q_heads, self.kv_heads, self.head_dim = window, q_heads, kv_heads, head_dim
+        self.max_batch = max_batch or num_rings
+        self.max_proposals = max_proposals
+        self.scale = (1.0 / math.sqrt(head_dim)) if scale is None else scale
+        self.device = torch.device(device)
+        shape = (num_rings, window, kv_heads, head_dim)
+        self.k_ring = torch.empty(shape, dtype=torch.bfloat16, device=self.device)
+        self.v_ring = torch.empty(shape, dtype=torch.bfloat16, device=self.device)
+        if fill is not None:
+            self.k_ring.fill_(fill)
+            self.v_ring.fill_(fill)
+        self.displaced = torch.zeros((self.max_batch, max(max_proposals - 1, 1), 2, kv_heads,
+                                      head_dim), dtype=torch.bfloat16, device=self.device)
+        self.workspace = carat.workspace_tensor(
+            max(carat.swa_workspace_bytes(self.max_batch, p, q_heads, kv_heads, head_dim, window)
+                for p in range(1, max_proposals + 1)), self.device)
+
+    def append(self, k_new, v_new, context_lengths, ring_ids=None, save_displaced=True,
+               stream=None):
+        k = k_new.shape[1]
+        disp = self.displaced if (save_displaced and k > 1) else None
+        carat.carat_ring_append(self.k_ring, self.v_ring, k_new, v_new, context_lengths,
+                                ring_ids=ring_ids, displaced=disp, window=self.window,
+                                stream=stream)
+
+    def attend(self, queries, context_lengths, ring_ids=None, out=None, stream=None):
+        if out is None:
+            out = torch.empty(queries.shape, dtype=torch.float32, device=self.device)
+        carat.carat_swa_attention(out, queries, self.k_ring, self.v_ring, context_lengths,
+                                  scale=self.scale, workspace=self.workspace, ring_ids=ring_ids,
+                                  displaced=self.displaced, stream=stream)
+        return out
+
+    def step(self, queries, k_new, v_new, context_lengths, ring_ids=None, out=None, stream=None):
+        self.append(k_new, v_new, context_lengths, ring_ids=ring_ids, stream=stream)
+        return self.attend(queries, context_lengths, ring_ids=ring_ids, out=out, stream=stream)
+
+
+class GlobalLayer:
+    """Full K/V cache of one global layer (zero-initialised, rows past the key
+    count stay zero and are masked)."""
+
+    def __init__(self, num_caches: int, *, capacity: int, q_heads: int = 16, kv_heads: int = 2,
+                 head_dim: int = 512, max_batch: int | None = None, max_proposals: int = 4,
+                 scale: float | None = None, device="cuda", fill: float | None = 0.0):
+        self.capacity, self.q_heads, self.kv_heads, self.head_dim = capacity, q_heads, kv_heads, head_dim
+        self.max_batch = max_batch or num_caches
+        self.scale = (1.0 / math.sqrt(head_dim)) if scale is None else scale
+        self.device = torch.device(device)
+        shape = (num_caches, capacity, kv_heads, head_dim)
+        self.key_cache = torch.empty(shape, dtype=torch.bfloat16, device=self.device)
+        self.value_cache = torch.empty(shape, dtype=torch.bfloat16, device=self.device)
+        if fill is not None:
+            self.key_cache.fill_(fill)
+            self.value_cache.fill_(fill)
+        self.workspace = carat.workspace_tensor(
+            max(carat.global_workspace_bytes(self.max_batch, p, q_heads, kv_heads, head_dim,
+                                             capacity)
+                for p in range(1, max_proposals + 1)), self.device)
+
+    def append(self, k_new, v_new, context_lengths, cache_ids=None, stream=None):
+        carat.carat_ring_append(self.key_cache, self.value_cache, k_new, v_new, context_lengths,
+                                ring_ids=cache_ids, window=self.capacity, stream=stream)
+
+    def attend(self, queries, context_lengths, cache_ids=None, out=None, stream=None):
+        if out is None:
+            out = torch.empty(queries.shape, dtype=torch.float32, device=self.device)
+        carat.carat_global_verify_attention(out, queries, self.key_cache, self.value_cache,
+                                            context_lengths, scale=self.scale,
+                                            workspace=self.workspace, cache_ids=cache_ids,
+                                            stream=stream)
+        return out
+
+    def step(self, queries, k_new, v_new, context_lengths, cache_ids=None, out=None, stream=None):
+        self.append(k_new, v_new, context_lengths, cache_ids=cache_ids, stream=stream)
+        return self.attend(queries, context_lengths, cache_ids=cache_ids, out=out, stream=stream)
+
+
+# ---------------------------------------------------------------------------
+# Staging a synthetic workload: history written through the library's own
+# append (in the pages' terms, the prompt's KV written after prefill), then
+# the step's inputs.
+# ---------------------------------------------------------------------------
+
+class StepInputs:
+    """Device tensors for one step of one layer, plus the host arrays."""
+
+    def __init__(self, queries, k_new, v_new, context_lengths, host):
+        self.queries, self.k_new, self.v_new = queries, k_new, v_new
+        self.context_lengths = context_lengths
+        self.host = host
+
+
+def _prefill(layer_append, k_rows, v_rows, first_position, b, device, window):
+    """Write history rows [first_position, first_position + n) of request b,
+    at most `window` rows per call."""
+    n = k_rows.shape[0]
+    done = 0
+    while done < n:
+        cnt = min(window, n - done)
+        kt = _bf16_tensor(k_rows[done:done + cnt], device).unsqueeze(0)
+        vt = _bf16_tensor(v_rows[done:done + cnt], device).unsqueeze(0)
+        layer_append(kt, vt, _i32([first_position + done], device), _i32([b], device))
+        done += cnt
+
+
+def stage_sliding(w: synth.Workload, layer_index: int, layer: SlidingLayer, requests=None):
+    """Fill each request's ring with the `window` positions before its context
+    length and return the step's inputs.  Request b uses ring b."""
+    dev = layer.device
+    B, k = w.batch, w.proposal_count
+    ctx = w.context_lengths
+    q_all = np.zeros((B, k, w.q_heads, w.head_dim), np.uint16)
+    kn = np.zeros((B, k, w.kv_heads, w.head_dim), np.uint16)
+    vn = np.zeros_like(kn)
+    hist = {}
+    for b in range(B) if requests is None else requests:
+        first, kh, vh = synth.last_rows(w, layer_index, b, w.window + k)
+        n_old = int(ctx[b]) - first
+        if n_old > 0:
+            _prefill(lambda kt, vt, c, r: layer.append(kt, vt, c, ring_ids=r, save_displaced=False),
+                     kh[:n_old], vh[:n_old], first, b, dev, w.window)
+        kn[b], vn[b] = kh[n_old:n_old + k], vh[n_old:n_old + k]
+        q_all[b] = synth.queries(w, layer_index, b)
+        hist[b] = (first, kh, vh)
+    inputs = StepInputs(_bf16_tensor(q_all, dev), _bf16_tensor(kn, dev), _bf16_tensor(vn, dev),
+                        _i32(ctx, dev), {"q": q_all, "k_new": kn, "v_new": vn, "hist": hist})
+    return inputs
+
+
+def stage_global(w: synth.Workload, layer_index: int, layer: GlobalLayer, requests=None,
+                 keep_history=True):
+    """Fill each request's cache rows [0, context_length) and return the step's
+    inputs.  Request b uses cache b."""
+    dev = layer.device
+    B, k = w.batch, w.proposal_count
+    ctx = w.context_lengths
+    q_all = np.zeros((B, k, w.q_heads, w.head_dim), np.uint16)
+    kn = np.zeros((B, k, w.kv_heads, w.head_dim), np.uint16)
+    vn = np.zeros_like(kn)
+    hist = {}
+    for b in range(B) if requests is None else requests:
+        kh = synth.history(w, layer_index, b, 0, int(w.key_counts[b]), "k")
+        vh = synth.history(w, layer_index, b, 0, int(w.key_counts[b]), "v")
+        n_old = int(ctx[b])
+        if n_old > 0:
+            _prefill(lambda kt, vt, c, r: layer.append(kt, vt, c, cache_ids=r),
+                     kh[:n_old], vh[:n_old], 0, b, dev, layer.capacity)
+        kn[b], vn[b] = kh[n_old:n_old + k], vh[n_old:n_old + k]
+        q_all[b] = synth.queries(w, layer_index, b)
+        if keep_history:
+            hist[b] = (0, kh, vh)
+    return StepInputs(_bf16_tensor(q_all, dev), _bf16_tensor(kn, dev), _bf16_tensor(vn, dev),
+                      _i32(ctx, dev), {"q": q_all, "k_new": kn, "v_new": vn, "hist": hist})

@@ -1,0 +1,155 @@
+"""The C ABI on the host (CPU only, no GPU needed).
+
+Loads libcarat.so, checks that it exports every function include/carat.h
+declares, and exercises the host-side argument checks: every call here fails
+validation, which happens before any CUDA call, so nothing touches a device.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "carat.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sliding_window_gqa_ring_gb300 import build, carat
+    if not os.path.exists(carat.LIBRARY):
+        build.build()
+    return carat.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(carat_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_three_entry_points():
+    names = declared_functions()
+    for n in ("carat_ring_append", "carat_swa_attention", "carat_global_verify_attention"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from sliding_window_gqa_ring_gb300 import carat
+    names = declared_functions()
+    assert set(carat.EXPORTED) <= set(names) | {"carat_abi_version"}
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in carat.h but not exported"
+
+
+def test_abi_version(lib):
+    assert lib.carat_abi_version() == 1
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert lib.carat_status_string(code)
+    assert lib.carat_status_string(99) == b"unknown status"
+
+
+def test_workspace_queries(lib):
+    assert lib.carat_swa_workspace_bytes(56, 1, 16, 8, 256, 1024) > 0
+    assert lib.carat_global_workspace_bytes(8, 15, 16, 2, 512, 32768) > 0
+    assert lib.carat_swa_workspace_bytes(0, 1, 16, 8, 256, 1024) == 0
+    assert lib.carat_swa_workspace_bytes(1, 1, 16, 8, 128, 1024) == 0       # unsupported D
+    assert lib.carat_global_workspace_bytes(1, 17, 16, 2, 512, 1024) == 0   # too many proposals
+    assert lib.carat_global_workspace_bytes(1, 16, 16, 1, 512, 1024) == 0   # 256 rows > 128
+    # monotone in batch
+    a = lib.carat_global_workspace_bytes(4, 4, 16, 2, 512, 8192)
+    b = lib.carat_global_workspace_bytes(8, 4, 16, 2, 512, 8192)
+    assert b >= a
+
+
+FAKE = 0x10000          # aligned, never dereferenced: every call below fails validation
+MISALIGNED = 0x10008
+
+
+def _swa(lib, **kw):
+    a = dict(out=FAKE, q=FAKE, kr=FAKE, vr=FAKE, nr=4, ids=None, disp=FAKE, ctx=FAKE, k=1, B=4,
+             hq=16, hkv=8, d=256, w=1024, scale=0.0625, ws=FAKE, wsb=0, stream=None)
+    a.update(kw)
+    return lib.carat_swa_attention(a["out"], a["q"], a["kr"], a["vr"], a["nr"], a["ids"],
+                                   a["disp"], a["ctx"], a["k"], a["B"], a["hq"], a["hkv"], a["d"],
+                                   a["w"], a["scale"], a["ws"], a["wsb"], a["stream"])
+
+
+def _glob(lib, **kw):
+    a = dict(out=FAKE, q=FAKE, kc=FAKE, vc=FAKE, nc=4, ids=None, ctx=FAKE, k=4, B=4, hq=16, hkv=2,
+             d=512, cap=8192, scale=0.04, ws=FAKE, wsb=0, stream=None)
+    a.update(kw)
+    return lib.carat_global_verify_attention(a["out"], a["q"], a["kc"], a["vc"], a["nc"], a["ids"],
+                                             a["ctx"], a["k"], a["B"], a["hq"], a["hkv"], a["d"],
+                                             a["cap"], a["scale"], a["ws"], a["wsb"], a["stream"])
+
+
+def _app(lib, **kw):
+    a = dict(kr=FAKE, vr=FAKE, nr=4, ids=None, kn=FAKE, vn=FAKE, ctx=FAKE, k=1, disp=None, B=4,
+             hkv=8, d=256, w=1024, stream=None)
+    a.update(kw)
+    return lib.carat_ring_append(a["kr"], a["vr"], a["nr"], a["ids"], a["kn"], a["vn"], a["ctx"],
+                                 a["k"], a["disp"], a["B"], a["hkv"], a["d"], a["w"], a["stream"])
+
+
+def test_swa_argument_checks(lib):
+    from sliding_window_gqa_ring_gb300 import carat as c
+    assert _swa(lib, B=-1) == c.CARAT_ERR_INVALID_ARG
+    assert _swa(lib, out=None) == c.CARAT_ERR_INVALID_ARG
+    assert _swa(lib, q=MISALIGNED) == c.CARAT_ERR_INVALID_ARG
+    assert _swa(lib, hq=12, hkv=8) == c.CARAT_ERR_INVALID_ARG        # not a multiple
+    assert _swa(lib, d=128) == c.CARAT_ERR_UNSUPPORTED
+    assert _swa(lib, k=17) == c.CARAT_ERR_INVALID_ARG
+    assert _swa(lib, k=4, disp=None) == c.CARAT_ERR_INVALID_ARG       # k > 1 needs displaced
+    assert _swa(lib, k=5, w=4) == c.CARAT_ERR_INVALID_ARG             # k > window
+    assert _swa(lib, nr=2) == c.CARAT_ERR_INVALID_ARG                 # fewer rings than requests
+    assert _swa(lib, scale=float("nan")) == c.CARAT_ERR_INVALID_ARG
+    assert _swa(lib, hq=64, hkv=1, k=4) == c.CARAT_ERR_UNSUPPORTED    # 256 rows per tile
+    assert _swa(lib, wsb=16) == c.CARAT_ERR_WORKSPACE
+    assert _swa(lib, ws=None, wsb=1 << 30) == c.CARAT_ERR_WORKSPACE
+    assert _swa(lib, B=0) == c.CARAT_OK                               # empty batch: no launch
+
+
+def test_global_argument_checks(lib):
+    from sliding_window_gqa_ring_gb300 import carat as c
+    assert _glob(lib, cap=3) == c.CARAT_ERR_INVALID_ARG               # capacity < proposals
+    assert _glob(lib, kc=None) == c.CARAT_ERR_INVALID_ARG
+    assert _glob(lib, vc=MISALIGNED) == c.CARAT_ERR_INVALID_ARG
+    assert _glob(lib, d=64) == c.CARAT_ERR_UNSUPPORTED
+    assert _glob(lib, k=15, hq=32, hkv=2) == c.CARAT_ERR_UNSUPPORTED  # 240 rows
+    assert _glob(lib, wsb=1024) == c.CARAT_ERR_WORKSPACE
+    assert _glob(lib, B=0) == c.CARAT_OK
+
+
+def test_append_argument_checks(lib):
+    from sliding_window_gqa_ring_gb300 import carat as c
+    assert _app(lib, k=0) == c.CARAT_ERR_INVALID_ARG
+    assert _app(lib, k=1025) == c.CARAT_ERR_INVALID_ARG               # more rows than slots
+    assert _app(lib, k=17, disp=FAKE) == c.CARAT_ERR_INVALID_ARG
+    assert _app(lib, kn=MISALIGNED) == c.CARAT_ERR_INVALID_ARG
+    assert _app(lib, hkv=1, d=4) == c.CARAT_ERR_INVALID_ARG           # 8-byte rows
+    assert _app(lib, nr=0) == c.CARAT_ERR_INVALID_ARG
+    assert _app(lib, ctx=None) == c.CARAT_ERR_INVALID_ARG
+    assert _app(lib, B=0) == c.CARAT_OK
+
+
+def test_device_status_needs_output_pointer(lib):
+    from sliding_window_gqa_ring_gb300 import carat as c
+    assert lib.carat_get_device_status(None, 0, None) == c.CARAT_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    from sliding_window_gqa_ring_gb300 import carat
+    monkeypatch.setattr(carat, "LIBRARY", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(carat, "_lib", None)
+    with pytest.raises(carat.CaratError):
+        carat.library()
+
+
+def test_python_status_text_matches_library(lib):
+    from sliding_window_gqa_ring_gb300 import carat
+    for code in range(6):
+        assert carat.status_string(code) == lib.carat_status_string(code).decode()

@@ -1,0 +1,296 @@
+"""GPU parity: libcarat.so (through the C ABI) against the fp64 oracle.
+
+Ring slots and appended bytes are compared bit for bit; attention outputs with
+the tolerance in gpu_harness.  Every input comes from the seeded generators in
+``synth``; the oracle sees the linear history, the GPU the rings it built itself
+with carat_ring_append.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_harness import assert_close, bits
+from sliding_window_gqa_ring_gb300 import carat, engine, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    carat.library()
+    carat.carat_get_device_status(clear=True)
+    yield
+    assert carat.carat_get_device_status(clear=True) == 0
+
+
+def _run_sliding(orc, w, layer_index=0, requests=None, fill=0.0, check_ring=True):
+    layer = engine.SlidingLayer(w.batch, window=w.window, q_heads=w.q_heads, kv_heads=w.kv_heads,
+                                head_dim=w.head_dim, max_proposals=w.proposal_count,
+                                scale=w.scale, fill=fill)
+    inp = engine.stage_sliding(w, layer_index, layer, requests=requests)
+    out = layer.step(inp.queries, inp.k_new, inp.v_new, inp.context_lengths)
+    torch.cuda.synchronize()
+    out_h = out.cpu().numpy()
+    reqs = list(range(w.batch)) if requests is None else list(requests)
+    jobs = []
+    for b in reqs:
+        first, kh, vh = inp.host["hist"][b]
+        jobs.append((inp.host["q"][b], kh, vh, first, int(w.context_lengths[b]), w.window, w.scale))
+    refs = orc.attention_batch(jobs)
+    for b, ref in zip(reqs, refs):
+        assert_close(out_h[b], ref, f"{w.name} request {b}")
+    if check_ring:
+        k_ring, v_ring, disp = bits(layer.k_ring), bits(layer.v_ring), bits(layer.displaced)
+        for b in reqs:
+            first, kh, vh = inp.host["hist"][b]
+            kc = int(w.key_counts[b])
+            exp_k, valid = orc.ring_expected(kh, first, kc, w.window)
+            exp_v, _ = orc.ring_expected(vh, first, kc, w.window)
+            assert np.array_equal(k_ring[b][valid], exp_k[valid]), f"K ring bytes, request {b}"
+            assert np.array_equal(v_ring[b][valid], exp_v[valid]), f"V ring bytes, request {b}"
+            if w.proposal_count > 1:
+                exp_d, dvalid = orc.displaced_expected(kh, vh, first, int(w.context_lengths[b]),
+                                                       w.proposal_count, w.window)
+                assert np.array_equal(disp[b][:w.proposal_count - 1][dvalid], exp_d[dvalid]), \
+                    f"displaced bytes, request {b}"
+    return out_h
+
+
+def _run_global(orc, w, layer_index=0, requests=None, rows=None, fill=0.0):
+    layer = engine.GlobalLayer(w.batch, capacity=w.capacity, q_heads=w.q_heads,
+                               kv_heads=w.kv_heads, head_dim=w.head_dim,
+                               max_proposals=w.proposal_count, scale=w.scale, fill=fill)
+    inp = engine.stage_global(w, layer_index, layer, requests=requests)
+    out = layer.step(inp.queries, inp.k_new, inp.v_new, inp.context_lengths)
+    torch.cuda.synchronize()
+    out_h = out.cpu().numpy()
+    reqs = list(range(w.batch)) if requests is None else list(requests)
+    g = w.q_heads // w.kv_heads
+    if rows is None:
+        refs = orc.attention_batch([(inp.host["q"][b], inp.host["hist"][b][1],
+                                     inp.host["hist"][b][2], 0, int(w.context_lengths[b]), 0,
+                                     w.scale) for b in reqs])
+        for b, ref in zip(reqs, refs):
+            assert_close(out_h[b], ref, f"{w.name} request {b}")
+    else:
+        for b in reqs:
+            _, kh, vh = inp.host["hist"][b]
+            for (j, h) in rows:
+                j = min(j, w.proposal_count - 1)
+                ref = orc.attention_row(inp.host["q"][b][j, h], kh, vh, 0, h // g,
+                                        int(w.context_lengths[b]) + j, 0, w.scale)
+                assert_close(out_h[b, j, h], ref, f"{w.name} request {b} row ({j},{h})")
+    # appended rows landed at their positions, bit for bit
+    kc_h = bits(layer.key_cache)
+    for b in reqs:
+        ctx = int(w.context_lengths[b])
+        assert np.array_equal(kc_h[b, ctx:ctx + w.proposal_count], inp.host["k_new"][b])
+    return out_h
+
+
+# --- the five workloads ------------------------------------------------------
+
+def test_sliding_single_request_1500(orc):
+    _run_sliding(orc, synth.sliding_single())
+
+
+def test_sliding_batched_56(orc):
+    _run_sliding(orc, synth.sliding_batched())
+
+
+def test_global_single_6005(orc):
+    _run_global(orc, synth.global_single())
+
+
+@pytest.mark.parametrize("k", [4, 15])
+def test_global_sweep(orc, k):
+    w = synth.global_sweep(k)
+    rows = [(0, 0), (k - 1, 15), (k // 2, 7), (1, 8), (k - 1, 0), (0, 9)]
+    _run_global(orc, w, rows=rows)
+
+
+def test_mixed_step_sampled(orc):
+    sliding, glob = synth.mixed_step()
+    ctx = sliding.context_lengths
+    order = np.argsort(ctx)
+    sample = sorted({int(order[0]), int(order[1]), int(order[len(order) // 2]), int(order[-1]),
+                     int(np.argmin(np.abs(ctx - 1024))), 5})
+    for layer_index in range(sliding.layers):
+        _run_sliding(orc, sliding, layer_index=layer_index, requests=sample)
+    _run_global(orc, glob, requests=sample, rows=[(0, 0), (3, 15), (2, 6), (1, 9)])
+
+
+# --- edge cases ----------------------------------------------------------------
+
+SLIDING_EDGES = [
+    # (key counts, proposal_count, q_heads, kv_heads, head_dim)
+    ([1], 1, 16, 8, 256),                 # a single key
+    ([2, 3, 1023, 1024, 1025, 2048, 2049, 1500], 1, 16, 8, 256),
+    ([4, 5, 1027, 1028, 1029, 3000, 1024, 64], 4, 16, 8, 256),
+    ([15, 16, 17, 1038, 1039, 1040, 5000], 15, 2, 1, 256),
+    ([16, 1040, 1041, 4096], 16, 8, 8, 512),
+    ([300, 1024 + 63, 1024 + 65], 2, 16, 2, 512),
+]
+
+
+@pytest.mark.parametrize("case", range(len(SLIDING_EDGES)))
+def test_sliding_edges(orc, case):
+    kcs, k, hq, hkv, d = SLIDING_EDGES[case]
+    w = synth.small(f"swa_edge{case}", seed=2000 + case, batch=len(kcs), proposal_count=k,
+                    q_heads=hq, kv_heads=hkv, head_dim=d, key_counts=kcs, window=1024)
+    _run_sliding(orc, w, fill=float("nan"))
+
+
+GLOBAL_EDGES = [
+    ([1, 2, 63, 64, 65, 127, 128, 129], 1, 16, 2, 512, 256),
+    ([4, 6005, 6016, 6017, 5, 68], 4, 16, 2, 512, 8192),
+    ([15, 16, 200, 1000], 15, 16, 2, 512, 1024),
+    ([16, 17, 4096], 16, 8, 1, 256, 4096),
+    ([100, 257, 2049], 3, 4, 4, 256, 2049),
+]
+
+
+@pytest.mark.parametrize("case", range(len(GLOBAL_EDGES)))
+def test_global_edges(orc, case):
+    kcs, k, hq, hkv, d, cap = GLOBAL_EDGES[case]
+    w = synth.small(f"global_edge{case}", seed=3000 + case, batch=len(kcs), proposal_count=k,
+                    q_heads=hq, kv_heads=hkv, head_dim=d, key_counts=kcs, capacity=cap,
+                    outlier_fraction=0.01)
+    _run_global(orc, w, fill=float("nan"))
+
+
+def _probe_values(n_keys, d, marks):
+    """V rows marking chosen positions in chosen columns; K all zero so every
+    visible key gets the same weight and the output counts positions."""
+    v = np.zeros((n_keys, 1, d), dtype=np.float32)
+    for col, positions in marks.items():
+        for t in positions:
+            if 0 <= t < n_keys:
+                v[t, 0, col] = 1.0
+    v[:, 0, d - 1] = 1.0
+    return synth.bf16_bits(v)
+
+
+@pytest.mark.parametrize("key_count", [1500, 1024, 1025, 700, 3])
+@pytest.mark.parametrize("k", [1, 4])
+def test_sliding_window_probe(orc, key_count, k):
+    """Structured inputs that make a one-position window error large: all
+    scores equal, V columns flag the window's first position, the position just
+    before it and the query's own."""
+    if key_count < k:
+        pytest.skip("fewer keys than queries")
+    window, d = 1024, 256
+    ctx = key_count - k
+    marks = {0: [], 1: [], 2: []}
+    for j in range(k):
+        p = ctx + j
+        marks[0].append(max(0, p - window + 1))
+        marks[1].append(p - window)
+        marks[2].append(p)
+    v = _probe_values(key_count, d, marks)
+    kk = np.zeros_like(v)
+    layer = engine.SlidingLayer(1, window=window, q_heads=1, kv_heads=1, head_dim=d,
+                                max_proposals=k, fill=float("nan"))
+    first = max(0, ctx - window)
+    if ctx > first:
+        layer.append(engine._bf16_tensor(kk[first:ctx], "cuda").unsqueeze(0),
+                     engine._bf16_tensor(v[first:ctx], "cuda").unsqueeze(0),
+                     engine._i32([first], "cuda"), save_displaced=False)
+    q = np.zeros((1, k, 1, d), np.uint16)
+    out = layer.step(engine._bf16_tensor(q, "cuda"),
+                     engine._bf16_tensor(kk[ctx:], "cuda").unsqueeze(0),
+                     engine._bf16_tensor(v[ctx:], "cuda").unsqueeze(0),
+                     engine._i32([ctx], "cuda"))
+    torch.cuda.synchronize()
+    ref = orc.attention_request(q[0], kk, v, 0, ctx, window, layer.scale)
+    np.testing.assert_allclose(out.cpu().numpy()[0], ref, rtol=0, atol=1e-5)
+
+
+def test_global_tail_probe(orc):
+    """Key counts 6005 and 6016 (the pages' padding example): the cache tail is
+    NaN-filled and must not reach the result; V flags the last visible key."""
+    d, k = 512, 4
+    for kc in (6005, 6016, 6017):
+        ctx = kc - k
+        v = _probe_values(kc, d, {0: [kc - 1], 1: [ctx], 2: [0]})
+        kk = np.zeros_like(v)
+        layer = engine.GlobalLayer(1, capacity=8192, q_heads=8, kv_heads=1, head_dim=d,
+                                   max_proposals=k, fill=float("nan"))
+        layer.append(engine._bf16_tensor(kk[:ctx], "cuda").unsqueeze(0),
+                     engine._bf16_tensor(v[:ctx], "cuda").unsqueeze(0), engine._i32([0], "cuda"))
+        q = np.zeros((1, k, 8, d), np.uint16)
+        out = layer.step(engine._bf16_tensor(q, "cuda"),
+                         engine._bf16_tensor(kk[ctx:], "cuda").unsqueeze(0),
+                         engine._bf16_tensor(v[ctx:], "cuda").unsqueeze(0),
+                         engine._i32([ctx], "cuda"))
+        torch.cuda.synchronize()
+        ref = orc.attention_request(q[0], kk, v, 0, ctx, 0, layer.scale)
+        np.testing.assert_allclose(out.cpu().numpy()[0], ref, rtol=0, atol=1e-5)
+
+
+def test_bad_device_values_flagged():
+    """A negative context length or an out-of-range ring id on the device: the
+    request is skipped, its output is NaN, the status word says why, and the
+    other requests are still computed."""
+    w = synth.small("bad", seed=4000, batch=3, proposal_count=1, q_heads=16, kv_heads=8,
+                    head_dim=256, key_counts=[10, 20, 30], window=1024)
+    layer = engine.SlidingLayer(3, window=1024, max_proposals=1)
+    inp = engine.stage_sliding(w, 0, layer)
+    carat.carat_get_device_status(clear=True)
+    bad_ctx = torch.tensor([9, -5, 29], dtype=torch.int32, device="cuda")
+    out = layer.attend(inp.queries, bad_ctx)
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    assert np.isnan(o[1]).all() and np.isfinite(o[0]).all() and np.isfinite(o[2]).all()
+    assert carat.carat_get_device_status(clear=True) & carat.CARAT_DEV_BAD_CONTEXT
+    ids = torch.tensor([0, 7, 2], dtype=torch.int32, device="cuda")
+    out = layer.attend(inp.queries, inp.context_lengths, ring_ids=ids)
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    assert np.isnan(o[1]).all() and np.isfinite(o[0]).all()
+    assert carat.carat_get_device_status(clear=True) & carat.CARAT_DEV_BAD_CACHE_ID
+    glayer = engine.GlobalLayer(1, capacity=64, max_proposals=4)
+    q = torch.zeros((1, 4, 16, 512), dtype=torch.bfloat16, device="cuda")
+    out = glayer.attend(q, torch.tensor([61], dtype=torch.int32, device="cuda"))  # 65 > 64
+    torch.cuda.synchronize()
+    assert np.isnan(out.cpu().numpy()).all()
+    assert carat.carat_get_device_status(clear=True) & carat.CARAT_DEV_BAD_CONTEXT
+
+
+def test_ring_ids_indirection(orc):
+    """Requests mapped to rings in a shuffled order give the same outputs."""
+    w = synth.small("ids", seed=4100, batch=4, proposal_count=4, q_heads=16, kv_heads=8,
+                    head_dim=256, key_counts=[1030, 77, 4000, 1024], window=1024)
+    base = _run_sliding(orc, w)
+    layer = engine.SlidingLayer(6, window=1024, max_batch=4, max_proposals=4)
+    ids = [5, 0, 3, 1]
+    dev_ids = torch.tensor(ids, dtype=torch.int32, device="cuda")
+    k = w.proposal_count
+    q_all, kn, vn = [], [], []
+    for b in range(4):
+        first, kh, vh = synth.last_rows(w, 0, b, 1024 + k)
+        n_old = int(w.context_lengths[b]) - first
+        layer.append(engine._bf16_tensor(kh[:n_old], "cuda").unsqueeze(0),
+                     engine._bf16_tensor(vh[:n_old], "cuda").unsqueeze(0),
+                     engine._i32([first], "cuda"), ring_ids=dev_ids[b:b + 1],
+                     save_displaced=False)
+        kn.append(kh[n_old:n_old + k])
+        vn.append(vh[n_old:n_old + k])
+        q_all.append(synth.queries(w, 0, b))
+    out = layer.step(engine._bf16_tensor(np.stack(q_all), "cuda"),
+                     engine._bf16_tensor(np.stack(kn), "cuda"),
+                     engine._bf16_tensor(np.stack(vn), "cuda"),
+                     engine._i32(w.context_lengths, "cuda"), ring_ids=dev_ids)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out.cpu().numpy(), base)
+
+
+def test_batch_zero_is_noop():
+    layer = engine.SlidingLayer(1, window=1024, max_proposals=1)
+    q = torch.empty((0, 1, 16, 256), dtype=torch.bfloat16, device="cuda")
+    out = layer.attend(q, torch.empty((0,), dtype=torch.int32, device="cuda"))
+    assert out.shape[0] == 0
