@@ -9,7 +9,9 @@ in libcarat.so; torch only allocates device memory and supplies the stream.
 """
 from __future__ import annotations
 
+import concurrent.futures
 import math
+import os
 
 import numpy as np
 import torch
@@ -126,6 +128,13 @@ class StepInputs:
         self.host = host
 
 
+def _parallel(fn, items):
+    """fn over items on a thread pool (numpy's generators and array ops release
+    the GIL), results in order."""
+    with concurrent.futures.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as pool:
+        return list(pool.map(fn, items))
+
+
 def _prefill(layer_append, k_rows, v_rows, first_position, b, device, window):
     """Write history rows [first_position, first_position + n) of request b,
     at most `window` rows per call."""
@@ -149,8 +158,9 @@ def stage_sliding(w: synth.Workload, layer_index: int, layer: SlidingLayer, requ
     kn = np.zeros((B, k, w.kv_heads, w.head_dim), np.uint16)
     vn = np.zeros_like(kn)
     hist = {}
-    for b in range(B) if requests is None else requests:
-        first, kh, vh = synth.last_rows(w, layer_index, b, w.window + k)
+    reqs = list(range(B)) if requests is None else list(requests)
+    rows = _parallel(lambda b: synth.last_rows(w, layer_index, b, w.window + k), reqs)
+    for b, (first, kh, vh) in zip(reqs, rows):
         n_old = int(ctx[b]) - first
         if n_old > 0:
             _prefill(lambda kt, vt, c, r: layer.append(kt, vt, c, ring_ids=r, save_displaced=False),
@@ -174,9 +184,13 @@ def stage_global(w: synth.Workload, layer_index: int, layer: GlobalLayer, reques
     kn = np.zeros((B, k, w.kv_heads, w.head_dim), np.uint16)
     vn = np.zeros_like(kn)
     hist = {}
-    for b in range(B) if requests is None else requests:
-        kh = synth.history(w, layer_index, b, 0, int(w.key_counts[b]), "k")
-        vh = synth.history(w, layer_index, b, 0, int(w.key_counts[b]), "v")
+    reqs = list(range(B)) if requests is None else list(requests)
+
+    def gen(b):
+        return (synth.history(w, layer_index, b, 0, int(w.key_counts[b]), "k"),
+                synth.history(w, layer_index, b, 0, int(w.key_counts[b]), "v"))
+
+    for b, (kh, vh) in zip(reqs, _parallel(gen, reqs)):
         n_old = int(ctx[b])
         if n_old > 0:
             _prefill(lambda kt, vt, c, r: layer.append(kt, vt, c, cache_ids=r),
