@@ -189,6 +189,42 @@ carat_status carat_global_verify_attention(float *out, const void *queries,
                                            void *workspace, size_t workspace_bytes,
                                            void *stream);
 
+/*
+ * carat_swa_attention_noalloc -- carat_swa_attention without a workspace
+ * argument, for callers that cannot allocate device memory: for example a
+ * plugin running inside a host runtime that owns all GPU memory and gives its
+ * plugins no allocator, or a latency-critical loop that must not call
+ * cudaMalloc (which can synchronise the device).  The pages have no
+ * counterpart to this entry point; it exists only for such callers.
+ *
+ * The split-K scratch lives in a fixed device array of
+ * CARAT_NOALLOC_SCRATCH_BYTES (32 MiB) inside the library, which every GPU
+ * that loads the library keeps reserved until the process exits.  Arguments,
+ * layouts and results are those of carat_swa_attention.  Sizes whose
+ * carat_swa_workspace_bytes(...) exceeds the array return
+ * CARAT_ERR_WORKSPACE without launching anything (e.g. batch 64 with 4
+ * proposals needs about 12 MiB and fits; batch 64 with 16 proposals does not).
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any
+ * stream capture begins.  Every call uses the same array and nothing in it
+ * needs to start at zero, but calls that can run at the same time on the GPU
+ * (other streams or host threads without ordering between them) race on it:
+ * order them on one stream.  No device memory is allocated or freed.
+ */
+#define CARAT_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+carat_status carat_swa_attention_noalloc(float *out, const void *queries,
+                                         const void *k_ring, const void *v_ring,
+                                         int num_rings, const int32_t *ring_ids,
+                                         const void *displaced,
+                                         const int32_t *context_lengths, int proposal_count,
+                                         int batch, int q_heads, int kv_heads, int head_dim,
+                                         int window, float scale, void *stream);
+
+/* Size in bytes of the built-in scratch array used by
+ * carat_swa_attention_noalloc (CARAT_NOALLOC_SCRATCH_BYTES). */
+size_t carat_noalloc_scratch_bytes(void);
+
 /* Workspace bytes the two attention calls need for these sizes (0 if the
  * sizes are invalid).  Pure host arithmetic; no CUDA call. */
 size_t carat_swa_workspace_bytes(int batch, int proposal_count, int q_heads, int kv_heads,

@@ -38,6 +38,7 @@ EXPORTED = (
     "carat_ring_append", "carat_swa_attention", "carat_global_verify_attention",
     "carat_swa_workspace_bytes", "carat_global_workspace_bytes", "carat_get_device_status",
     "carat_status_string", "carat_abi_version", "carat_kernel_launches",
+    "carat_swa_attention_noalloc", "carat_noalloc_scratch_bytes",
 )
 
 
@@ -73,6 +74,11 @@ def _declare(lib):
     lib.carat_abi_version.argtypes = []
     lib.carat_kernel_launches.restype = ctypes.c_uint64
     lib.carat_kernel_launches.argtypes = []
+    lib.carat_swa_attention_noalloc.restype = i32
+    lib.carat_swa_attention_noalloc.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, i32, i32, i32,
+                                                i32, i32, i32, f32, vp]
+    lib.carat_noalloc_scratch_bytes.restype = sz
+    lib.carat_noalloc_scratch_bytes.argtypes = []
     return lib
 
 
@@ -175,6 +181,27 @@ def carat_swa_attention(out, queries, k_ring, v_ring, context_lengths, *, scale,
         _ptr(displaced), _ptr(context_lengths), k, batch, q_heads, kv_heads, head_dim, window,
         float(scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)), "carat_swa_attention")
+
+
+def carat_swa_attention_noalloc(out, queries, k_ring, v_ring, context_lengths, *, scale,
+                                ring_ids=None, displaced=None, stream=None):
+    """carat_swa_attention with the library's built-in scratch instead of a
+    workspace, for callers that cannot allocate device memory.  Raises
+    CaratError (CARAT_ERR_WORKSPACE) for sizes that need more scratch than
+    noalloc_scratch_bytes().  Calls that overlap on the GPU share the scratch
+    and race; order them on one stream."""
+    _expect(queries, torch.bfloat16, "queries")
+    _expect(out, torch.float32, "out")
+    batch, k, q_heads, head_dim = queries.shape
+    num_rings, window, kv_heads, _ = k_ring.shape
+    _check(library().carat_swa_attention_noalloc(
+        _ptr(out), _ptr(queries), _ptr(k_ring), _ptr(v_ring), num_rings, _ptr(ring_ids),
+        _ptr(displaced), _ptr(context_lengths), k, batch, q_heads, kv_heads, head_dim, window,
+        float(scale), _stream(stream)), "carat_swa_attention_noalloc")
+
+
+def noalloc_scratch_bytes() -> int:
+    return int(library().carat_noalloc_scratch_bytes())
 
 
 def carat_global_verify_attention(out, queries, key_cache, value_cache, context_lengths, *,

@@ -1,0 +1,78 @@
+"""The allocation-free sliding-window attention entry point.
+
+carat_swa_attention_noalloc serves callers that cannot allocate device memory
+(a plugin inside a runtime that owns all GPU memory, or a loop that must never
+call cudaMalloc): it uses a fixed scratch array inside the library instead of a
+caller workspace.  These tests call it through the C ABI and compare it with
+carat_swa_attention (the entry point that takes a workspace), on two calls in a
+row, since the second call finds the previous call's partial results still in
+the shared scratch.  This file is named to be collected last.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_harness import assert_close
+from sliding_window_gqa_ring_gb300 import carat, engine, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    carat.library()
+
+
+def _staged(w):
+    layer = engine.SlidingLayer(w.batch, window=w.window, q_heads=w.q_heads, kv_heads=w.kv_heads,
+                                head_dim=w.head_dim, max_proposals=w.proposal_count,
+                                scale=w.scale)
+    inp = engine.stage_sliding(w, 0, layer)
+    layer.append(inp.k_new, inp.v_new, inp.context_lengths)
+    return layer, inp
+
+
+@pytest.mark.parametrize("which", ["decode_b56", "verify_k4"])
+def test_noalloc_matches_workspace_entry_point(which):
+    if which == "decode_b56":
+        w = synth.sliding_batched()
+    else:
+        w = synth.small("noalloc_k4", seed=5100, batch=12, proposal_count=4, q_heads=16,
+                        kv_heads=8, head_dim=256, key_counts=[5, 700, 1023, 1024, 1027, 1028,
+                                                              2000, 4096, 9000, 64, 300, 1500],
+                        window=1024)
+    layer, inp = _staged(w)
+    need = carat.swa_workspace_bytes(w.batch, w.proposal_count, w.q_heads, w.kv_heads,
+                                     w.head_dim, w.window)
+    assert 0 < need <= carat.noalloc_scratch_bytes()
+    ref = layer.attend(inp.queries, inp.context_lengths)
+    outs = []
+    for _ in range(2):
+        out = torch.full(inp.queries.shape, float("nan"), dtype=torch.float32, device="cuda")
+        carat.carat_swa_attention_noalloc(out, inp.queries, layer.k_ring, layer.v_ring,
+                                          inp.context_lengths, scale=layer.scale,
+                                          displaced=layer.displaced)
+        outs.append(out)
+    torch.cuda.synchronize()
+    r = ref.cpu().numpy()
+    for out in outs:
+        assert_close(out.cpu().numpy(), r, f"noalloc {which}")
+    assert carat.carat_get_device_status(clear=True) == 0
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch():
+    # 64 requests x 16 proposals need ~48 MiB of scratch, more than the array.
+    need = carat.swa_workspace_bytes(64, 16, 16, 8, 256, 1024)
+    assert need > carat.noalloc_scratch_bytes()
+    q = torch.zeros((64, 16, 16, 256), dtype=torch.bfloat16, device="cuda")
+    ring = torch.zeros((64, 1024, 8, 256), dtype=torch.bfloat16, device="cuda")
+    disp = torch.zeros((64, 15, 2, 8, 256), dtype=torch.bfloat16, device="cuda")
+    ctx = torch.full((64,), 2000, dtype=torch.int32, device="cuda")
+    out = torch.empty((64, 16, 16, 256), dtype=torch.float32, device="cuda")
+    before = carat.kernel_launches()
+    with pytest.raises(carat.CaratError) as e:
+        carat.carat_swa_attention_noalloc(out, q, ring, ring, ctx, scale=0.0625, displaced=disp)
+    assert e.value.status == carat.CARAT_ERR_WORKSPACE
+    assert carat.kernel_launches() == before
