@@ -35,7 +35,7 @@ def sources() -> list[str]:
 
 def _compile(src: str, verbose: bool) -> str:
     obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-    deps = [src] + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh")]
+    deps = [src] + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     deps.append(os.path.join(INCLUDE, "carat.h"))
     if os.path.exists(obj) and all(os.path.getmtime(obj) >= os.path.getmtime(d) for d in deps):
         return obj
@@ -66,6 +66,28 @@ def build(verbose: bool = False) -> str:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIBRARY)
     return LIBRARY
+
+
+PROBE_SOURCE = os.path.join(os.path.dirname(HERE), "tests", "cuda", "tc_probe.cu")
+PROBE_LIBRARY = os.path.join(os.path.dirname(HERE), "tests", "cuda", "_build", "libtc_probe.so")
+
+
+def build_probe() -> str:
+    """Test-only library that checks the tensor-core primitives on a GPU."""
+    if not os.path.exists(PROBE_SOURCE):
+        return ""
+    os.makedirs(os.path.dirname(PROBE_LIBRARY), exist_ok=True)
+    deps = [PROBE_SOURCE] + [os.path.join(CSRC, f) for f in os.listdir(CSRC)
+                             if f.endswith((".cuh", ".h"))]
+    if os.path.exists(PROBE_LIBRARY) and all(os.path.getmtime(PROBE_LIBRARY) >= os.path.getmtime(d)
+                                             for d in deps):
+        return PROBE_LIBRARY
+    cmd = [nvcc(), *NVCC_FLAGS, "-shared", "-cudart", "shared", "-o", PROBE_LIBRARY,
+           PROBE_SOURCE, "-Xlinker", "-rpath", "-Xlinker", "/usr/local/cuda/lib64"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed for the probe:\n{r.stdout}\n{r.stderr}")
+    return PROBE_LIBRARY
 
 
 if __name__ == "__main__":
