@@ -71,6 +71,7 @@ typedef enum carat_status {
 /* Bits of the device status word. */
 #define CARAT_DEV_BAD_CONTEXT 0x1 /* context_length < 0, or key_count > capacity */
 #define CARAT_DEV_BAD_CACHE_ID 0x2 /* ring/cache id outside [0, num_rings) */
+#define CARAT_DEV_TIMEOUT 0x4      /* a kernel gave up waiting (bounded wait); results invalid */
 
 /* Largest proposal_count the attention entry points accept. */
 #define CARAT_MAX_PROPOSALS 16

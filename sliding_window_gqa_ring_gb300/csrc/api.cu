@@ -41,11 +41,10 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool supported_head_dim(int d) { return d == 256 || d == 512; }
 
-// Occupancy target for the split plan: CTAs wanted in flight.
-constexpr long long kTargetCtas = 8LL * 152;
-
 struct SplitPlan {
-    int chunk = 0;
+    bool tc = false;           // tensor-core kernel (else CUDA-core kernel)
+    int chunk = 0;             // keys per split
+    int tiles_per_chunk = 0;   // tensor-core path: 128-key tiles per split
     int nchunks = 0;
     size_t ml_bytes = 0;
     size_t o_bytes = 0;
@@ -54,25 +53,54 @@ struct SplitPlan {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Choose keys per split: the largest power of two in [64, 4096] that still
-// gives kTargetCtas CTAs over all (request, KV head) pairs.
-SplitPlan make_plan(long long pairs, long long keys, int rows, int head_dim) {
+void size_workspace(SplitPlan &p, long long pairs, int rows, int head_dim) {
+    const size_t parts = (size_t)pairs * p.nchunks * rows;
+    p.ml_bytes = align256(parts * sizeof(float2));
+    p.o_bytes = align256(parts * (size_t)head_dim * sizeof(float));
+    p.total = p.ml_bytes + p.o_bytes;
+}
+
+// CUDA-core path: the largest power-of-two chunk in [64, 4096] keys that still
+// gives about 8 CTAs per SM.
+SplitPlan simt_plan(long long pairs, long long keys, int rows, int head_dim) {
+    constexpr long long kTargetCtas = 8LL * 152;
     SplitPlan p;
     int chunk = 64;
     for (int c = 4096; c >= 64; c >>= 1) {
-        long long n = (keys + c - 1) / c;
-        if (pairs * n >= kTargetCtas) {
+        if (pairs * ((keys + c - 1) / c) >= kTargetCtas) {
             chunk = c;
             break;
         }
     }
     p.chunk = chunk;
     p.nchunks = (int)((keys + chunk - 1) / chunk);
-    const size_t parts = (size_t)pairs * p.nchunks * rows;
-    p.ml_bytes = align256(parts * sizeof(float2));
-    p.o_bytes = align256(parts * (size_t)head_dim * sizeof(float));
-    p.total = p.ml_bytes + p.o_bytes;
+    size_workspace(p, pairs, rows, head_dim);
     return p;
+}
+
+// Tensor-core path: 128-key tiles; a chunk is tiles_per_chunk tiles, chosen so
+// the grid holds about `target` CTAs when every request is as long as the
+// cache allows (ceil(total tiles / target), at most max_tpc).
+SplitPlan tc_plan(long long pairs, int row_groups, long long max_tiles, int rows, int head_dim,
+                  long long target, int max_tpc) {
+    SplitPlan p;
+    p.tc = true;
+    const long long total = pairs * row_groups * max_tiles;
+    long long tpc = (total + target - 1) / target;
+    if (tpc < 1) tpc = 1;
+    if (tpc > max_tpc) tpc = max_tpc;
+    p.tiles_per_chunk = (int)tpc;
+    p.chunk = (int)tpc * kTcTileKeys;
+    p.nchunks = (int)((max_tiles + tpc - 1) / tpc);
+    size_workspace(p, pairs, rows, head_dim);
+    return p;
+}
+
+int row_groups_for(int group, int k) {
+    const int n = tc_rows_per_tile(group, k);
+    int ppg = n / group;
+    if (ppg > k) ppg = k;
+    return (k + ppg - 1) / ppg;
 }
 
 bool attention_shape_ok(int batch, int proposal_count, int q_heads, int kv_heads, int head_dim) {
@@ -88,15 +116,36 @@ carat_status attention_unsupported(int proposal_count, int q_heads, int kv_heads
 
 SplitPlan swa_plan(int batch, int proposal_count, int q_heads, int kv_heads, int head_dim,
                    int window) {
-    const int rows = (q_heads / kv_heads) * proposal_count;
-    return make_plan((long long)batch * kv_heads,
-                     keys_scanned(KeySource::kRing, window, proposal_count, 0), rows, head_dim);
+    const int group = q_heads / kv_heads;
+    const int rows = group * proposal_count;
+    const long long pairs = (long long)batch * kv_heads;
+    if (tc_supported(head_dim, group, proposal_count)) {
+        const long long tiles = (window + kTcTileKeys - 1) / kTcTileKeys + (proposal_count > 1 ? 1 : 0);
+        return tc_plan(pairs, row_groups_for(group, proposal_count), tiles, rows, head_dim,
+                       4LL * 152, 4);
+    }
+    return simt_plan(pairs, keys_scanned(KeySource::kRing, window, proposal_count, 0), rows,
+                     head_dim);
 }
 
 SplitPlan global_plan(int batch, int proposal_count, int q_heads, int kv_heads, int head_dim,
                       int capacity) {
-    const int rows = (q_heads / kv_heads) * proposal_count;
-    return make_plan((long long)batch * kv_heads, capacity, rows, head_dim);
+    const int group = q_heads / kv_heads;
+    const int rows = group * proposal_count;
+    const long long pairs = (long long)batch * kv_heads;
+    if (tc_supported(head_dim, group, proposal_count)) {
+        const long long tiles = (capacity + kTcTileKeys - 1) / kTcTileKeys;
+        return tc_plan(pairs, row_groups_for(group, proposal_count), tiles, rows, head_dim,
+                       2LL * 152, 8);
+    }
+    return simt_plan(pairs, capacity, rows, head_dim);
+}
+
+cudaError_t launch_attention(const AttnParams &p, const SplitPlan &plan, cudaStream_t stream) {
+    cudaError_t e = plan.tc ? launch_attention_tc(p, plan.tiles_per_chunk, stream)
+                            : launch_attention_simt(p, stream);
+    if (e != cudaSuccess) return e;
+    return launch_combine(p, stream);
 }
 
 carat_status launch_status(cudaError_t e) { return e == cudaSuccess ? CARAT_OK : CARAT_ERR_CUDA; }
@@ -232,7 +281,7 @@ carat_status carat_swa_attention(float *out, const void *queries, const void *k_
     p.nchunks = plan.nchunks;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.source = KeySource::kRing;
-    return launch_status(launch_attention_simt(p, static_cast<cudaStream_t>(stream)));
+    return launch_status(launch_attention(p, plan, static_cast<cudaStream_t>(stream)));
 }
 
 carat_status carat_global_verify_attention(float *out, const void *queries, const void *key_cache,
@@ -280,7 +329,7 @@ carat_status carat_global_verify_attention(float *out, const void *queries, cons
     p.nchunks = plan.nchunks;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.source = KeySource::kLinear;
-    return launch_status(launch_attention_simt(p, static_cast<cudaStream_t>(stream)));
+    return launch_status(launch_attention(p, plan, static_cast<cudaStream_t>(stream)));
 }
 
 carat_status carat_get_device_status(int32_t *host_out, int clear, void *stream) {

@@ -233,51 +233,10 @@ __global__ void __launch_bounds__(kWarps * 32) attn_partial_simt(const AttnParam
     }
 }
 
-template <int D>
-__global__ void __launch_bounds__(128) attn_combine(const AttnParams p) {
-    const int r = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
-    const int j = r / p.group, hp = r % p.group;
-    float *orow = p.out + (((size_t)b * p.k + j) * p.q_heads + (size_t)c * p.group + hp) * D;
-    int id;
-    long long ctx;
-    if (!request_ok(p, b, &id, &ctx)) {
-        if (r == 0 && c == 0 && threadIdx.x == 0) set_status(p.dev_status, request_error_bits(p, id, ctx));
-        for (int d = threadIdx.x; d < D; d += blockDim.x) orow[d] = __int_as_float(0x7fc00000);
-        return;
-    }
-    const long long nkeys = keys_scanned(p.source, p.window, p.k, ctx + p.k);
-    const int nch = (int)((nkeys + p.chunk - 1) / p.chunk);
-    const size_t part0 = ((size_t)b * p.kv_heads + c) * p.nchunks;
-    float M = -INFINITY;
-    for (int ch = 0; ch < nch; ++ch) {
-        const float2 v = p.part_ml[(part0 + ch) * p.rows + r];
-        if (v.y > 0.f) M = fmaxf(M, v.x);
-    }
-    float L = 0.f;
-    for (int ch = 0; ch < nch; ++ch) {
-        const float2 v = p.part_ml[(part0 + ch) * p.rows + r];
-        if (v.y > 0.f) L += v.y * fast_exp2(v.x - M);
-    }
-    const float inv = 1.f / L;
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        float acc = 0.f;
-        for (int ch = 0; ch < nch; ++ch) {
-            const float2 v = p.part_ml[(part0 + ch) * p.rows + r];
-            if (v.y > 0.f) acc += p.part_o[((part0 + ch) * p.rows + r) * D + d] * fast_exp2(v.x - M);
-        }
-        orow[d] = acc * inv;
-    }
-}
-
 template <int D, int RG>
 static cudaError_t launch_d(const AttnParams &p, cudaStream_t stream) {
     dim3 grid(p.nchunks, p.kv_heads, p.batch);
     attn_partial_simt<D, RG><<<grid, kWarps * 32, 0, stream>>>(p);
-    count_launches(1);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    dim3 cgrid(p.rows, p.kv_heads, p.batch);
-    attn_combine<D><<<cgrid, 128, 0, stream>>>(p);
     count_launches(1);
     return cudaGetLastError();
 }

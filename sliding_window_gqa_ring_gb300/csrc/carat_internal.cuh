@@ -125,5 +125,14 @@ void count_launches(int n);
 // ---------------------------------------------------------------------------
 cudaError_t launch_ring_append(const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_attention_simt(const AttnParams &p, cudaStream_t stream);
+cudaError_t launch_combine(const AttnParams &p, cudaStream_t stream);
+
+// Tensor-core path (attention_tc.cu): rows per tile (16, 32 or 64) for a
+// group size and proposal count, whether the shape is supported, and the
+// launch of the split-K partial kernel over tiles of 128 keys.
+constexpr int kTcTileKeys = 128;
+int tc_rows_per_tile(int group, int k);
+bool tc_supported(int head_dim, int group, int k);
+cudaError_t launch_attention_tc(const AttnParams &p, int tiles_per_chunk, cudaStream_t stream);
 
 }  // namespace carat
