@@ -203,8 +203,10 @@ carat_status carat_global_verify_attention(float *out, const void *queries,
  * that loads the library keeps reserved until the process exits.  Arguments,
  * layouts and results are those of carat_swa_attention.  Sizes whose
  * carat_swa_workspace_bytes(...) exceeds the array return
- * CARAT_ERR_WORKSPACE without launching anything (e.g. batch 64 with 4
- * proposals needs about 12 MiB and fits; batch 64 with 16 proposals does not).
+ * CARAT_ERR_WORKSPACE without launching anything (e.g. 12 requests with 4
+ * proposals at head_dim 256 need about 4 MiB and fit; 8 requests with 16
+ * proposals and 8 query heads per KV head at head_dim 512 need about 36 MiB
+ * and do not).  Shapes whose workspace size is 0 use no scratch at all.
  *
  * The first call on each device looks up the array's device address (with
  * that device current) and caches it; make that first call before any

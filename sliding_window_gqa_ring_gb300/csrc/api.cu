@@ -43,6 +43,7 @@ bool supported_head_dim(int d) { return d == 256 || d == 512; }
 
 struct SplitPlan {
     bool tc = false;           // tensor-core kernel (else CUDA-core kernel)
+    bool direct = false;       // one split: the kernel writes the output, no combine
     int chunk = 0;             // keys per split
     int tiles_per_chunk = 0;   // tensor-core path: 128-key tiles per split
     int nchunks = 0;
@@ -60,38 +61,56 @@ void size_workspace(SplitPlan &p, long long pairs, int rows, int head_dim) {
     p.total = p.ml_bytes + p.o_bytes;
 }
 
+// Largest number of splits the combine kernel merges per (request, KV head).
+constexpr long long kMaxSplits = 1024;
+
 // CUDA-core path: the largest power-of-two chunk in [64, 4096] keys that still
-// gives about 8 CTAs per SM.
+// gives about 8 CTAs per SM (never more than kMaxSplits chunks).
 SplitPlan simt_plan(long long pairs, long long keys, int rows, int head_dim) {
     constexpr long long kTargetCtas = 8LL * 152;
     SplitPlan p;
-    int chunk = 64;
+    long long chunk = 64;
     for (int c = 4096; c >= 64; c >>= 1) {
         if (pairs * ((keys + c - 1) / c) >= kTargetCtas) {
             chunk = c;
             break;
         }
     }
-    p.chunk = chunk;
+    while ((keys + chunk - 1) / chunk > kMaxSplits) chunk *= 2;
+    p.chunk = (int)chunk;
     p.nchunks = (int)((keys + chunk - 1) / chunk);
     size_workspace(p, pairs, rows, head_dim);
     return p;
 }
 
-// Tensor-core path: 128-key tiles; a chunk is tiles_per_chunk tiles, chosen so
-// the grid holds about `target` CTAs when every request is as long as the
-// cache allows (ceil(total tiles / target), at most max_tpc).
+// Tensor-core path: 128-key tiles, tiles_per_chunk of them per split.  When
+// the (request, KV head, row group) units alone fill every SM, one CTA takes
+// all of a unit's tiles and writes the output directly (no combine).  Else
+// splits are sized for about two waves of CTAs with every request as long as
+// the cache allows, at most max_tpc tiles each.
 SplitPlan tc_plan(long long pairs, int row_groups, long long max_tiles, int rows, int head_dim,
-                  long long target, int max_tpc) {
+                  int ctas_per_sm, int max_tpc) {
     SplitPlan p;
     p.tc = true;
-    const long long total = pairs * row_groups * max_tiles;
-    long long tpc = (total + target - 1) / target;
-    if (tpc < 1) tpc = 1;
-    if (tpc > max_tpc) tpc = max_tpc;
+    const long long units = pairs * row_groups;
+    const long long slots = (long long)ctas_per_sm * 152;
+    long long tpc;
+    if (units >= slots && max_tiles <= 16) {
+        tpc = max_tiles;
+    } else {
+        tpc = (units * max_tiles + 2 * slots - 1) / (2 * slots);
+        if (tpc > max_tpc) tpc = max_tpc;
+        if (tpc < 1) tpc = 1;
+    }
+    if ((max_tiles + tpc - 1) / tpc > kMaxSplits) tpc = (max_tiles + kMaxSplits - 1) / kMaxSplits;
     p.tiles_per_chunk = (int)tpc;
     p.chunk = (int)tpc * kTcTileKeys;
     p.nchunks = (int)((max_tiles + tpc - 1) / tpc);
+    p.direct = p.nchunks == 1;
+    if (p.direct) {
+        p.total = 0;  // partials are never written
+        return p;
+    }
     size_workspace(p, pairs, rows, head_dim);
     return p;
 }
@@ -122,7 +141,7 @@ SplitPlan swa_plan(int batch, int proposal_count, int q_heads, int kv_heads, int
     if (tc_supported(head_dim, group, proposal_count)) {
         const long long tiles = (window + kTcTileKeys - 1) / kTcTileKeys + (proposal_count > 1 ? 1 : 0);
         return tc_plan(pairs, row_groups_for(group, proposal_count), tiles, rows, head_dim,
-                       4LL * 152, 4);
+                       tc_ctas_per_sm(head_dim, tc_rows_per_tile(group, proposal_count)), 4);
     }
     return simt_plan(pairs, keys_scanned(KeySource::kRing, window, proposal_count, 0), rows,
                      head_dim);
@@ -136,7 +155,7 @@ SplitPlan global_plan(int batch, int proposal_count, int q_heads, int kv_heads, 
     if (tc_supported(head_dim, group, proposal_count)) {
         const long long tiles = (capacity + kTcTileKeys - 1) / kTcTileKeys;
         return tc_plan(pairs, row_groups_for(group, proposal_count), tiles, rows, head_dim,
-                       2LL * 152, 8);
+                       tc_ctas_per_sm(head_dim, tc_rows_per_tile(group, proposal_count)), 8);
     }
     return simt_plan(pairs, capacity, rows, head_dim);
 }
@@ -144,7 +163,7 @@ SplitPlan global_plan(int batch, int proposal_count, int q_heads, int kv_heads, 
 cudaError_t launch_attention(const AttnParams &p, const SplitPlan &plan, cudaStream_t stream) {
     cudaError_t e = plan.tc ? launch_attention_tc(p, plan.tiles_per_chunk, stream)
                             : launch_attention_simt(p, stream);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess || plan.direct) return e;
     return launch_combine(p, stream);
 }
 
@@ -253,7 +272,7 @@ carat_status carat_swa_attention(float *out, const void *queries, const void *k_
     if (st != CARAT_OK) return st;
     if (proposal_count > 1 && (!displaced || !aligned16(displaced))) return CARAT_ERR_INVALID_ARG;
     const SplitPlan plan = swa_plan(batch, proposal_count, q_heads, kv_heads, head_dim, window);
-    if (!workspace || workspace_bytes < plan.total || !aligned16(workspace))
+    if (plan.total > 0 && (!workspace || workspace_bytes < plan.total || !aligned16(workspace)))
         return CARAT_ERR_WORKSPACE;
 
     AttnParams p{};
@@ -279,6 +298,8 @@ carat_status carat_swa_attention(float *out, const void *queries, const void *k_
     p.capacity = 0;
     p.chunk = plan.chunk;
     p.nchunks = plan.nchunks;
+    p.tiles_per_chunk = plan.tc ? plan.tiles_per_chunk : 0;
+    p.direct = plan.direct ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.source = KeySource::kRing;
     return launch_status(launch_attention(p, plan, static_cast<cudaStream_t>(stream)));
@@ -301,7 +322,7 @@ carat_status carat_global_verify_attention(float *out, const void *queries, cons
                                 context_lengths, batch);
     if (st != CARAT_OK) return st;
     const SplitPlan plan = global_plan(batch, proposal_count, q_heads, kv_heads, head_dim, capacity);
-    if (!workspace || workspace_bytes < plan.total || !aligned16(workspace))
+    if (plan.total > 0 && (!workspace || workspace_bytes < plan.total || !aligned16(workspace)))
         return CARAT_ERR_WORKSPACE;
 
     AttnParams p{};
@@ -327,6 +348,8 @@ carat_status carat_global_verify_attention(float *out, const void *queries, cons
     p.capacity = capacity;
     p.chunk = plan.chunk;
     p.nchunks = plan.nchunks;
+    p.tiles_per_chunk = plan.tc ? plan.tiles_per_chunk : 0;
+    p.direct = plan.direct ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.source = KeySource::kLinear;
     return launch_status(launch_attention(p, plan, static_cast<cudaStream_t>(stream)));

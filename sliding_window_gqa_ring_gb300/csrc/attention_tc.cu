@@ -53,6 +53,8 @@ namespace {
 constexpr int kTileKeys = 128;
 constexpr int kBoxBytes = 128 * 128;        // [128 keys][64 bf16]
 constexpr int kStageBytes = 2 * kBoxBytes;  // 128 keys x 128 d
+constexpr int kDispRows = 16;               // displaced rows loaded per tile (>= k - 1)
+constexpr int kDispBoxBytes = kDispRows * 128;
 constexpr int kThreads = 192;
 constexpr uint32_t kFull = 0xffffffffu;
 
@@ -74,6 +76,9 @@ struct Layout {
     static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64
                                    : kTmemUsed <= 128 ? 128 : kTmemUsed <= 256 ? 256 : 512;
     static_assert(kAlloc <= 232448, "more dynamic shared memory than one CTA may use");
+    // The softmax warps zero masked V rows while all KS stages of a V tile are
+    // resident, before the tile's PV product releases any of them.
+    static_assert(NS >= KS, "the stage ring must hold a whole V tile");
     static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kPBlock % 1024 == 0 &&
                       kQBlock % 1024 == 0,
                   "operand blocks must be 1024-byte aligned for the 128-byte swizzle");
@@ -88,7 +93,6 @@ struct TcMaps {
 
 struct TcPlan {
     int tiles_per_chunk;
-    int ring_tiles;       // tiles covering the ring slots (ring source)
     int row_groups;
     int pos_per_group;    // proposal positions per row group
 };
@@ -162,8 +166,8 @@ struct KeyInfo {
 
 }  // namespace
 
-template <int D, int N, int NS>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, int N, int NS, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB)
     attn_tc_kernel(const AttnParams p, const TcPlan plan, const __grid_constant__ TcMaps maps) {
     using L = Layout<D, N, NS>;
     constexpr int KS = L::KS;
@@ -178,10 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool ok = request_ok(p, b, &id, &ctx);
     const long long key_count = ctx + p.k;
     const bool ring = p.source == KeySource::kRing;
-    const int disp_tile = (ring && p.k > 1) ? plan.ring_tiles : -1;
-    const int ntiles = !ok ? 0
-                       : ring ? plan.ring_tiles + (p.k > 1 ? 1 : 0)
-                              : (int)((key_count + kTileKeys - 1) / kTileKeys);
+    int disp_tile = -1;
+    const int ntiles = ok ? tc_request_tiles(p.source, p.window, p.k, key_count, &disp_tile) : 0;
     const int t0 = chunk * plan.tiles_per_chunk;
     const int t1 = min(t0 + plan.tiles_per_chunk, ntiles);
     const int pos0 = rg * plan.pos_per_group;                       // first position of the group
@@ -193,7 +195,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     float2 *ml = p.part_ml + part * p.rows + row0;
     float *po = p.part_o + (part * p.rows + row0) * D;
     if (t0 >= t1) {
-        for (int r = threadIdx.x; r < rows_here; r += blockDim.x) ml[r] = make_float2(-INFINITY, 0.f);
+        if (p.direct) {
+            // One split per request: no combine follows, so a request rejected
+            // on the device gets its NaN outputs and status bit here.
+            if (!ok && chunk == 0) {
+                if (c == 0 && rg == 0 && threadIdx.x == 0)
+                    set_status(p.dev_status, request_error_bits(p, id, ctx));
+                for (int x = threadIdx.x; x < rows_here * D; x += blockDim.x) {
+                    const int row = row0 + x / D, j = row / p.group, hp = row % p.group;
+                    p.out[(((size_t)b * p.k + j) * p.q_heads + (size_t)c * p.group + hp) * D + x % D] =
+                        __int_as_float(0x7fc00000);
+                }
+            }
+        } else {
+            for (int r = threadIdx.x; r < rows_here; r += blockDim.x)
+                ml[r] = make_float2(-INFINITY, 0.f);
+        }
         return;
     }
 
@@ -260,7 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         alive = false;
                         break;
                     }
-                    tc::mbar_arrive_expect_tx(&full[s], kStageBytes);
+                    tc::mbar_arrive_expect_tx(&full[s], i == disp_tile ? 2 * kDispBoxBytes
+                                                                       : kStageBytes);
                     const bool is_v = part_i >= KS;
                     const int d0 = (part_i % KS) * 128;
                     uint8_t *dst = smem + s * kStageBytes;
@@ -523,7 +541,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < kHeldL; ++e) red_sum[q4 * N + rbl + e] = l_part[e];
         alive = !named_bar_softmax_any(!alive || *abort_flag);
-        if (alive) {
+        if (alive && p.direct) {
+            // This CTA saw every key of its rows: normalise and write the output.
+            float inv_l[N];
+#pragma unroll
+            for (int r = 0; r < N; ++r)
+                inv_l[r] = 1.f / (red_sum[r] + red_sum[N + r] + red_sum[2 * N + r] + red_sum[3 * N + r]);
+#pragma unroll
+            for (int ob = 0; ob < KS; ++ob) {
+#pragma unroll
+                for (int cb = 0; cb < N / 16; ++cb) {
+                    uint32_t r16[16];
+                    tc::tmem_ld16(tmem_o + ob * N + lane_off + cb * 16, r16);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int r = cb * 16 + e;
+                        if (r < rows_here) {
+                            const int row = row0 + r, j = row / p.group, hp = row % p.group;
+                            p.out[(((size_t)b * p.k + j) * p.q_heads + (size_t)c * p.group + hp) * D +
+                                  ob * 128 + t] = __uint_as_float(r16[e]) * inv_l[r];
+                        }
+                    }
+                }
+            }
+        } else if (alive) {
             if (t == 0) {
 #pragma unroll
                 for (int r = 0; r < N; ++r) {
@@ -565,11 +607,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 namespace {
 
-template <int D, int N, int NS>
+template <int D, int N, int NS, int MINB>
 cudaError_t launch_tc(const AttnParams &p, const TcPlan &plan, const TcMaps &maps,
                       cudaStream_t stream) {
     using L = Layout<D, N, NS>;
-    auto kernel = attn_tc_kernel<D, N, NS>;
+    static_assert(MINB == 1 || 2 * (L::kAlloc + 1024) <= 233472, "two CTAs must fit one SM");
+    auto kernel = attn_tc_kernel<D, N, NS, MINB>;
     static int configured_devices[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -594,6 +637,10 @@ int tc_rows_per_tile(int group, int k) {
     return 64;
 }
 
+int tc_ctas_per_sm(int head_dim, int rows_per_tile) {
+    return (head_dim == 256 && rows_per_tile == 16) ? 2 : 1;
+}
+
 bool tc_supported(int head_dim, int group, int k) {
     if (head_dim != 256 && head_dim != 512) return false;
     const int n = tc_rows_per_tile(group, k);
@@ -604,7 +651,6 @@ cudaError_t launch_attention_tc(const AttnParams &p, int tiles_per_chunk, cudaSt
     const int n = tc_rows_per_tile(p.group, p.k);
     TcPlan plan{};
     plan.tiles_per_chunk = tiles_per_chunk;
-    plan.ring_tiles = (p.window + kTileKeys - 1) / kTileKeys;
     plan.pos_per_group = n / p.group;
     if (plan.pos_per_group > p.k) plan.pos_per_group = p.k;
     plan.row_groups = (p.k + plan.pos_per_group - 1) / plan.pos_per_group;
@@ -623,7 +669,7 @@ cudaError_t launch_attention_tc(const AttnParams &p, int tiles_per_chunk, cudaSt
     if (p.source == KeySource::kRing && p.k > 1) {
         const uint64_t dims4[4] = {D, (uint64_t)p.kv_heads, 2, (uint64_t)p.batch * (p.k - 1)};
         const uint64_t strides4[3] = {D * 2, row_bytes, 2 * row_bytes};
-        const uint32_t box4[4] = {64, 1, 1, (uint32_t)kTileKeys};
+        const uint32_t box4[4] = {64, 1, 1, (uint32_t)kDispRows};
         if (!make_bf16_tensor_map(&maps.disp, p.displaced, 4, dims4, strides4, box4, true))
             return cudaErrorInvalidValue;
     } else {
@@ -638,16 +684,18 @@ cudaError_t launch_attention_tc(const AttnParams &p, int tiles_per_chunk, cudaSt
             return cudaErrorInvalidValue;
     }
 
-    // One CTA per SM (register use); the stage ring takes the shared memory
-    // left after Q and P.
+    // 16-row tiles at head_dim 256 fit two CTAs per SM (registers and shared
+    // memory), so one CTA's start-up and epilogue overlap the other's
+    // streaming; the others run one CTA per SM with the stage ring taking the
+    // rest of shared memory.
     if (p.head_dim == 256) {
-        if (n == 16) return launch_tc<256, 16, 6>(p, plan, maps, stream);
-        if (n == 32) return launch_tc<256, 32, 6>(p, plan, maps, stream);
-        return launch_tc<256, 64, 5>(p, plan, maps, stream);
+        if (n == 16) return launch_tc<256, 16, 3, 2>(p, plan, maps, stream);
+        if (n == 32) return launch_tc<256, 32, 6, 1>(p, plan, maps, stream);
+        return launch_tc<256, 64, 5, 1>(p, plan, maps, stream);
     }
-    if (n == 16) return launch_tc<512, 16, 6>(p, plan, maps, stream);
-    if (n == 32) return launch_tc<512, 32, 5>(p, plan, maps, stream);
-    return launch_tc<512, 64, 4>(p, plan, maps, stream);
+    if (n == 16) return launch_tc<512, 16, 4, 1>(p, plan, maps, stream);
+    if (n == 32) return launch_tc<512, 32, 5, 1>(p, plan, maps, stream);
+    return launch_tc<512, 64, 4, 1>(p, plan, maps, stream);
 }
 
 }  // namespace carat

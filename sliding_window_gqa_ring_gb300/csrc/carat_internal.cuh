@@ -38,6 +38,8 @@ struct AttnParams {
     int capacity;               // cache rows (kLinear)
     int chunk;                  // keys per split
     int nchunks;                // splits per (request, KV head)
+    int tiles_per_chunk;        // tensor-core path: 128-key tiles per split (0: CUDA-core path)
+    int direct;                 // 1: one split covers every key, the kernel writes `out` itself
     float scale_log2;           // softmax scale * log2(e)
     KeySource source;
 };
@@ -111,6 +113,24 @@ __device__ __forceinline__ int request_error_bits(const AttnParams &p, int id, l
     return bits;
 }
 
+// Tensor-core path: 128-key tiles a request needs.  Ring: the tiles covering
+// the slots that hold tokens (all `window` slots once the ring has wrapped),
+// plus one tile of displaced rows when some exist (key_count > window and
+// k > 1).  Cache: ceil(key_count / 128).  *disp_tile = index of the displaced
+// tile, or -1.
+__host__ __device__ __forceinline__ int tc_request_tiles(KeySource src, int window, int k,
+                                                         long long key_count, int *disp_tile) {
+    if (src == KeySource::kRing) {
+        const long long held = key_count < window ? key_count : window;
+        const int ring_tiles = (int)((held + 127) / 128);
+        const bool disp = k > 1 && key_count > window;
+        *disp_tile = disp ? ring_tiles : -1;
+        return ring_tiles + (disp ? 1 : 0);
+    }
+    *disp_tile = -1;
+    return (int)((key_count + 127) / 128);
+}
+
 // Number of key slots scanned per (request, KV head).
 __host__ __device__ __forceinline__ long long keys_scanned(KeySource src, int window, int k,
                                                           long long key_count) {
@@ -132,6 +152,7 @@ cudaError_t launch_combine(const AttnParams &p, cudaStream_t stream);
 // launch of the split-K partial kernel over tiles of 128 keys.
 constexpr int kTcTileKeys = 128;
 int tc_rows_per_tile(int group, int k);
+int tc_ctas_per_sm(int head_dim, int rows_per_tile);
 bool tc_supported(int head_dim, int group, int k);
 cudaError_t launch_attention_tc(const AttnParams &p, int tiles_per_chunk, cudaStream_t stream);
 
