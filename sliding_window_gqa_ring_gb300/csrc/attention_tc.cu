@@ -68,11 +68,11 @@ struct Layout {
     static constexpr int kOffRed = kOffP + 2 * kPBlock;
     static constexpr int kRedFloats = 3 * 4 * N;       // 2 x max buffers + sum buffer
     static constexpr int kOffBar = kOffRed + kRedFloats * 4;
-    static constexpr int kNumBars = 2 * NS + 5;
+    static constexpr int kNumBars = 2 * NS + 6;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kBytes = kOffMisc + 16;
     static constexpr int kAlloc = kBytes + 1024;       // base alignment slack
-    static constexpr int kTmemUsed = N * (1 + D / 128);
+    static constexpr int kTmemUsed = N * (2 + D / 128);   // two S^T buffers + O^T
     static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64
                                    : kTmemUsed <= 128 ? 128 : kTmemUsed <= 256 ? 256 : 512;
     static_assert(kAlloc <= 232448, "more dynamic shared memory than one CTA may use");
@@ -159,6 +159,15 @@ __device__ __forceinline__ int warp_transpose_reduce(float (&v)[N], int lane) {
     return row_base;
 }
 
+// Bits [0, n) set (n <= 64).
+__device__ __forceinline__ uint64_t low_bits(int n) {
+    return n >= 64 ? ~0ull : ((1ull << n) - 1ull);
+}
+
+// A row's running maximum is replaced only when a tile's maximum exceeds it by
+// more than this (log2 units), so P <= 2^8 and O^T rescales are rare.
+constexpr float kRescaleSlack = 8.0f;
+
 struct KeyInfo {
     long long pos;  // absolute position of the token this key row holds
     bool data;      // the smem row holds a token of this request (else: zero it)
@@ -220,11 +229,11 @@ __global__ void __launch_bounds__(kThreads, MINB)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffBar);
     uint64_t *full = bars;
     uint64_t *empty = bars + NS;
-    uint64_t *s_full = bars + 2 * NS;
-    uint64_t *p_full = s_full + 1;
-    uint64_t *o_done = s_full + 2;
-    uint64_t *q_full = s_full + 3;
-    uint64_t *fin = s_full + 4;
+    uint64_t *s_full = bars + 2 * NS;   // [2]: one per S^T buffer
+    uint64_t *p_full = s_full + 2;
+    uint64_t *o_done = s_full + 3;
+    uint64_t *q_full = s_full + 4;
+    uint64_t *fin = s_full + 5;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffMisc + 4);
     float *red = reinterpret_cast<float *>(smem + L::kOffRed);
@@ -236,7 +245,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
             tc::mbar_init(&full[i], 1);
             tc::mbar_init(&empty[i], 1);
         }
-        tc::mbar_init(s_full, 1);
+        tc::mbar_init(&s_full[0], 1);
+        tc::mbar_init(&s_full[1], 1);
         tc::mbar_init(p_full, 128);
         tc::mbar_init(o_done, 1);
         tc::mbar_init(q_full, 1);
@@ -252,8 +262,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_s = tmem;          // S^T: N columns
-    const uint32_t tmem_o = tmem + N;      // O^T: KS blocks of N columns
+    const uint32_t tmem_o = tmem + 2 * N;  // O^T: KS blocks of N columns (S^T buffers: 0, N)
+    const int n = t1 - t0;                 // tiles of this CTA
+    // Load / consume order of the 128-key tiles' K and V parts: K(0), then
+    // K(x+1) before V(x), then V(n-1), so the next tile's keys stream in and
+    // its scores are computed while this tile's softmax runs.  Part index of
+    // V(x) in that order (each part is KS stages):
+    auto v_part = [n](int x) { return x == n - 1 ? 2 * n - 1 : 2 * x + 2; };
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -269,8 +284,21 @@ __global__ void __launch_bounds__(kThreads, MINB)
                                 q_full, pol);
             uint32_t cnt = 0;
             bool alive = true;
-            for (int i = t0; i < t1 && alive; ++i) {
-                for (int part_i = 0; part_i < 2 * KS; ++part_i) {
+            for (int part = 0; part < 2 * n && alive; ++part) {
+                int x;
+                bool is_v;
+                if (part == 0) {
+                    x = 0;
+                    is_v = false;
+                } else if (part == 2 * n - 1) {
+                    x = n - 1;
+                    is_v = true;
+                } else {
+                    x = (part - 1) / 2 + ((part - 1) % 2 == 0 ? 1 : 0);
+                    is_v = (part - 1) % 2 == 1;
+                }
+                const int i = t0 + x;
+                for (int ks = 0; ks < KS; ++ks) {
                     const int s = cnt % NS;
                     if (cnt >= NS && !wait_or_abort(&empty[s], ((cnt / NS) & 1) ^ 1, abort_flag,
                                                     p.dev_status)) {
@@ -279,8 +307,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     }
                     tc::mbar_arrive_expect_tx(&full[s], i == disp_tile ? 2 * kDispBoxBytes
                                                                        : kStageBytes);
-                    const bool is_v = part_i >= KS;
-                    const int d0 = (part_i % KS) * 128;
+                    const int d0 = ks * 128;
                     uint8_t *dst = smem + s * kStageBytes;
 #pragma unroll
                     for (int box = 0; box < 2; ++box) {
@@ -312,57 +339,64 @@ __global__ void __launch_bounds__(kThreads, MINB)
             const uint32_t p_base = tc::smem_u32(s_p);
             bool alive = wait_or_abort(q_full, 0, abort_flag, p.dev_status);
             uint32_t cnt = 0;
-            for (int i = t0, idx = 0; i < t1 && alive; ++i, ++idx) {
-                // S^T = K_tile . Q^T over D in steps of 16
-                for (int ks = 0; ks < KS && alive; ++ks) {
-                    const int s = cnt % NS;
-                    if (!wait_or_abort(&full[s], (cnt / NS) & 1, abort_flag, p.dev_status)) {
-                        alive = false;
-                        break;
-                    }
-                    tc::tc_fence_after();
-                    const uint32_t base = tc::smem_u32(smem + s * kStageBytes);
-#pragma unroll
-                    for (int box = 0; box < 2; ++box) {
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t a = tc::sdesc_sw128(base + box * kBoxBytes + kk * 32, 16, 1024);
-                            const uint64_t q = tc::sdesc_sw128(
-                                q_base + (ks * 2 + box) * L::kQBlock + kk * 32, 16, 1024);
-                            tc::mma_bf16_ss(tmem_s, a, q, idesc_qk, (ks | box | kk) != 0);
+            for (int step = 0; step <= n && alive; ++step) {
+                if (step < n) {
+                    // S^T[step & 1] = K_tile . Q^T over D in steps of 16
+                    const uint32_t tmem_s = tmem + (step & 1) * N;
+                    for (int ks = 0; ks < KS && alive; ++ks) {
+                        const int s = cnt % NS;
+                        if (!wait_or_abort(&full[s], (cnt / NS) & 1, abort_flag, p.dev_status)) {
+                            alive = false;
+                            break;
                         }
+                        tc::tc_fence_after();
+                        const uint32_t base = tc::smem_u32(smem + s * kStageBytes);
+#pragma unroll
+                        for (int box = 0; box < 2; ++box) {
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint64_t a =
+                                    tc::sdesc_sw128(base + box * kBoxBytes + kk * 32, 16, 1024);
+                                const uint64_t q = tc::sdesc_sw128(
+                                    q_base + (ks * 2 + box) * L::kQBlock + kk * 32, 16, 1024);
+                                tc::mma_bf16_ss(tmem_s, a, q, idesc_qk, (ks | box | kk) != 0);
+                            }
+                        }
+                        tc::mma_commit(&empty[s]);
+                        ++cnt;
                     }
-                    tc::mma_commit(&empty[s]);
-                    ++cnt;
+                    if (!alive) break;
+                    tc::mma_commit(&s_full[step & 1]);
                 }
-                if (!alive) break;
-                tc::mma_commit(s_full);
-                // O^T += V_tile^T . P^T over the tile's 128 keys in steps of 16
-                if (!wait_or_abort(p_full, idx & 1, abort_flag, p.dev_status)) {
-                    alive = false;
-                    break;
-                }
-                tc::tc_fence_after();
-                for (int vs = 0; vs < KS && alive; ++vs) {
-                    const int s = cnt % NS;
-                    if (!wait_or_abort(&full[s], (cnt / NS) & 1, abort_flag, p.dev_status)) {
+                if (step >= 1) {
+                    // O^T += V_tile^T . P^T over tile x's 128 keys in steps of 16
+                    const int x = step - 1;
+                    if (!wait_or_abort(p_full, x & 1, abort_flag, p.dev_status)) {
                         alive = false;
                         break;
                     }
                     tc::tc_fence_after();
-                    const uint32_t base = tc::smem_u32(smem + s * kStageBytes);
+                    for (int vs = 0; vs < KS && alive; ++vs) {
+                        const int s = cnt % NS;
+                        if (!wait_or_abort(&full[s], (cnt / NS) & 1, abort_flag, p.dev_status)) {
+                            alive = false;
+                            break;
+                        }
+                        tc::tc_fence_after();
+                        const uint32_t base = tc::smem_u32(smem + s * kStageBytes);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t a = tc::sdesc_sw128(base + kk * 2048, kBoxBytes, 1024);
-                        const uint64_t pp = tc::sdesc_sw128(
-                            p_base + (kk / 4) * L::kPBlock + (kk % 4) * 32, 16, 1024);
-                        tc::mma_bf16_ss(tmem_o + vs * N, a, pp, idesc_pv, (idx > 0 || kk > 0));
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t a = tc::sdesc_sw128(base + kk * 2048, kBoxBytes, 1024);
+                            const uint64_t pp = tc::sdesc_sw128(
+                                p_base + (kk / 4) * L::kPBlock + (kk % 4) * 32, 16, 1024);
+                            tc::mma_bf16_ss(tmem_o + vs * N, a, pp, idesc_pv, (x > 0 || kk > 0));
+                        }
+                        tc::mma_commit(&empty[s]);
+                        ++cnt;
                     }
-                    tc::mma_commit(&empty[s]);
-                    ++cnt;
+                    if (!alive) break;
+                    tc::mma_commit(o_done);
                 }
-                if (!alive) break;
-                tc::mma_commit(o_done);
             }
             if (!alive) {
                 // Make sure every MMA this thread issued has finished.
@@ -383,9 +417,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
         }
         bool alive = true;
         int idx = 0;
+        // Slot that holds the newest token (ring source).
+        const long long head_slot = ring ? (key_count - 1) % p.window : 0;
         for (int i = t0; i < t1; ++i, ++idx) {
             // warp-uniform: the TMEM load below is warp-collective
-            const bool w_ok = __all_sync(kFull, wait_or_abort(s_full, idx & 1, abort_flag, p.dev_status));
+            const bool w_ok = __all_sync(
+                kFull, wait_or_abort(&s_full[idx & 1], (idx >> 1) & 1, abort_flag, p.dev_status));
+            const uint32_t tmem_s = tmem + (idx & 1) * N;
             float x[N];
             if (w_ok) {
                 tc::tc_fence_after();
@@ -407,23 +445,27 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 ki.pos = (t < p.k - 1) ? ctx - p.window + 1 + t : -1;
                 ki.data = t < p.k - 1 && ki.pos >= 0;
             } else if (ring) {
-                const long long slot = (long long)i * kTileKeys + t;
-                const long long w = p.window;
-                ki.pos = slot < w ? key_count - 1 - (((key_count - 1 - slot) % w) + w) % w : -1;
+                // Slot s holds the newest position congruent to s: head_slot - s
+                // (mod window) positions before the newest token.
+                const int slot = i * kTileKeys + t;
+                long long delta = head_slot - slot;
+                if (delta < 0) delta += p.window;
+                ki.pos = slot < p.window ? key_count - 1 - delta : -1;
                 ki.data = ki.pos >= 0;
             } else {
                 const long long u = (long long)i * kTileKeys + t;
                 ki.pos = u < key_count ? u : -1;
                 ki.data = ki.pos >= 0;
             }
+            // Query j of the group (position ctx + pos0 + j) sees the key iff
+            // j >= d0 and, for a sliding window, j < d0 + window.
             uint64_t rowmask = 0;
-            const uint64_t group_bits = p.group >= 64 ? ~0ull : ((1ull << p.group) - 1ull);
             if (ki.data) {
-                for (int j = 0; j < npos; ++j) {
-                    const long long qp = ctx + pos0 + j;
-                    const bool vis = ki.pos <= qp && (!ring || ki.pos > qp - p.window);
-                    if (vis) rowmask |= group_bits << (j * p.group);
-                }
+                const long long d0 = ki.pos - (ctx + pos0);
+                const long long jlo = d0 < 0 ? 0 : d0;
+                long long jhi = ring ? d0 + p.window : npos;
+                if (jhi > npos) jhi = npos;
+                if (jlo < jhi) rowmask = low_bits((int)jhi * p.group) & ~low_bits((int)jlo * p.group);
             }
             float tmax[N];
 #pragma unroll
@@ -455,7 +497,11 @@ __global__ void __launch_bounds__(kThreads, MINB)
             bool rescale = false;
 #pragma unroll
             for (int r = 0; r < N; ++r) {
-                const float mn = fmaxf(m_run[r], tmax[r]);
+                // Keep a stale running maximum unless the tile's maximum exceeds
+                // it by more than kRescaleSlack (log2 units): P stays below
+                // 2^kRescaleSlack and O^T is rescaled only when a row's maximum
+                // really moves.
+                const float mn = tmax[r] > m_run[r] + kRescaleSlack ? tmax[r] : m_run[r];
                 const float ms = mn == -INFINITY ? 0.f : mn;
                 alpha[r] = fast_exp2(m_run[r] - ms);
                 const float pr = fast_exp2(x[r] - ms);
@@ -504,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     (!ring && (long long)(i + 1) * kTileKeys > key_count);
                 if (tile_partial) {
                     for (int vs = 0; vs < KS; ++vs) {
-                        const uint32_t x_cnt = (uint32_t)idx * 2 * KS + KS + vs;
+                        const uint32_t x_cnt = (uint32_t)v_part(idx) * KS + vs;
                         const int s = x_cnt % NS;
                         if (!wait_or_abort(&full[s], (x_cnt / NS) & 1, abort_flag, p.dev_status)) {
                             alive = false;

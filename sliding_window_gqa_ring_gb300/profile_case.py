@@ -1,0 +1,57 @@
+"""Run a few attention calls of one staged layer, for profiler captures.
+
+    python -m sliding_window_gqa_ring_gb300.profile_case --case swa_mixed --calls 3
+
+The layer is staged from the seeded workloads in ``synth`` (rings or caches
+written with carat_ring_append, then this step's append), after which only
+the attention call repeats, so a profiler filtered on the attention kernels
+sees exactly ``--calls`` launches of each.  Every case keeps a few GB or less
+on the device and reads more than the 129 MB L2 per call.
+"""
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+from . import carat, engine, synth
+
+CASES = {
+    "swa_b1": lambda: synth.sliding_single(),
+    "swa_b56": lambda: synth.sliding_batched(),
+    "swa_mixed": lambda: synth.mixed_step()[0],
+    "global_single": lambda: synth.global_single(),
+    "global_sweep4": lambda: synth.global_sweep(4),
+    "global_sweep15": lambda: synth.global_sweep(15),
+}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--case", choices=sorted(CASES), required=True)
+    ap.add_argument("--calls", type=int, default=3)
+    args = ap.parse_args()
+    w = CASES[args.case]()
+    if w.window:
+        layer = engine.SlidingLayer(w.batch, window=w.window, q_heads=w.q_heads,
+                                    kv_heads=w.kv_heads, head_dim=w.head_dim,
+                                    max_proposals=w.proposal_count, scale=w.scale)
+        inp = engine.stage_sliding(w, 0, layer)
+    else:
+        layer = engine.GlobalLayer(w.batch, capacity=w.capacity, q_heads=w.q_heads,
+                                   kv_heads=w.kv_heads, head_dim=w.head_dim,
+                                   max_proposals=w.proposal_count, scale=w.scale)
+        inp = engine.stage_global(w, 0, layer, keep_history=False)
+    layer.append(inp.k_new, inp.v_new, inp.context_lengths)
+    out = torch.empty(inp.queries.shape, dtype=torch.float32, device=layer.device)
+    for _ in range(args.calls):
+        layer.attend(inp.queries, inp.context_lengths, out=out)
+    torch.cuda.synchronize()
+    status = carat.carat_get_device_status(clear=True)
+    print(f"{args.case}: {args.calls} calls, device status {status:#x}")
+    if status:
+        raise SystemExit(1)
+
+
+if __name__ == "__main__":
+    main()
