@@ -100,7 +100,7 @@ def measured_peaks():
 def kernel_source_hash():
     h = hashlib.sha256()
     for f in sorted(os.listdir(KERNEL_SOURCES)):
-        if f.endswith((".cu", ".cuh")):
+        if f.endswith((".cu", ".cuh", ".h")):
             with open(os.path.join(KERNEL_SOURCES, f), "rb") as fh:
                 h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
