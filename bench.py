@@ -184,6 +184,24 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+def max_over_ranks(value, device="cpu"):
+    """Max of a float over all ranks (no-op without torch.distributed).  The
+    only collective of the benchmark: the path itself exchanges nothing."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(bytes_per_step, steps, ms_max, world):
+    """Whole-job GB/s: every replica moved bytes_per_step per step, and the
+    job took as long as the slowest replica."""
+    return world * bytes_per_step * steps / (ms_max / 1e3) / 1e9
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -299,7 +317,32 @@ def run_carat(args, world, rank, local):
         step()
     torch.cuda.synchronize()
 
-    # --- timed region
+    # --- timed region: CUDA events around the whole region and around every
+    # call of every step (all on the stream the library launches on)
+    call_names = []
+    for _ in layers:
+        call_names += ["swa_append", "swa_attention"]
+    call_names += ["global_append", "global_attention"]
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in call_names] for _ in range(min(args.steps, 300))]
+
+    def timed_step(marks):
+        x = 0
+        for (lay, inp), out in zip(layers, outs):
+            marks[x][0].record(stream)
+            lay.append(inp.k_new, inp.v_new, inp.context_lengths)
+            marks[x][1].record(stream)
+            marks[x + 1][0].record(stream)
+            lay.attend(inp.queries, inp.context_lengths, out=out)
+            marks[x + 1][1].record(stream)
+            x += 2
+        marks[x][0].record(stream)
+        glay.append(ginp.k_new, ginp.v_new, ginp.context_lengths)
+        marks[x][1].record(stream)
+        marks[x + 1][0].record(stream)
+        glay.attend(ginp.queries, ginp.context_lengths, out=gout)
+        marks[x + 1][1].record(stream)
+
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -313,41 +356,24 @@ def run_carat(args, world, rank, local):
         e1.record(stream)
         torch.cuda.synchronize()
     launches = carat.kernel_launches() - launches0
-    ms = e0.elapsed_time(e1)
+    # A second timed region of the same steps with events around every call
+    # (the records themselves add a few us per call, so `value` comes from the
+    # uninstrumented region above).
+    for st in range(len(ev)):
+        timed_step(ev[st])
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), dev)
     if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
         torch.distributed.barrier()
     clocks = clk.summary()
     ms_per_step = ms / args.steps
-    value = world * nbytes["step"] * args.steps / (ms / 1e3) / 1e9
+    value = replica_throughput(nbytes["step"], args.steps, ms, world)
 
-    # --- per-call breakdown (events around each call)
-    calls = {"swa_append": [], "swa_attention": [], "global_append": [],
-             "global_attention": []}
-    reps = max(3, min(args.steps, 50))
-    ev = []
-    for _ in range(reps):
-        for (lay, inp), out in zip(layers, outs):
-            a, bb, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-            a.record(stream)
-            lay.append(inp.k_new, inp.v_new, inp.context_lengths)
-            bb.record(stream)
-            lay.attend(inp.queries, inp.context_lengths, out=out)
-            c.record(stream)
-            ev.append(("swa", a, bb, c))
-        a, bb, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-        a.record(stream)
-        glay.append(ginp.k_new, ginp.v_new, ginp.context_lengths)
-        bb.record(stream)
-        glay.attend(ginp.queries, ginp.context_lengths, out=gout)
-        c.record(stream)
-        ev.append(("global", a, bb, c))
-    torch.cuda.synchronize()
-    for kind, a, bb, c in ev:
-        calls[f"{kind}_append"].append(a.elapsed_time(bb) * 1e3)
-        calls[f"{kind}_attention"].append(bb.elapsed_time(c) * 1e3)
+    # --- per-call durations from the same timed steps
+    calls = {n: [] for n in ("swa_append", "swa_attention", "global_append", "global_attention")}
+    for st in range(len(ev)):
+        for name, (a, bb) in zip(call_names, ev[st]):
+            calls[name].append(a.elapsed_time(bb) * 1e3)
     per_call = {}
     for name, us in calls.items():
         mean_us = statistics.mean(us)
@@ -362,7 +388,9 @@ def run_carat(args, world, rank, local):
                 "peak_source": f"{peak_kind} hbm_gbs", "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": profiled_traffic(dominant),
                 "algorithmic_bytes_per_launch": nbytes[dominant],
-                "timing": "CUDA events around the whole call (split-K kernel + combine)"}
+                "timing": ("mean of CUDA events around every call of this kind over a second "
+                           "timed region of up to 300 steps (the whole call: attention kernel, "
+                           "plus the combine kernel when the call splits the keys)")}
 
     # --- end to end through the public API with host buffers
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())  # noqa: E731
@@ -401,12 +429,8 @@ def run_carat(args, world, rank, local):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * nbytes["step"] * e2e_steps / (e2e_ms / 1e3) / 1e9
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    e2e_value = replica_throughput(nbytes["step"], e2e_steps, e2e_ms, world)
 
     status = carat.carat_get_device_status(clear=True)
     if rank != 0:
@@ -490,7 +514,7 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["carat", "reference"], default="carat")
     ap.add_argument("--sample-requests", type=int, default=16,
