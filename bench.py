@@ -50,9 +50,13 @@ KERNEL_SOURCES = os.path.join(ROOT, "sliding_window_gqa_ring_gb300", "csrc")
 # ---------------------------------------------------------------------------
 
 def sliding_call_bytes(w, b):
-    """Bytes one request moves in one sliding layer: the K and V rows of the
-    union of its queries' windows, its queries, its fp32 outputs, and the
-    append (new rows read + written, displaced rows read + written)."""
+    """Bytes one request moves in one sliding layer.
+
+    attention: the K and V rows of the union of its queries' windows (the
+    step's own rows included), its queries and its fp32 outputs.  The fused
+    append+attention call adds the new rows written into the ring; the
+    separate append reads and writes them and also saves and reads back the
+    displaced rows."""
     k, hkv, d, hq = w.proposal_count, w.kv_heads, w.head_dim, w.q_heads
     kc = int(w.key_counts[b])
     ctx = kc - k
@@ -60,8 +64,9 @@ def sliding_call_bytes(w, b):
     row = hkv * d * 2
     attn = keys * row * 2 + k * hq * d * 2 + k * hq * d * 4
     disp = sum(1 for i in range(k - 1) if ctx - w.window + 1 + i >= 0)
+    fused_writes = k * row * 2
     append = k * row * 2 * 2 + disp * row * 2 * 2
-    return attn, append
+    return attn, fused_writes, append
 
 
 def global_call_bytes(w, b):
@@ -69,18 +74,23 @@ def global_call_bytes(w, b):
     kc = int(w.key_counts[b])
     row = hkv * d * 2
     attn = kc * row * 2 + k * hq * d * 2 + k * hq * d * 4
-    append = k * row * 2 * 2
-    return attn, append
+    return attn, k * row * 2, k * row * 2 * 2
 
 
 def step_bytes(sliding, glob):
-    s_attn = sum(sliding_call_bytes(sliding, b)[0] for b in range(sliding.batch))
-    s_app = sum(sliding_call_bytes(sliding, b)[1] for b in range(sliding.batch))
-    g_attn = sum(global_call_bytes(glob, b)[0] for b in range(glob.batch))
-    g_app = sum(global_call_bytes(glob, b)[1] for b in range(glob.batch))
-    return {"swa_attention": s_attn, "swa_append": s_app, "global_attention": g_attn,
-            "global_append": g_app,
-            "step": sliding.layers * (s_attn + s_app) + g_attn + g_app}
+    def tot(fn, w, i):
+        return sum(fn(w, b)[i] for b in range(w.batch))
+    s_attn, s_wr, s_app = (tot(sliding_call_bytes, sliding, i) for i in range(3))
+    g_attn, g_wr, g_app = (tot(global_call_bytes, glob, i) for i in range(3))
+    return {
+        # fused calls (the step as timed)
+        "swa_call": s_attn + s_wr, "global_call": g_attn + g_wr,
+        "step": sliding.layers * (s_attn + s_wr) + g_attn + g_wr,
+        # separate calls (timed for comparison)
+        "swa_append": s_app, "swa_attention": s_attn, "global_append": g_app,
+        "global_attention": g_attn,
+        "step_separate": sliding.layers * (s_attn + s_app) + g_attn + g_app,
+    }
 
 
 # ---------------------------------------------------------------------------
@@ -317,32 +327,7 @@ def run_carat(args, world, rank, local):
         step()
     torch.cuda.synchronize()
 
-    # --- timed region: CUDA events around the whole region and around every
-    # call of every step (all on the stream the library launches on)
-    call_names = []
-    for _ in layers:
-        call_names += ["swa_append", "swa_attention"]
-    call_names += ["global_append", "global_attention"]
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in call_names] for _ in range(min(args.steps, 300))]
-
-    def timed_step(marks):
-        x = 0
-        for (lay, inp), out in zip(layers, outs):
-            marks[x][0].record(stream)
-            lay.append(inp.k_new, inp.v_new, inp.context_lengths)
-            marks[x][1].record(stream)
-            marks[x + 1][0].record(stream)
-            lay.attend(inp.queries, inp.context_lengths, out=out)
-            marks[x + 1][1].record(stream)
-            x += 2
-        marks[x][0].record(stream)
-        glay.append(ginp.k_new, ginp.v_new, ginp.context_lengths)
-        marks[x][1].record(stream)
-        marks[x + 1][0].record(stream)
-        glay.attend(ginp.queries, ginp.context_lengths, out=gout)
-        marks[x + 1][1].record(stream)
-
+    # --- timed region (uninstrumented): the step as a user runs it
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -356,12 +341,6 @@ def run_carat(args, world, rank, local):
         e1.record(stream)
         torch.cuda.synchronize()
     launches = carat.kernel_launches() - launches0
-    # A second timed region of the same steps with events around every call
-    # (the records themselves add a few us per call, so `value` comes from the
-    # uninstrumented region above).
-    for st in range(len(ev)):
-        timed_step(ev[st])
-    torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1), dev)
     if world > 1:
         torch.distributed.barrier()
@@ -369,17 +348,55 @@ def run_carat(args, world, rank, local):
     ms_per_step = ms / args.steps
     value = replica_throughput(nbytes["step"], args.steps, ms, world)
 
-    # --- per-call durations from the same timed steps
-    calls = {n: [] for n in ("swa_append", "swa_attention", "global_append", "global_attention")}
-    for st in range(len(ev)):
-        for name, (a, bb) in zip(call_names, ev[st]):
-            calls[name].append(a.elapsed_time(bb) * 1e3)
+    # --- a second timed region of the same steps with CUDA events around
+    # every call (the records add a few us per call, so `value` comes from the
+    # region above)
+    nrep = min(args.steps, 300)
+
+    def bracket(fn):
+        a = torch.cuda.Event(enable_timing=True)
+        bb = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        bb.record(stream)
+        return a, bb
+
+    marks = {"swa_call": [], "global_call": []}
+    for _ in range(nrep):
+        for (lay, inp), out in zip(layers, outs):
+            marks["swa_call"].append(bracket(lambda: lay.step(
+                inp.queries, inp.k_new, inp.v_new, inp.context_lengths, out=out)))
+        marks["global_call"].append(bracket(lambda: glay.step(
+            ginp.queries, ginp.k_new, ginp.v_new, ginp.context_lengths, out=gout)))
+    torch.cuda.synchronize()
     per_call = {}
-    for name, us in calls.items():
-        mean_us = statistics.mean(us)
+    for name, pairs in marks.items():
+        mean_us = statistics.mean(a.elapsed_time(bb) * 1e3 for a, bb in pairs)
         per_call[name] = {"us": round(mean_us, 3), "gb_s": round(nbytes[name] / (mean_us * 1e3), 1),
                           "bytes": nbytes[name],
                           "launches_per_step": (sliding.layers if name.startswith("swa") else 1)}
+
+    # --- the same step through the separate append and attention calls
+    def step_separate():
+        for (lay, inp), out in zip(layers, outs):
+            lay.step(inp.queries, inp.k_new, inp.v_new, inp.context_lengths, out=out, fused=False)
+        glay.step(ginp.queries, ginp.k_new, ginp.v_new, ginp.context_lengths, out=gout,
+                  fused=False)
+
+    for _ in range(3):
+        step_separate()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(nrep):
+        step_separate()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sep_ms = e0.elapsed_time(e1) / nrep
+    separate = {"ms_per_step": round(sep_ms, 4),
+                "gb_s": round(nbytes["step_separate"] / (sep_ms * 1e6), 1),
+                "step_bytes": nbytes["step_separate"],
+                "calls": "carat_ring_append + carat_swa_attention (x5), carat_ring_append + "
+                         "carat_global_verify_attention"}
     share = {n: per_call[n]["us"] * per_call[n]["launches_per_step"] for n in per_call}
     dominant = max(share, key=share.get)
     peak, peak_kind = measured_peaks()
@@ -389,8 +406,8 @@ def run_carat(args, world, rank, local):
                 "frac": round(achieved / peak, 4), "traffic": profiled_traffic(dominant),
                 "algorithmic_bytes_per_launch": nbytes[dominant],
                 "timing": ("mean of CUDA events around every call of this kind over a second "
-                           "timed region of up to 300 steps (the whole call: attention kernel, "
-                           "plus the combine kernel when the call splits the keys)")}
+                           "timed region of up to 300 steps (the whole fused append+attention "
+                           "call: one kernel, plus the combine kernel when it splits the keys)")}
 
     # --- end to end through the public API with host buffers
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())  # noqa: E731
@@ -451,6 +468,7 @@ def run_carat(args, world, rank, local):
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline,
         "per_call": per_call,
+        "separate_calls": separate,
         "cpu_baseline": cpu_baseline,
         "parity_sample": parity,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,

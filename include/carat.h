@@ -228,8 +228,55 @@ carat_status carat_swa_attention_noalloc(float *out, const void *queries,
  * carat_swa_attention_noalloc (CARAT_NOALLOC_SCRATCH_BYTES). */
 size_t carat_noalloc_scratch_bytes(void);
 
-/* Workspace bytes the two attention calls need for these sizes (0 if the
- * sizes are invalid).  Pure host arithmetic; no CUDA call. */
+/*
+ * carat_swa_append_attention -- carat_ring_append followed by
+ * carat_swa_attention in one launch, without a displaced-row buffer.
+ *
+ * Same contract as the two calls in sequence (the pages' order: this step's
+ * K/V rows are written into the ring, then attention reads the ring in place
+ * -- "Improving Decode Throughput on Intel Gaudi 3", "Our approach"), except
+ * that the rings are passed as they are BEFORE this step: the kernel reads the
+ * old ring contents and this step's rows (k_new, v_new, layout as in
+ * carat_ring_append) as keys, and each 128-slot tile of the ring that holds a
+ * slot of a new row is overwritten only by the CTA that loads that tile,
+ * after its own copy of the tile has landed.  On return (in stream order) the
+ * rings hold exactly what carat_ring_append would have written.  When more
+ * than 64 rows share a KV head the rows are split over several CTAs per tile;
+ * then the new rows are written by a ring append launched right after the
+ * attention.  workspace: carat_swa_workspace_bytes(...) bytes.
+ * Supported: as carat_swa_attention, for (q_heads/kv_heads) <= 64 (otherwise
+ * CARAT_ERR_UNSUPPORTED).
+ */
+carat_status carat_swa_append_attention(float *out, const void *queries,
+                                        void *k_ring, void *v_ring, int num_rings,
+                                        const int32_t *ring_ids,
+                                        const void *k_new, const void *v_new,
+                                        const int32_t *context_lengths, int proposal_count,
+                                        int batch, int q_heads, int kv_heads, int head_dim,
+                                        int window, float scale,
+                                        void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * carat_global_append_verify_attention -- appending this step's rows to the
+ * global caches (rows context_length + j) followed by
+ * carat_global_verify_attention, in one launch.  The caches are passed as
+ * they are before this step; this step's rows are read from k_new / v_new and
+ * written to the caches by the kernel.  context_length + proposal_count must
+ * be <= capacity.  workspace: carat_global_workspace_bytes(...) bytes.
+ */
+carat_status carat_global_append_verify_attention(float *out, const void *queries,
+                                                  void *key_cache, void *value_cache,
+                                                  int num_caches, const int32_t *cache_ids,
+                                                  const void *k_new, const void *v_new,
+                                                  const int32_t *context_lengths,
+                                                  int proposal_count, int batch, int q_heads,
+                                                  int kv_heads, int head_dim, int capacity,
+                                                  float scale, void *workspace,
+                                                  size_t workspace_bytes, void *stream);
+
+/* Workspace bytes the attention calls need for these sizes (the same for the
+ * plain and the fused-append entry points; 0 if the sizes are invalid, or if
+ * the call needs no scratch).  Pure host arithmetic; no CUDA call. */
 size_t carat_swa_workspace_bytes(int batch, int proposal_count, int q_heads, int kv_heads,
                                  int head_dim, int window);
 size_t carat_global_workspace_bytes(int batch, int proposal_count, int q_heads,

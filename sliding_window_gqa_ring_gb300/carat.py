@@ -39,6 +39,7 @@ EXPORTED = (
     "carat_swa_workspace_bytes", "carat_global_workspace_bytes", "carat_get_device_status",
     "carat_status_string", "carat_abi_version", "carat_kernel_launches",
     "carat_swa_attention_noalloc", "carat_noalloc_scratch_bytes",
+    "carat_swa_append_attention", "carat_global_append_verify_attention",
 )
 
 
@@ -79,6 +80,12 @@ def _declare(lib):
                                                 i32, i32, i32, f32, vp]
     lib.carat_noalloc_scratch_bytes.restype = sz
     lib.carat_noalloc_scratch_bytes.argtypes = []
+    lib.carat_swa_append_attention.restype = i32
+    lib.carat_swa_append_attention.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32,
+                                               i32, i32, i32, f32, vp, sz, vp]
+    lib.carat_global_append_verify_attention.restype = i32
+    lib.carat_global_append_verify_attention.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, i32,
+                                                         i32, i32, i32, i32, i32, f32, vp, sz, vp]
     return lib
 
 
@@ -216,6 +223,40 @@ def carat_global_verify_attention(out, queries, key_cache, value_cache, context_
         _ptr(cache_ids), _ptr(context_lengths), k, batch, q_heads, kv_heads, head_dim, capacity,
         float(scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)), "carat_global_verify_attention")
+
+
+def carat_swa_append_attention(out, queries, k_ring, v_ring, k_new, v_new, context_lengths, *,
+                                scale, workspace, ring_ids=None, stream=None):
+    """Append this step's rows to the rings and attend, in one launch.  Rings
+    are passed as before the step; afterwards they hold the new rows."""
+    _expect(queries, torch.bfloat16, "queries")
+    _expect(out, torch.float32, "out")
+    _expect(k_new, torch.bfloat16, "k_new")
+    batch, k, q_heads, head_dim = queries.shape
+    num_rings, window, kv_heads, _ = k_ring.shape
+    _check(library().carat_swa_append_attention(
+        _ptr(out), _ptr(queries), _ptr(k_ring), _ptr(v_ring), num_rings, _ptr(ring_ids),
+        _ptr(k_new), _ptr(v_new), _ptr(context_lengths), k, batch, q_heads, kv_heads, head_dim,
+        window, float(scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "carat_swa_append_attention")
+
+
+def carat_global_append_verify_attention(out, queries, key_cache, value_cache, k_new, v_new,
+                                         context_lengths, *, scale, workspace, cache_ids=None,
+                                         stream=None):
+    """Append this step's rows to the global caches and run grouped verify
+    attention, in one launch."""
+    _expect(queries, torch.bfloat16, "queries")
+    _expect(out, torch.float32, "out")
+    _expect(k_new, torch.bfloat16, "k_new")
+    batch, k, q_heads, head_dim = queries.shape
+    num_caches, capacity, kv_heads, _ = key_cache.shape
+    _check(library().carat_global_append_verify_attention(
+        _ptr(out), _ptr(queries), _ptr(key_cache), _ptr(value_cache), num_caches,
+        _ptr(cache_ids), _ptr(k_new), _ptr(v_new), _ptr(context_lengths), k, batch, q_heads,
+        kv_heads, head_dim, capacity, float(scale), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)),
+        "carat_global_append_verify_attention")
 
 
 def carat_get_device_status(clear: bool = True, stream=None) -> int:

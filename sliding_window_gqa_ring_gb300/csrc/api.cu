@@ -139,7 +139,8 @@ SplitPlan swa_plan(int batch, int proposal_count, int q_heads, int kv_heads, int
     const int rows = group * proposal_count;
     const long long pairs = (long long)batch * kv_heads;
     if (tc_supported(head_dim, group, proposal_count)) {
-        const long long tiles = (window + kTcTileKeys - 1) / kTcTileKeys + (proposal_count > 1 ? 1 : 0);
+        // ring tiles + one tile of displaced rows or (fused append) new rows
+        const long long tiles = (window + kTcTileKeys - 1) / kTcTileKeys + 1;
         return tc_plan(pairs, row_groups_for(group, proposal_count), tiles, rows, head_dim,
                        tc_ctas_per_sm(head_dim, tc_rows_per_tile(group, proposal_count)), 4);
     }
@@ -153,7 +154,8 @@ SplitPlan global_plan(int batch, int proposal_count, int q_heads, int kv_heads, 
     const int rows = group * proposal_count;
     const long long pairs = (long long)batch * kv_heads;
     if (tc_supported(head_dim, group, proposal_count)) {
-        const long long tiles = (capacity + kTcTileKeys - 1) / kTcTileKeys;
+        // cache tiles + one tile of new rows (fused append)
+        const long long tiles = (capacity + kTcTileKeys - 1) / kTcTileKeys + 1;
         return tc_plan(pairs, row_groups_for(group, proposal_count), tiles, rows, head_dim,
                        tc_ctas_per_sm(head_dim, tc_rows_per_tile(group, proposal_count)), 8);
     }
@@ -353,6 +355,124 @@ carat_status carat_global_verify_attention(float *out, const void *queries, cons
     p.scale_log2 = scale * 1.4426950408889634f;
     p.source = KeySource::kLinear;
     return launch_status(launch_attention(p, plan, static_cast<cudaStream_t>(stream)));
+}
+
+// Shared by the two fused entry points: attention over the caches as they are
+// before this step plus this step's rows, which are then written into the
+// caches (by the attention kernel itself, or by a ring append launched after
+// it when several CTAs read each ring tile).
+static carat_status append_attention(float *out, const void *queries, void *k_base, void *v_base,
+                                     int num_ids, const int32_t *ids, const void *k_new,
+                                     const void *v_new, const int32_t *context_lengths,
+                                     int proposal_count, int batch, int q_heads, int kv_heads,
+                                     int head_dim, int window, int capacity, float scale,
+                                     void *workspace, size_t workspace_bytes, void *stream,
+                                     KeySource source) {
+    const bool ring = source == KeySource::kRing;
+    if (!attention_shape_ok(batch, proposal_count, q_heads, kv_heads, head_dim) ||
+        !std::isfinite(scale))
+        return CARAT_ERR_INVALID_ARG;
+    if (ring ? (window < 1 || proposal_count > window) : capacity < proposal_count)
+        return CARAT_ERR_INVALID_ARG;
+    carat_status st = attention_unsupported(proposal_count, q_heads, kv_heads, head_dim);
+    if (st != CARAT_OK) return st;
+    const int group = q_heads / kv_heads;
+    if (!tc_supported(head_dim, group, proposal_count)) return CARAT_ERR_UNSUPPORTED;
+    if (batch == 0) return CARAT_OK;
+    st = check_attention_common(out, queries, k_base, v_base, num_ids, ids, context_lengths, batch);
+    if (st != CARAT_OK) return st;
+    if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return CARAT_ERR_INVALID_ARG;
+    const SplitPlan plan =
+        ring ? swa_plan(batch, proposal_count, q_heads, kv_heads, head_dim, window)
+             : global_plan(batch, proposal_count, q_heads, kv_heads, head_dim, capacity);
+    if (plan.total > 0 && (!workspace || workspace_bytes < plan.total || !aligned16(workspace)))
+        return CARAT_ERR_WORKSPACE;
+
+    AttnParams p{};
+    p.q = static_cast<const uint16_t *>(queries);
+    p.k_base = static_cast<const uint16_t *>(k_base);
+    p.v_base = static_cast<const uint16_t *>(v_base);
+    p.ids = ids;
+    p.displaced = nullptr;
+    p.context_lengths = context_lengths;
+    p.out = out;
+    p.part_ml = static_cast<float2 *>(workspace);
+    p.part_o = plan.total ? reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.ml_bytes)
+                          : nullptr;
+    p.dev_status = device_status_ptr();
+    p.num_ids = num_ids;
+    p.batch = batch;
+    p.k = proposal_count;
+    p.q_heads = q_heads;
+    p.kv_heads = kv_heads;
+    p.head_dim = head_dim;
+    p.group = group;
+    p.rows = group * proposal_count;
+    p.window = ring ? window : 0;
+    p.capacity = ring ? 0 : capacity;
+    p.chunk = plan.chunk;
+    p.nchunks = plan.nchunks;
+    p.tiles_per_chunk = plan.tiles_per_chunk;
+    p.direct = plan.direct ? 1 : 0;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.source = source;
+    p.fused = 1;
+    p.k_new = static_cast<const uint16_t *>(k_new);
+    p.v_new = static_cast<const uint16_t *>(v_new);
+    p.k_dst = static_cast<uint16_t *>(k_base);
+    p.v_dst = static_cast<uint16_t *>(v_base);
+    // Several row groups read every ring tile: none of them may overwrite a
+    // slot, so a ring append follows the attention instead.
+    p.fused_write = (!ring || row_groups_for(group, proposal_count) == 1) ? 1 : 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_attention(p, plan, s);
+    if (e == cudaSuccess && !p.fused_write) {
+        AppendParams a{};
+        a.k_ring = static_cast<uint16_t *>(k_base);
+        a.v_ring = static_cast<uint16_t *>(v_base);
+        a.ids = ids;
+        a.k_new = p.k_new;
+        a.v_new = p.v_new;
+        a.context_lengths = context_lengths;
+        a.displaced = nullptr;
+        a.dev_status = p.dev_status;
+        a.num_ids = num_ids;
+        a.batch = batch;
+        a.k = proposal_count;
+        a.kv_heads = kv_heads;
+        a.head_dim = head_dim;
+        a.window = window;
+        e = launch_ring_append(a, s);
+    }
+    return launch_status(e);
+}
+
+carat_status carat_swa_append_attention(float *out, const void *queries, void *k_ring,
+                                        void *v_ring, int num_rings, const int32_t *ring_ids,
+                                        const void *k_new, const void *v_new,
+                                        const int32_t *context_lengths, int proposal_count,
+                                        int batch, int q_heads, int kv_heads, int head_dim,
+                                        int window, float scale, void *workspace,
+                                        size_t workspace_bytes, void *stream) {
+    return append_attention(out, queries, k_ring, v_ring, num_rings, ring_ids, k_new, v_new,
+                            context_lengths, proposal_count, batch, q_heads, kv_heads, head_dim,
+                            window, 0, scale, workspace, workspace_bytes, stream,
+                            KeySource::kRing);
+}
+
+carat_status carat_global_append_verify_attention(float *out, const void *queries,
+                                                  void *key_cache, void *value_cache,
+                                                  int num_caches, const int32_t *cache_ids,
+                                                  const void *k_new, const void *v_new,
+                                                  const int32_t *context_lengths,
+                                                  int proposal_count, int batch, int q_heads,
+                                                  int kv_heads, int head_dim, int capacity,
+                                                  float scale, void *workspace,
+                                                  size_t workspace_bytes, void *stream) {
+    return append_attention(out, queries, key_cache, value_cache, num_caches, cache_ids, k_new,
+                            v_new, context_lengths, proposal_count, batch, q_heads, kv_heads,
+                            head_dim, 0, capacity, scale, workspace, workspace_bytes, stream,
+                            KeySource::kLinear);
 }
 
 carat_status carat_get_device_status(int32_t *host_out, int clear, void *stream) {

@@ -89,6 +89,8 @@ struct TcMaps {
     CUtensorMap v;
     CUtensorMap disp;  // (D, Hkv, 2, B*(k-1))    displaced rows, K (0) / V (1)
     CUtensorMap q;     // (D, Hq, k, B)           queries
+    CUtensorMap knew;  // (D, Hkv, B*k)           this step's rows (fused append)
+    CUtensorMap vnew;
 };
 
 struct TcPlan {
@@ -191,8 +193,14 @@ __global__ void __launch_bounds__(kThreads, MINB)
     const bool ok = request_ok(p, b, &id, &ctx);
     const long long key_count = ctx + p.k;
     const bool ring = p.source == KeySource::kRing;
-    int disp_tile = -1;
-    const int ntiles = ok ? tc_request_tiles(p.source, p.window, p.k, key_count, &disp_tile) : 0;
+    int special = -1;
+    const int ntiles =
+        ok ? tc_request_tiles(p.source, p.window, p.k, key_count, p.fused != 0, &special) : 0;
+    const int disp_tile = p.fused ? -1 : special;   // displaced rows (append done before)
+    const int new_tile = p.fused ? special : -1;    // this step's rows (fused append)
+    // Tokens the caches hold for this call: all key_count of them, or with a
+    // fused append only the context_length older ones.
+    const long long held_tokens = p.fused ? ctx : key_count;
     const int t0 = chunk * plan.tiles_per_chunk;
     const int t1 = min(t0 + plan.tiles_per_chunk, ntiles);
     const int pos0 = rg * plan.pos_per_group;                       // first position of the group
@@ -264,6 +272,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
     const uint32_t tmem = *tmem_slot;
     const uint32_t tmem_o = tmem + 2 * N;  // O^T: KS blocks of N columns (S^T buffers: 0, N)
     const int n = t1 - t0;                 // tiles of this CTA
+    // Processing order of the CTA's tiles: the small tile of this step's rows
+    // (fused append; always the request's last tile index) goes first, so its
+    // work overlaps the first loads of the big tiles instead of ending the CTA.
+    const bool new_first = new_tile >= t0 && new_tile < t1;
+    auto tile_at = [t0, new_first, new_tile](int x) {
+        return new_first ? (x == 0 ? new_tile : t0 + x - 1) : t0 + x;
+    };
     // Load / consume order of the 128-key tiles' K and V parts: K(0), then
     // K(x+1) before V(x), then V(n-1), so the next tile's keys stream in and
     // its scores are computed while this tile's softmax runs.  Part index of
@@ -297,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     x = (part - 1) / 2 + ((part - 1) % 2 == 0 ? 1 : 0);
                     is_v = (part - 1) % 2 == 1;
                 }
-                const int i = t0 + x;
+                const int i = tile_at(x);
                 for (int ks = 0; ks < KS; ++ks) {
                     const int s = cnt % NS;
                     if (cnt >= NS && !wait_or_abort(&empty[s], ((cnt / NS) & 1) ^ 1, abort_flag,
@@ -305,8 +320,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
                         alive = false;
                         break;
                     }
-                    tc::mbar_arrive_expect_tx(&full[s], i == disp_tile ? 2 * kDispBoxBytes
-                                                                       : kStageBytes);
+                    tc::mbar_arrive_expect_tx(&full[s], (i == disp_tile || i == new_tile)
+                                                            ? 2 * kDispBoxBytes
+                                                            : kStageBytes);
                     const int d0 = ks * 128;
                     uint8_t *dst = smem + s * kStageBytes;
 #pragma unroll
@@ -314,6 +330,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
                         if (i == disp_tile) {
                             tc::tma_load_4d(dst + box * kBoxBytes, &maps.disp, d0 + box * 64, c,
                                             is_v ? 1 : 0, b * (p.k - 1), &full[s], pol);
+                        } else if (i == new_tile) {
+                            tc::tma_load_3d(dst + box * kBoxBytes, is_v ? &maps.vnew : &maps.knew,
+                                            d0 + box * 64, c, b * p.k, &full[s], pol);
                         } else {
                             const long long row = ring ? (long long)id * p.window + (long long)i * kTileKeys
                                                        : (long long)id * p.capacity + (long long)i * kTileKeys;
@@ -417,9 +436,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
         }
         bool alive = true;
         int idx = 0;
-        // Slot that holds the newest token (ring source).
-        const long long head_slot = ring ? (key_count - 1) % p.window : 0;
-        for (int i = t0; i < t1; ++i, ++idx) {
+        // Slot that holds the newest token the caches hold (ring source).
+        const long long newest = held_tokens - 1;
+        const long long head_slot = (ring && newest >= 0) ? newest % p.window : 0;
+        // Fused append: slot of this step's first row (ring source).
+        const int base_slot = (ring && p.fused) ? (int)(ctx % p.window) : 0;
+        for (; idx < n; ++idx) {
+            const int i = tile_at(idx);
             // warp-uniform: the TMEM load below is warp-collective
             const bool w_ok = __all_sync(
                 kFull, wait_or_abort(&s_full[idx & 1], (idx >> 1) & 1, abort_flag, p.dev_status));
@@ -441,7 +464,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
             }
             // Position of key t of tile i and which rows may see it.
             KeyInfo ki;
-            if (ring && i == disp_tile) {
+            if (i == new_tile) {
+                ki.pos = t < p.k ? ctx + t : -1;
+                ki.data = t < p.k;
+            } else if (ring && i == disp_tile) {
                 ki.pos = (t < p.k - 1) ? ctx - p.window + 1 + t : -1;
                 ki.data = t < p.k - 1 && ki.pos >= 0;
             } else if (ring) {
@@ -450,11 +476,11 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 const int slot = i * kTileKeys + t;
                 long long delta = head_slot - slot;
                 if (delta < 0) delta += p.window;
-                ki.pos = slot < p.window ? key_count - 1 - delta : -1;
+                ki.pos = (slot < p.window && newest >= 0) ? newest - delta : -1;
                 ki.data = ki.pos >= 0;
             } else {
                 const long long u = (long long)i * kTileKeys + t;
-                ki.pos = u < key_count ? u : -1;
+                ki.pos = u < held_tokens ? u : -1;
                 ki.data = ki.pos >= 0;
             }
             // Query j of the group (position ctx + pos0 + j) sees the key iff
@@ -545,10 +571,21 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 // Rows of the tile that hold no token of this request: zero their
                 // V rows so their contents cannot reach O through P = 0.
                 const bool tile_partial =
-                    (ring && i == disp_tile) ||
-                    (ring && ((long long)(i + 1) * kTileKeys > min((long long)p.window, key_count))) ||
-                    (!ring && (long long)(i + 1) * kTileKeys > key_count);
-                if (tile_partial) {
+                    i == disp_tile || i == new_tile ||
+                    (ring && ((long long)(i + 1) * kTileKeys > min((long long)p.window, held_tokens))) ||
+                    (!ring && (long long)(i + 1) * kTileKeys > held_tokens);
+                // Fused append into a ring: this CTA is the only one that loads
+                // tile i, and it overwrites slots of the tile once its own
+                // copies of the tile have landed.
+                bool tile_writes = false;
+                if (p.fused_write && ring && i != new_tile) {
+                    for (int j = 0; j < p.k; ++j) {
+                        int sj = base_slot + j;
+                        if (sj >= p.window) sj -= p.window;
+                        tile_writes |= sj / kTileKeys == i;
+                    }
+                }
+                if (tile_partial || tile_writes) {
                     for (int vs = 0; vs < KS; ++vs) {
                         const uint32_t x_cnt = (uint32_t)v_part(idx) * KS + vs;
                         const int s = x_cnt % NS;
@@ -556,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                             alive = false;
                             break;
                         }
-                        if (!ki.data) {
+                        if (!ki.data && tile_partial) {
                             uint8_t *row0p = smem + s * kStageBytes + t * 128;
 #pragma unroll
                             for (int box = 0; box < 2; ++box)
@@ -575,6 +612,35 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 break;
             }
             tc::mbar_arrive(p_full);
+            if (p.fused_write && (ring || rg == 0)) {
+                // Write this step's rows whose slot this tile covers (ring), or
+                // that no loaded tile covers, or every row (cache), from the new
+                // rows to the caches: warp q4 takes rows j = q4, q4 + 4, ...
+                for (int j = q4; j < p.k; j += 4) {
+                    long long dst_row;
+                    int writer;
+                    if (ring) {
+                        int sj = base_slot + j;
+                        if (sj >= p.window) sj -= p.window;
+                        writer = sj / kTileKeys < new_tile ? sj / kTileKeys : new_tile;
+                        dst_row = (long long)id * p.window + sj;
+                    } else {
+                        writer = new_tile;
+                        dst_row = (long long)id * p.capacity + ctx + j;
+                    }
+                    if (writer != i) continue;
+                    const size_t src = (((size_t)b * p.k + j) * p.kv_heads + c) * D;
+                    const size_t dst = ((size_t)dst_row * p.kv_heads + c) * D;
+                    const uint4 *ks = reinterpret_cast<const uint4 *>(p.k_new + src);
+                    const uint4 *vs = reinterpret_cast<const uint4 *>(p.v_new + src);
+                    uint4 *kd = reinterpret_cast<uint4 *>(p.k_dst + dst);
+                    uint4 *vd = reinterpret_cast<uint4 *>(p.v_dst + dst);
+                    for (int e = lane; e < D / 8; e += 32) {
+                        kd[e] = ks[e];
+                        vd[e] = vs[e];
+                    }
+                }
+            }
         }
         // ------------------------------------------------------------ epilogue
         if (alive) {
@@ -720,6 +786,16 @@ cudaError_t launch_attention_tc(const AttnParams &p, int tiles_per_chunk, cudaSt
             return cudaErrorInvalidValue;
     } else {
         maps.disp = maps.k;
+    }
+    if (p.fused) {
+        const uint64_t dimsn[3] = {D, (uint64_t)p.kv_heads, (uint64_t)p.batch * p.k};
+        const uint32_t boxn[3] = {64, 1, (uint32_t)kDispRows};
+        if (!make_bf16_tensor_map(&maps.knew, p.k_new, 3, dimsn, strides3, boxn, true) ||
+            !make_bf16_tensor_map(&maps.vnew, p.v_new, 3, dimsn, strides3, boxn, true))
+            return cudaErrorInvalidValue;
+    } else {
+        maps.knew = maps.k;
+        maps.vnew = maps.v;
     }
     {
         const uint64_t dimsq[4] = {D, (uint64_t)p.q_heads, (uint64_t)p.k, (uint64_t)p.batch};

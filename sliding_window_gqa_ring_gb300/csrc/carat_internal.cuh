@@ -40,6 +40,15 @@ struct AttnParams {
     int nchunks;                // splits per (request, KV head)
     int tiles_per_chunk;        // tensor-core path: 128-key tiles per split (0: CUDA-core path)
     int direct;                 // 1: one split covers every key, the kernel writes `out` itself
+    // Fused append (tensor-core path): the caches hold the tokens before this
+    // step and this step's rows come from k_new / v_new [B][k][Hkv][D]; when
+    // fused_write is set the kernel also writes them into k_dst / v_dst.
+    int fused;
+    int fused_write;
+    const uint16_t *k_new;
+    const uint16_t *v_new;
+    uint16_t *k_dst;
+    uint16_t *v_dst;
     float scale_log2;           // softmax scale * log2(e)
     KeySource source;
 };
@@ -113,21 +122,34 @@ __device__ __forceinline__ int request_error_bits(const AttnParams &p, int id, l
     return bits;
 }
 
-// Tensor-core path: 128-key tiles a request needs.  Ring: the tiles covering
-// the slots that hold tokens (all `window` slots once the ring has wrapped),
-// plus one tile of displaced rows when some exist (key_count > window and
-// k > 1).  Cache: ceil(key_count / 128).  *disp_tile = index of the displaced
-// tile, or -1.
+// Tensor-core path: 128-key tiles a request needs, and the index of its
+// one special tile (or -1).
+//  * Ring, append done before the call: the tiles covering the slots that hold
+//    tokens (all `window` slots once the ring has wrapped), plus one tile of
+//    displaced rows when some exist (key_count > window and k > 1).
+//  * Ring, fused append: the tiles covering the slots that hold the tokens
+//    before this step (min(context_length, window) slots), plus one tile of
+//    this step's k new rows.
+//  * Cache: ceil(key_count / 128); fused append: ceil(context_length / 128)
+//    tiles of old rows plus the tile of new rows.
 __host__ __device__ __forceinline__ int tc_request_tiles(KeySource src, int window, int k,
-                                                         long long key_count, int *disp_tile) {
+                                                         long long key_count, bool fused,
+                                                         int *special_tile) {
+    const long long ctx = key_count - k;
     if (src == KeySource::kRing) {
-        const long long held = key_count < window ? key_count : window;
+        const long long tokens = fused ? ctx : key_count;
+        const long long held = tokens < window ? tokens : window;
         const int ring_tiles = (int)((held + 127) / 128);
-        const bool disp = k > 1 && key_count > window;
-        *disp_tile = disp ? ring_tiles : -1;
-        return ring_tiles + (disp ? 1 : 0);
+        const bool extra = fused || (k > 1 && key_count > window);
+        *special_tile = extra ? ring_tiles : -1;
+        return ring_tiles + (extra ? 1 : 0);
     }
-    *disp_tile = -1;
+    if (fused) {
+        const int old_tiles = (int)((ctx + 127) / 128);
+        *special_tile = old_tiles;
+        return old_tiles + 1;
+    }
+    *special_tile = -1;
     return (int)((key_count + 127) / 128);
 }
 

@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine(const AttnParams
     int nch = p.nchunks;
     if (p.tiles_per_chunk > 0) {
         int disp;
-        const int tiles = tc_request_tiles(p.source, p.window, p.k, ctx + p.k, &disp);
+        const int tiles = tc_request_tiles(p.source, p.window, p.k, ctx + p.k, p.fused != 0, &disp);
         nch = min(nch, (tiles + p.tiles_per_chunk - 1) / p.tiles_per_chunk);
     }
     nch = min(nch, kMaxCombineChunks);

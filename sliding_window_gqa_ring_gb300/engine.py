@@ -68,9 +68,20 @@ class SlidingLayer:
                                   displaced=self.displaced, stream=stream)
         return out
 
-    def step(self, queries, k_new, v_new, context_lengths, ring_ids=None, out=None, stream=None):
-        self.append(k_new, v_new, context_lengths, ring_ids=ring_ids, stream=stream)
-        return self.attend(queries, context_lengths, ring_ids=ring_ids, out=out, stream=stream)
+    def step(self, queries, k_new, v_new, context_lengths, ring_ids=None, out=None, stream=None,
+             fused=True):
+        """This step's append then attention: one fused launch by default, or
+        carat_ring_append + carat_swa_attention (fused=False)."""
+        if not fused:
+            self.append(k_new, v_new, context_lengths, ring_ids=ring_ids, stream=stream)
+            return self.attend(queries, context_lengths, ring_ids=ring_ids, out=out, stream=stream)
+        if out is None:
+            out = torch.empty(queries.shape, dtype=torch.float32, device=self.device)
+        carat.carat_swa_append_attention(out, queries, self.k_ring, self.v_ring, k_new, v_new,
+                                         context_lengths, scale=self.scale,
+                                         workspace=self.workspace, ring_ids=ring_ids,
+                                         stream=stream)
+        return out
 
 
 class GlobalLayer:
@@ -108,9 +119,21 @@ class GlobalLayer:
                                             stream=stream)
         return out
 
-    def step(self, queries, k_new, v_new, context_lengths, cache_ids=None, out=None, stream=None):
-        self.append(k_new, v_new, context_lengths, cache_ids=cache_ids, stream=stream)
-        return self.attend(queries, context_lengths, cache_ids=cache_ids, out=out, stream=stream)
+    def step(self, queries, k_new, v_new, context_lengths, cache_ids=None, out=None, stream=None,
+             fused=True):
+        """This step's append then verify attention: one fused launch by
+        default, or carat_ring_append + carat_global_verify_attention."""
+        if not fused:
+            self.append(k_new, v_new, context_lengths, cache_ids=cache_ids, stream=stream)
+            return self.attend(queries, context_lengths, cache_ids=cache_ids, out=out,
+                               stream=stream)
+        if out is None:
+            out = torch.empty(queries.shape, dtype=torch.float32, device=self.device)
+        carat.carat_global_append_verify_attention(out, queries, self.key_cache, self.value_cache,
+                                                   k_new, v_new, context_lengths,
+                                                   scale=self.scale, workspace=self.workspace,
+                                                   cache_ids=cache_ids, stream=stream)
+        return out
 
 
 # ---------------------------------------------------------------------------

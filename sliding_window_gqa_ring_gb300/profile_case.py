@@ -3,10 +3,11 @@
     python -m sliding_window_gqa_ring_gb300.profile_case --case swa_mixed --calls 3
 
 The layer is staged from the seeded workloads in ``synth`` (rings or caches
-written with carat_ring_append, then this step's append), after which only
-the attention call repeats, so a profiler filtered on the attention kernels
-sees exactly ``--calls`` launches of each.  Every case keeps a few GB or less
-on the device and reads more than the 129 MB L2 per call.
+written with carat_ring_append), then the step's fused append+attention call
+repeats ``--calls`` times (with ``--separate``: one carat_ring_append, then the
+attention call alone repeats), so a profiler filtered on the attention kernel
+sees exactly ``--calls`` launches.  Every case keeps a few GB or less on the
+device and reads more than the 129 MB L2 per call.
 """
 from __future__ import annotations
 
@@ -30,6 +31,8 @@ def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--case", choices=sorted(CASES), required=True)
     ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--separate", action="store_true",
+                    help="time carat_ring_append + the attention call instead of the fused call")
     args = ap.parse_args()
     w = CASES[args.case]()
     if w.window:
@@ -42,10 +45,14 @@ def main():
                                    kv_heads=w.kv_heads, head_dim=w.head_dim,
                                    max_proposals=w.proposal_count, scale=w.scale)
         inp = engine.stage_global(w, 0, layer, keep_history=False)
-    layer.append(inp.k_new, inp.v_new, inp.context_lengths)
     out = torch.empty(inp.queries.shape, dtype=torch.float32, device=layer.device)
-    for _ in range(args.calls):
-        layer.attend(inp.queries, inp.context_lengths, out=out)
+    if args.separate:
+        layer.append(inp.k_new, inp.v_new, inp.context_lengths)
+        for _ in range(args.calls):
+            layer.attend(inp.queries, inp.context_lengths, out=out)
+    else:
+        for _ in range(args.calls):
+            layer.step(inp.queries, inp.k_new, inp.v_new, inp.context_lengths, out=out)
     torch.cuda.synchronize()
     status = carat.carat_get_device_status(clear=True)
     print(f"{args.case}: {args.calls} calls, device status {status:#x}")

@@ -27,12 +27,12 @@ def _cuda():
     assert carat.carat_get_device_status(clear=True) == 0
 
 
-def _run_sliding(orc, w, layer_index=0, requests=None, fill=0.0, check_ring=True):
+def _run_sliding(orc, w, layer_index=0, requests=None, fill=0.0, check_ring=True, fused=True):
     layer = engine.SlidingLayer(w.batch, window=w.window, q_heads=w.q_heads, kv_heads=w.kv_heads,
                                 head_dim=w.head_dim, max_proposals=w.proposal_count,
                                 scale=w.scale, fill=fill)
     inp = engine.stage_sliding(w, layer_index, layer, requests=requests)
-    out = layer.step(inp.queries, inp.k_new, inp.v_new, inp.context_lengths)
+    out = layer.step(inp.queries, inp.k_new, inp.v_new, inp.context_lengths, fused=fused)
     torch.cuda.synchronize()
     out_h = out.cpu().numpy()
     reqs = list(range(w.batch)) if requests is None else list(requests)
@@ -52,7 +52,7 @@ def _run_sliding(orc, w, layer_index=0, requests=None, fill=0.0, check_ring=True
             exp_v, _ = orc.ring_expected(vh, first, kc, w.window)
             assert np.array_equal(k_ring[b][valid], exp_k[valid]), f"K ring bytes, request {b}"
             assert np.array_equal(v_ring[b][valid], exp_v[valid]), f"V ring bytes, request {b}"
-            if w.proposal_count > 1:
+            if w.proposal_count > 1 and not fused:
                 exp_d, dvalid = orc.displaced_expected(kh, vh, first, int(w.context_lengths[b]),
                                                        w.proposal_count, w.window)
                 assert np.array_equal(disp[b][:w.proposal_count - 1][dvalid], exp_d[dvalid]), \
@@ -60,12 +60,12 @@ def _run_sliding(orc, w, layer_index=0, requests=None, fill=0.0, check_ring=True
     return out_h
 
 
-def _run_global(orc, w, layer_index=0, requests=None, rows=None, fill=0.0):
+def _run_global(orc, w, layer_index=0, requests=None, rows=None, fill=0.0, fused=True):
     layer = engine.GlobalLayer(w.batch, capacity=w.capacity, q_heads=w.q_heads,
                                kv_heads=w.kv_heads, head_dim=w.head_dim,
                                max_proposals=w.proposal_count, scale=w.scale, fill=fill)
     inp = engine.stage_global(w, layer_index, layer, requests=requests)
-    out = layer.step(inp.queries, inp.k_new, inp.v_new, inp.context_lengths)
+    out = layer.step(inp.queries, inp.k_new, inp.v_new, inp.context_lengths, fused=fused)
     torch.cuda.synchronize()
     out_h = out.cpu().numpy()
     reqs = list(range(w.batch)) if requests is None else list(requests)
@@ -93,35 +93,45 @@ def _run_global(orc, w, layer_index=0, requests=None, rows=None, fill=0.0):
 
 
 # --- the five workloads ------------------------------------------------------
+# Each runs through the fused append+attention launch and through the separate
+# carat_ring_append + attention calls; ring and cache bytes are checked either way.
 
-def test_sliding_single_request_1500(orc):
-    _run_sliding(orc, synth.sliding_single())
-
-
-def test_sliding_batched_56(orc):
-    _run_sliding(orc, synth.sliding_batched())
+FUSED = pytest.mark.parametrize("fused", [True, False], ids=["fused", "separate"])
 
 
-def test_global_single_6005(orc):
-    _run_global(orc, synth.global_single())
+@FUSED
+def test_sliding_single_request_1500(orc, fused):
+    _run_sliding(orc, synth.sliding_single(), fused=fused)
 
 
+@FUSED
+def test_sliding_batched_56(orc, fused):
+    _run_sliding(orc, synth.sliding_batched(), fused=fused)
+
+
+@FUSED
+def test_global_single_6005(orc, fused):
+    _run_global(orc, synth.global_single(), fused=fused)
+
+
+@FUSED
 @pytest.mark.parametrize("k", [4, 15])
-def test_global_sweep(orc, k):
+def test_global_sweep(orc, k, fused):
     w = synth.global_sweep(k)
     rows = [(0, 0), (k - 1, 15), (k // 2, 7), (1, 8), (k - 1, 0), (0, 9)]
-    _run_global(orc, w, rows=rows)
+    _run_global(orc, w, rows=rows, fused=fused)
 
 
-def test_mixed_step_sampled(orc):
+@FUSED
+def test_mixed_step_sampled(orc, fused):
     sliding, glob = synth.mixed_step()
     ctx = sliding.context_lengths
     order = np.argsort(ctx)
     sample = sorted({int(order[0]), int(order[1]), int(order[len(order) // 2]), int(order[-1]),
                      int(np.argmin(np.abs(ctx - 1024))), 5})
     for layer_index in range(sliding.layers):
-        _run_sliding(orc, sliding, layer_index=layer_index, requests=sample)
-    _run_global(orc, glob, requests=sample, rows=[(0, 0), (3, 15), (2, 6), (1, 9)])
+        _run_sliding(orc, sliding, layer_index=layer_index, requests=sample, fused=fused)
+    _run_global(orc, glob, requests=sample, rows=[(0, 0), (3, 15), (2, 6), (1, 9)], fused=fused)
 
 
 # --- edge cases ----------------------------------------------------------------
@@ -134,15 +144,18 @@ SLIDING_EDGES = [
     ([15, 16, 17, 1038, 1039, 1040, 5000], 15, 2, 1, 256),
     ([16, 1040, 1041, 4096], 16, 8, 8, 512),
     ([300, 1024 + 63, 1024 + 65], 2, 16, 2, 512),
+    ([100, 1030, 2000], 16, 16, 2, 512),  # 128 rows per KV head: two row groups
+    ([7, 1031, 3000], 5, 6, 2, 256),      # 3 heads per KV head (rows not a power of two)
 ]
 
 
+@FUSED
 @pytest.mark.parametrize("case", range(len(SLIDING_EDGES)))
-def test_sliding_edges(orc, case):
+def test_sliding_edges(orc, case, fused):
     kcs, k, hq, hkv, d = SLIDING_EDGES[case]
     w = synth.small(f"swa_edge{case}", seed=2000 + case, batch=len(kcs), proposal_count=k,
                     q_heads=hq, kv_heads=hkv, head_dim=d, key_counts=kcs, window=1024)
-    _run_sliding(orc, w, fill=float("nan"))
+    _run_sliding(orc, w, fill=float("nan"), fused=fused)
 
 
 GLOBAL_EDGES = [
@@ -151,16 +164,19 @@ GLOBAL_EDGES = [
     ([15, 16, 200, 1000], 15, 16, 2, 512, 1024),
     ([16, 17, 4096], 16, 8, 1, 256, 4096),
     ([100, 257, 2049], 3, 4, 4, 256, 2049),
+    ([128, 129, 5000], 16, 16, 2, 512, 5000),   # two row groups
+    ([5, 640, 1300], 3, 10, 2, 256, 1408),      # 5 heads per KV head
 ]
 
 
+@FUSED
 @pytest.mark.parametrize("case", range(len(GLOBAL_EDGES)))
-def test_global_edges(orc, case):
+def test_global_edges(orc, case, fused):
     kcs, k, hq, hkv, d, cap = GLOBAL_EDGES[case]
     w = synth.small(f"global_edge{case}", seed=3000 + case, batch=len(kcs), proposal_count=k,
                     q_heads=hq, kv_heads=hkv, head_dim=d, key_counts=kcs, capacity=cap,
                     outlier_fraction=0.01)
-    _run_global(orc, w, fill=float("nan"))
+    _run_global(orc, w, fill=float("nan"), fused=fused)
 
 
 def _probe_values(n_keys, d, marks):
