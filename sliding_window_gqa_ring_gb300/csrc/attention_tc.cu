@@ -248,29 +248,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
     uint8_t *s_q = smem + L::kOffQ;
     uint8_t *s_p = smem + L::kOffP;
 
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < NS; ++i) {
-            tc::mbar_init(&full[i], 1);
-            tc::mbar_init(&empty[i], 1);
-        }
-        tc::mbar_init(&s_full[0], 1);
-        tc::mbar_init(&s_full[1], 1);
-        tc::mbar_init(p_full, 128);
-        tc::mbar_init(o_done, 1);
-        tc::mbar_init(q_full, 1);
-        tc::mbar_init(fin, 1);
-        *abort_flag = 0;
-        tc::fence_mbar_init();
-    }
-    if (warp == 1) {
-        tc::tmem_alloc(tmem_slot, L::kTmemCols);
-        tc::tmem_relinquish();
-    }
-    tc::tc_fence_before();
-    __syncthreads();
-    tc::tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_o = tmem + 2 * N;  // O^T: KS blocks of N columns (S^T buffers: 0, N)
     const int n = t1 - t0;                 // tiles of this CTA
     // Processing order of the CTA's tiles: the small tile of this step's rows
     // (fused append; always the request's last tile index) goes first, so its
@@ -285,64 +262,103 @@ __global__ void __launch_bounds__(kThreads, MINB)
     // V(x) in that order (each part is KS stages):
     auto v_part = [n](int x) { return x == n - 1 ? 2 * n - 1 : 2 * x + 2; };
 
+    // Producer state (thread 0): the next stage load to issue.
+    uint32_t cnt = 0;
+    int ppart = 0, pks = 0;
+    bool alive_p = true;
+    uint64_t pol = 0;
+    // Issue stage loads in order until `limit` stages have been issued or the
+    // tiles run out; a stage is reused only after the MMA released it.
+    auto produce = [&](uint32_t limit) {
+        while (alive_p && ppart < 2 * n && cnt < limit) {
+            int x;
+            bool is_v;
+            if (ppart == 0) {
+                x = 0;
+                is_v = false;
+            } else if (ppart == 2 * n - 1) {
+                x = n - 1;
+                is_v = true;
+            } else {
+                x = (ppart - 1) / 2 + ((ppart - 1) % 2 == 0 ? 1 : 0);
+                is_v = (ppart - 1) % 2 == 1;
+            }
+            const int i = tile_at(x);
+            const int s = cnt % NS;
+            if (cnt >= NS &&
+                !wait_or_abort(&empty[s], ((cnt / NS) & 1) ^ 1, abort_flag, p.dev_status)) {
+                alive_p = false;
+                break;
+            }
+            tc::mbar_arrive_expect_tx(&full[s], (i == disp_tile || i == new_tile)
+                                                    ? 2 * kDispBoxBytes
+                                                    : kStageBytes);
+            const int d0 = pks * 128;
+            uint8_t *dst = smem + s * kStageBytes;
+#pragma unroll
+            for (int box = 0; box < 2; ++box) {
+                if (i == disp_tile) {
+                    tc::tma_load_4d(dst + box * kBoxBytes, &maps.disp, d0 + box * 64, c,
+                                    is_v ? 1 : 0, b * (p.k - 1), &full[s], pol);
+                } else if (i == new_tile) {
+                    tc::tma_load_3d(dst + box * kBoxBytes, is_v ? &maps.vnew : &maps.knew,
+                                    d0 + box * 64, c, b * p.k, &full[s], pol);
+                } else {
+                    const long long row = ring ? (long long)id * p.window + (long long)i * kTileKeys
+                                               : (long long)id * p.capacity + (long long)i * kTileKeys;
+                    tc::tma_load_3d(dst + box * kBoxBytes, is_v ? &maps.v : &maps.k,
+                                    d0 + box * 64, c, (int)row, &full[s], pol);
+                }
+            }
+            ++cnt;
+            if (++pks == KS) {
+                pks = 0;
+                ++ppart;
+            }
+        }
+    };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            tc::mbar_init(&full[i], 1);
+            tc::mbar_init(&empty[i], 1);
+        }
+        tc::mbar_init(&s_full[0], 1);
+        tc::mbar_init(&s_full[1], 1);
+        tc::mbar_init(p_full, 128);
+        tc::mbar_init(o_done, 1);
+        tc::mbar_init(q_full, 1);
+        tc::mbar_init(fin, 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+        // Start streaming before the block-wide barrier: this thread made the
+        // barriers, and the first NS stages need no release.
+        pol = tc::l2_evict_first_policy();
+        tc::tma_prefetch_map(&maps.k);
+        tc::tma_prefetch_map(&maps.v);
+        tc::tma_prefetch_map(&maps.q);
+        tc::mbar_arrive_expect_tx(q_full, (D / 64) * 128 * p.group * plan.pos_per_group);
+#pragma unroll
+        for (int db = 0; db < D / 64; ++db)
+            tc::tma_load_4d(s_q + db * L::kQBlock, &maps.q, db * 64, c * p.group, pos0, b,
+                            q_full, pol);
+        produce(NS);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, L::kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem_o = tmem + 2 * N;  // O^T: KS blocks of N columns (S^T buffers: 0, N)
+
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            const uint64_t pol = tc::l2_evict_first_policy();
-            tc::tma_prefetch_map(&maps.k);
-            tc::tma_prefetch_map(&maps.v);
-            tc::tma_prefetch_map(&maps.q);
-            tc::mbar_arrive_expect_tx(q_full, (D / 64) * 128 * p.group * plan.pos_per_group);
-#pragma unroll
-            for (int db = 0; db < D / 64; ++db)
-                tc::tma_load_4d(s_q + db * L::kQBlock, &maps.q, db * 64, c * p.group, pos0, b,
-                                q_full, pol);
-            uint32_t cnt = 0;
-            bool alive = true;
-            for (int part = 0; part < 2 * n && alive; ++part) {
-                int x;
-                bool is_v;
-                if (part == 0) {
-                    x = 0;
-                    is_v = false;
-                } else if (part == 2 * n - 1) {
-                    x = n - 1;
-                    is_v = true;
-                } else {
-                    x = (part - 1) / 2 + ((part - 1) % 2 == 0 ? 1 : 0);
-                    is_v = (part - 1) % 2 == 1;
-                }
-                const int i = tile_at(x);
-                for (int ks = 0; ks < KS; ++ks) {
-                    const int s = cnt % NS;
-                    if (cnt >= NS && !wait_or_abort(&empty[s], ((cnt / NS) & 1) ^ 1, abort_flag,
-                                                    p.dev_status)) {
-                        alive = false;
-                        break;
-                    }
-                    tc::mbar_arrive_expect_tx(&full[s], (i == disp_tile || i == new_tile)
-                                                            ? 2 * kDispBoxBytes
-                                                            : kStageBytes);
-                    const int d0 = ks * 128;
-                    uint8_t *dst = smem + s * kStageBytes;
-#pragma unroll
-                    for (int box = 0; box < 2; ++box) {
-                        if (i == disp_tile) {
-                            tc::tma_load_4d(dst + box * kBoxBytes, &maps.disp, d0 + box * 64, c,
-                                            is_v ? 1 : 0, b * (p.k - 1), &full[s], pol);
-                        } else if (i == new_tile) {
-                            tc::tma_load_3d(dst + box * kBoxBytes, is_v ? &maps.vnew : &maps.knew,
-                                            d0 + box * 64, c, b * p.k, &full[s], pol);
-                        } else {
-                            const long long row = ring ? (long long)id * p.window + (long long)i * kTileKeys
-                                                       : (long long)id * p.capacity + (long long)i * kTileKeys;
-                            tc::tma_load_3d(dst + box * kBoxBytes, is_v ? &maps.v : &maps.k,
-                                            d0 + box * 64, c, (int)row, &full[s], pol);
-                        }
-                    }
-                    ++cnt;
-                }
-            }
+            produce(0xffffffffu);
+            const bool alive = alive_p;
             if (!alive) {
                 // Wait (bounded) for the copies already issued before leaving.
                 for (uint32_t x = cnt > (uint32_t)NS ? cnt - NS : 0; x < cnt; ++x)
