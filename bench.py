@@ -291,11 +291,14 @@ def run_carat(args, world, rank, local):
     stage_s = time.perf_counter() - t_stage
 
     stream = torch.cuda.current_stream()
+    dstep = engine.DecodeStep(
+        [lay for lay, _ in layers] + [glay],
+        [(inp.queries, inp.k_new, inp.v_new, inp.context_lengths) for _, inp in layers]
+        + [(ginp.queries, ginp.k_new, ginp.v_new, ginp.context_lengths)],
+        outs + [gout])
 
     def step():
-        for (lay, inp), out in zip(layers, outs):
-            lay.step(inp.queries, inp.k_new, inp.v_new, inp.context_lengths, out=out)
-        glay.step(ginp.queries, ginp.k_new, ginp.v_new, ginp.context_lengths, out=gout)
+        dstep.run()
 
     # --- first step: its outputs are checked against the oracle sample
     step()
@@ -409,29 +412,31 @@ def run_carat(args, world, rank, local):
                            "timed region of up to 300 steps (the whole fused append+attention "
                            "call: one kernel, plus the combine kernel when it splits the keys)")}
 
-    # --- end to end through the public API with host buffers
+    # --- the step replayed from a CUDA graph (one host launch per step)
+    dstep.capture()
+    for _ in range(3):
+        dstep.replay()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(nrep):
+        dstep.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = e0.elapsed_time(e1) / nrep
+    graph = {"ms_per_step": round(graph_ms, 4),
+             "gb_s": round(nbytes["step"] / (graph_ms * 1e6), 1)}
+
+    # --- end to end through the public API with host buffers: every step
+    # copies all layers' inputs from pinned host memory and every output back,
+    # on a copy stream that overlaps them with the layers' compute
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())  # noqa: E731
-    h_in = [(pin(inp.queries), pin(inp.k_new), pin(inp.v_new), pin(inp.context_lengths))
-            for _, inp in layers]
-    g_in = (pin(ginp.queries), pin(ginp.k_new), pin(ginp.v_new), pin(ginp.context_lengths))
-    h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
-    g_hout = torch.empty(gout.shape, dtype=gout.dtype, pin_memory=True)
-    d_in = [tuple(torch.empty_like(x, device=dev) for x in hi) for hi in h_in]
-    gd_in = tuple(torch.empty_like(x, device=dev) for x in g_in)
-    h2d = sum(x.numel() * x.element_size() for hi in h_in for x in hi) + \
-        sum(x.numel() * x.element_size() for x in g_in)
-    d2h = sum(o.numel() * o.element_size() for o in h_out) + g_hout.numel() * g_hout.element_size()
+    h_in = [tuple(pin(x) for x in din) for din in dstep.inputs]
+    h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in dstep.outputs]
+    h2d = sum(x.numel() * x.element_size() for hi in h_in for x in hi)
+    d2h = sum(o.numel() * o.element_size() for o in h_out)
 
     def e2e_step():
-        for (lay, _), hi, di, out, ho in zip(layers, h_in, d_in, outs, h_out):
-            for src, dst in zip(hi, di):
-                dst.copy_(src, non_blocking=True)
-            lay.step(di[0], di[1], di[2], di[3], out=out)
-            ho.copy_(out, non_blocking=True)
-        for src, dst in zip(g_in, gd_in):
-            dst.copy_(src, non_blocking=True)
-        glay.step(gd_in[0], gd_in[1], gd_in[2], gd_in[3], out=gout)
-        g_hout.copy_(gout, non_blocking=True)
+        dstep.run_from_host(h_in, h_out)
 
     for _ in range(3):
         e2e_step()
@@ -469,11 +474,14 @@ def run_carat(args, world, rank, local):
         "roofline": roofline,
         "per_call": per_call,
         "separate_calls": separate,
+        "cuda_graph": graph,
         "cpu_baseline": cpu_baseline,
         "parity_sample": parity,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / e2e_steps, 4),
-                "steps": e2e_steps},
+                "steps": e2e_steps,
+                "how": "engine.DecodeStep.run_from_host: pinned host inputs of all 6 layers in, "
+                       "all outputs out, copies overlapped with compute on a copy stream"},
         "gpu_launches": launches,
         "clocks": clocks,
         "device_status": status,

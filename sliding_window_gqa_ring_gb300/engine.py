@@ -224,3 +224,82 @@ def stage_global(w: synth.Workload, layer_index: int, layer: GlobalLayer, reques
             hist[b] = (0, kh, vh)
     return StepInputs(_bf16_tensor(q_all, dev), _bf16_tensor(kn, dev), _bf16_tensor(vn, dev),
                       _i32(ctx, dev), {"q": q_all, "k_new": kn, "v_new": vn, "hist": hist})
+
+
+# ---------------------------------------------------------------------------
+# A decode step over several layers
+# ---------------------------------------------------------------------------
+
+class DecodeStep:
+    """One decode / verify step over a list of layers (SlidingLayer or
+    GlobalLayer), each with its own queries and new K/V rows.
+
+    run()        -- every layer's fused append+attention on the current stream
+                    (inputs already on the device).
+    run_from_host(host_inputs, host_outputs)
+                 -- the same step from pinned host buffers: all layers' inputs
+                    are copied on a separate copy stream up front, each layer
+                    waits only for its own inputs, and each layer's output is
+                    copied back while the next layer computes.
+    capture() / replay()
+                 -- record run() once into a CUDA graph and replay it (one
+                    launch of the whole step from the host).
+
+    `inputs[i]` = (queries, k_new, v_new, context_lengths) device tensors of
+    layer i; `outputs[i]` its fp32 output tensor.
+    """
+
+    def __init__(self, layers, inputs, outputs=None):
+        self.layers = list(layers)
+        self.inputs = [tuple(x) for x in inputs]
+        self.outputs = outputs or [torch.empty(q.shape, dtype=torch.float32, device=q.device)
+                                   for (q, _, _, _) in self.inputs]
+        self.device = self.inputs[0][0].device
+        self.copy_stream = torch.cuda.Stream(device=self.device)
+        self.graph = None
+        self._in_ready = [torch.cuda.Event() for _ in self.layers]
+        self._out_ready = [torch.cuda.Event() for _ in self.layers]
+
+    def run(self, stream=None):
+        for layer, (q, kn, vn, ctx), out in zip(self.layers, self.inputs, self.outputs):
+            layer.step(q, kn, vn, ctx, out=out, stream=stream)
+        return self.outputs
+
+    def run_from_host(self, host_inputs, host_outputs):
+        compute = torch.cuda.current_stream(self.device)
+        self.copy_stream.wait_stream(compute)
+        with torch.cuda.stream(self.copy_stream):
+            for i, (hin, din) in enumerate(zip(host_inputs, self.inputs)):
+                for src, dst in zip(hin, din):
+                    dst.copy_(src, non_blocking=True)
+                self._in_ready[i].record(self.copy_stream)
+        for i, (layer, (q, kn, vn, ctx), out) in enumerate(
+                zip(self.layers, self.inputs, self.outputs)):
+            compute.wait_event(self._in_ready[i])
+            layer.step(q, kn, vn, ctx, out=out)
+            self._out_ready[i].record(compute)
+            self.copy_stream.wait_event(self._out_ready[i])
+            with torch.cuda.stream(self.copy_stream):
+                host_outputs[i].copy_(out, non_blocking=True)
+        compute.wait_stream(self.copy_stream)
+        return host_outputs
+
+    def capture(self):
+        """Record run() into a CUDA graph (after at least one eager run, so
+        every lazily looked-up device address already exists)."""
+        self.run()
+        torch.cuda.synchronize(self.device)
+        self.graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device=self.device)
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(self.graph, stream=side):
+                self.run(stream=side)
+        torch.cuda.current_stream(self.device).wait_stream(side)
+        return self.graph
+
+    def replay(self):
+        if self.graph is None:
+            raise RuntimeError("capture() first")
+        self.graph.replay()
+        return self.outputs
