@@ -146,15 +146,19 @@ SLIDING_EDGES = [
     ([300, 1024 + 63, 1024 + 65], 2, 16, 2, 512),
     ([100, 1030, 2000], 16, 16, 2, 512),  # 128 rows per KV head: two row groups
     ([7, 1031, 3000], 5, 6, 2, 256),      # 3 heads per KV head (rows not a power of two)
+    ([5, 999, 1000, 1003, 2500], 4, 16, 8, 256, 1000),  # window not a multiple of 128
+    ([16, 130, 131, 145, 700], 16, 16, 8, 256, 130),     # window barely above one tile
+    ([3, 63, 64, 65, 300], 3, 4, 2, 512, 64),            # window inside one tile
 ]
 
 
 @FUSED
 @pytest.mark.parametrize("case", range(len(SLIDING_EDGES)))
 def test_sliding_edges(orc, case, fused):
-    kcs, k, hq, hkv, d = SLIDING_EDGES[case]
+    kcs, k, hq, hkv, d, *rest = SLIDING_EDGES[case]
+    window = rest[0] if rest else 1024
     w = synth.small(f"swa_edge{case}", seed=2000 + case, batch=len(kcs), proposal_count=k,
-                    q_heads=hq, kv_heads=hkv, head_dim=d, key_counts=kcs, window=1024)
+                    q_heads=hq, kv_heads=hkv, head_dim=d, key_counts=kcs, window=window)
     _run_sliding(orc, w, fill=float("nan"), fused=fused)
 
 
