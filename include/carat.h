@@ -120,6 +120,36 @@ carat_status carat_ring_append(void *k_ring, void *v_ring, int num_rings,
                                void *stream);
 
 /*
+ * carat_ring_rollback -- undo the rejected part of a speculative append.
+ *
+ * After a verify step appended proposal_count rows at positions
+ * context_lengths[b] + j (carat_ring_append or carat_swa_append_attention
+ * with a `displaced` buffer), the sampler keeps only the first accepted[b]
+ * of them.  For every rejected row j >= max(accepted[b], 1) whose slot held a
+ * token before the append (position context_lengths[b] + j - window >= 0),
+ * the slot's old K and V rows are copied back from displaced[b][j-1].  The
+ * ring then holds, for key count context_lengths[b] + accepted[b], the newest
+ * token of every slot a later query can see.  (With accepted[b] == 0 the slot
+ * of position context_lengths[b] - window is not restored: that position is
+ * outside every later window, and the next append overwrites the slot.)
+ * Rows of rejected proposals in slots that held no token stay where they are:
+ * attention treats such slots as empty for the smaller key count.
+ * The pages have no rollback step; the displaced rows are the reading
+ * explained at carat_ring_append.  Global caches need no rollback: rows at or
+ * past the key count are never read.
+ *
+ *   accepted   int32 [batch], device memory, 0 <= accepted[b] <=
+ *              proposal_count (outside: the request is skipped and
+ *              CARAT_DEV_BAD_CONTEXT is set).
+ *   Other arguments as in carat_ring_append.  2 <= proposal_count <= 16.
+ */
+carat_status carat_ring_rollback(void *k_ring, void *v_ring, int num_rings,
+                                 const int32_t *ring_ids, const void *displaced,
+                                 const int32_t *context_lengths, const int32_t *accepted,
+                                 int proposal_count, int batch, int kv_heads, int head_dim,
+                                 int window, void *stream);
+
+/*
  * carat_swa_attention -- sliding-window decode / verify attention read
  * straight from the rotated rings (no gather, no un-rotation).
  *
@@ -243,13 +273,15 @@ size_t carat_noalloc_scratch_bytes(void);
  * rings hold exactly what carat_ring_append would have written.  When more
  * than 64 rows share a KV head the rows are split over several CTAs per tile;
  * then the new rows are written by a ring append launched right after the
- * attention.  workspace: carat_swa_workspace_bytes(...) bytes.
+ * attention.  displaced: NULL, or a buffer as in carat_ring_append that
+ * receives the rows the new ones overwrite (for carat_ring_rollback).
+ * workspace: carat_swa_workspace_bytes(...) bytes.
  * Supported: as carat_swa_attention, for (q_heads/kv_heads) <= 64 (otherwise
  * CARAT_ERR_UNSUPPORTED).
  */
 carat_status carat_swa_append_attention(float *out, const void *queries,
                                         void *k_ring, void *v_ring, int num_rings,
-                                        const int32_t *ring_ids,
+                                        const int32_t *ring_ids, void *displaced,
                                         const void *k_new, const void *v_new,
                                         const int32_t *context_lengths, int proposal_count,
                                         int batch, int q_heads, int kv_heads, int head_dim,

@@ -40,6 +40,7 @@ EXPORTED = (
     "carat_status_string", "carat_abi_version", "carat_kernel_launches",
     "carat_swa_attention_noalloc", "carat_noalloc_scratch_bytes",
     "carat_swa_append_attention", "carat_global_append_verify_attention",
+    "carat_ring_rollback",
 )
 
 
@@ -81,8 +82,10 @@ def _declare(lib):
     lib.carat_noalloc_scratch_bytes.restype = sz
     lib.carat_noalloc_scratch_bytes.argtypes = []
     lib.carat_swa_append_attention.restype = i32
-    lib.carat_swa_append_attention.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32,
-                                               i32, i32, i32, f32, vp, sz, vp]
+    lib.carat_swa_append_attention.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, i32, i32,
+                                               i32, i32, i32, i32, f32, vp, sz, vp]
+    lib.carat_ring_rollback.restype = i32
+    lib.carat_ring_rollback.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
     lib.carat_global_append_verify_attention.restype = i32
     lib.carat_global_append_verify_attention.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, i32,
                                                          i32, i32, i32, i32, i32, f32, vp, sz, vp]
@@ -226,9 +229,10 @@ def carat_global_verify_attention(out, queries, key_cache, value_cache, context_
 
 
 def carat_swa_append_attention(out, queries, k_ring, v_ring, k_new, v_new, context_lengths, *,
-                                scale, workspace, ring_ids=None, stream=None):
+                                scale, workspace, ring_ids=None, displaced=None, stream=None):
     """Append this step's rows to the rings and attend, in one launch.  Rings
-    are passed as before the step; afterwards they hold the new rows."""
+    are passed as before the step; afterwards they hold the new rows (and
+    `displaced`, if given, the rows they overwrote, for carat_ring_rollback)."""
     _expect(queries, torch.bfloat16, "queries")
     _expect(out, torch.float32, "out")
     _expect(k_new, torch.bfloat16, "k_new")
@@ -236,9 +240,24 @@ def carat_swa_append_attention(out, queries, k_ring, v_ring, k_new, v_new, conte
     num_rings, window, kv_heads, _ = k_ring.shape
     _check(library().carat_swa_append_attention(
         _ptr(out), _ptr(queries), _ptr(k_ring), _ptr(v_ring), num_rings, _ptr(ring_ids),
-        _ptr(k_new), _ptr(v_new), _ptr(context_lengths), k, batch, q_heads, kv_heads, head_dim,
-        window, float(scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
-        _stream(stream)), "carat_swa_append_attention")
+        _ptr(displaced), _ptr(k_new), _ptr(v_new), _ptr(context_lengths), k, batch, q_heads,
+        kv_heads, head_dim, window, float(scale), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)),
+        "carat_swa_append_attention")
+
+
+def carat_ring_rollback(k_ring, v_ring, displaced, context_lengths, accepted, proposal_count, *,
+                        ring_ids=None, window=None, stream=None):
+    """Keep only the first accepted[b] of the proposal_count rows the last
+    append wrote; restore the slots of the rejected rows from `displaced`."""
+    _expect(k_ring, torch.bfloat16, "k_ring")
+    _expect(accepted, torch.int32, "accepted")
+    num_rings, ring_window, kv_heads, head_dim = k_ring.shape
+    batch = context_lengths.shape[0]
+    _check(library().carat_ring_rollback(
+        _ptr(k_ring), _ptr(v_ring), num_rings, _ptr(ring_ids), _ptr(displaced),
+        _ptr(context_lengths), _ptr(accepted), int(proposal_count), batch, kv_heads, head_dim,
+        ring_window if window is None else window, _stream(stream)), "carat_ring_rollback")
 
 
 def carat_global_append_verify_attention(out, queries, key_cache, value_cache, k_new, v_new,

@@ -362,7 +362,8 @@ carat_status carat_global_verify_attention(float *out, const void *queries, cons
 // caches (by the attention kernel itself, or by a ring append launched after
 // it when several CTAs read each ring tile).
 static carat_status append_attention(float *out, const void *queries, void *k_base, void *v_base,
-                                     int num_ids, const int32_t *ids, const void *k_new,
+                                     int num_ids, const int32_t *ids, void *displaced,
+                                     const void *k_new,
                                      const void *v_new, const int32_t *context_lengths,
                                      int proposal_count, int batch, int q_heads, int kv_heads,
                                      int head_dim, int window, int capacity, float scale,
@@ -382,6 +383,7 @@ static carat_status append_attention(float *out, const void *queries, void *k_ba
     st = check_attention_common(out, queries, k_base, v_base, num_ids, ids, context_lengths, batch);
     if (st != CARAT_OK) return st;
     if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return CARAT_ERR_INVALID_ARG;
+    if (displaced && !aligned16(displaced)) return CARAT_ERR_INVALID_ARG;
     const SplitPlan plan =
         ring ? swa_plan(batch, proposal_count, q_heads, kv_heads, head_dim, window)
              : global_plan(batch, proposal_count, q_heads, kv_heads, head_dim, capacity);
@@ -421,6 +423,7 @@ static carat_status append_attention(float *out, const void *queries, void *k_ba
     p.v_new = static_cast<const uint16_t *>(v_new);
     p.k_dst = static_cast<uint16_t *>(k_base);
     p.v_dst = static_cast<uint16_t *>(v_base);
+    p.displaced_out = (ring && proposal_count > 1) ? static_cast<uint16_t *>(displaced) : nullptr;
     // Several row groups read every ring tile: none of them may overwrite a
     // slot, so a ring append follows the attention instead.
     p.fused_write = (!ring || row_groups_for(group, proposal_count) == 1) ? 1 : 0;
@@ -434,7 +437,7 @@ static carat_status append_attention(float *out, const void *queries, void *k_ba
         a.k_new = p.k_new;
         a.v_new = p.v_new;
         a.context_lengths = context_lengths;
-        a.displaced = nullptr;
+        a.displaced = p.displaced_out;
         a.dev_status = p.dev_status;
         a.num_ids = num_ids;
         a.batch = batch;
@@ -449,12 +452,13 @@ static carat_status append_attention(float *out, const void *queries, void *k_ba
 
 carat_status carat_swa_append_attention(float *out, const void *queries, void *k_ring,
                                         void *v_ring, int num_rings, const int32_t *ring_ids,
-                                        const void *k_new, const void *v_new,
+                                        void *displaced, const void *k_new, const void *v_new,
                                         const int32_t *context_lengths, int proposal_count,
                                         int batch, int q_heads, int kv_heads, int head_dim,
                                         int window, float scale, void *workspace,
                                         size_t workspace_bytes, void *stream) {
-    return append_attention(out, queries, k_ring, v_ring, num_rings, ring_ids, k_new, v_new,
+    return append_attention(out, queries, k_ring, v_ring, num_rings, ring_ids, displaced, k_new,
+                            v_new,
                             context_lengths, proposal_count, batch, q_heads, kv_heads, head_dim,
                             window, 0, scale, workspace, workspace_bytes, stream,
                             KeySource::kRing);
@@ -469,10 +473,41 @@ carat_status carat_global_append_verify_attention(float *out, const void *querie
                                                   int kv_heads, int head_dim, int capacity,
                                                   float scale, void *workspace,
                                                   size_t workspace_bytes, void *stream) {
-    return append_attention(out, queries, key_cache, value_cache, num_caches, cache_ids, k_new,
-                            v_new, context_lengths, proposal_count, batch, q_heads, kv_heads,
+    return append_attention(out, queries, key_cache, value_cache, num_caches, cache_ids, nullptr,
+                            k_new, v_new, context_lengths, proposal_count, batch, q_heads, kv_heads,
                             head_dim, 0, capacity, scale, workspace, workspace_bytes, stream,
                             KeySource::kLinear);
+}
+
+carat_status carat_ring_rollback(void *k_ring, void *v_ring, int num_rings,
+                                 const int32_t *ring_ids, const void *displaced,
+                                 const int32_t *context_lengths, const int32_t *accepted,
+                                 int proposal_count, int batch, int kv_heads, int head_dim,
+                                 int window, void *stream) {
+    if (batch < 0 || kv_heads < 1 || head_dim < 1 || window < 1 || proposal_count < 2 ||
+        proposal_count > kMaxProposals || proposal_count > window || num_rings < 1)
+        return CARAT_ERR_INVALID_ARG;
+    if (((long long)kv_heads * head_dim * 2) % 16 != 0) return CARAT_ERR_INVALID_ARG;
+    if (!ring_ids && num_rings < batch) return CARAT_ERR_INVALID_ARG;
+    if (batch == 0) return CARAT_OK;
+    if (!k_ring || !v_ring || !displaced || !context_lengths || !accepted)
+        return CARAT_ERR_INVALID_ARG;
+    if (!aligned16(k_ring) || !aligned16(v_ring) || !aligned16(displaced))
+        return CARAT_ERR_INVALID_ARG;
+    AppendParams p{};
+    p.k_ring = static_cast<uint16_t *>(k_ring);
+    p.v_ring = static_cast<uint16_t *>(v_ring);
+    p.ids = ring_ids;
+    p.context_lengths = context_lengths;
+    p.displaced = static_cast<uint16_t *>(const_cast<void *>(displaced));
+    p.dev_status = device_status_ptr();
+    p.num_ids = num_rings;
+    p.batch = batch;
+    p.k = proposal_count;
+    p.kv_heads = kv_heads;
+    p.head_dim = head_dim;
+    p.window = window;
+    return launch_status(launch_ring_rollback(p, accepted, static_cast<cudaStream_t>(stream)));
 }
 
 carat_status carat_get_device_status(int32_t *host_out, int clear, void *stream) {

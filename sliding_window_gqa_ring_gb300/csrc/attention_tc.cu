@@ -651,7 +651,22 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     const uint4 *vs = reinterpret_cast<const uint4 *>(p.v_new + src);
                     uint4 *kd = reinterpret_cast<uint4 *>(p.k_dst + dst);
                     uint4 *vd = reinterpret_cast<uint4 *>(p.v_dst + dst);
+                    // Save the row this one displaces (position ctx + j - window),
+                    // read by the same lane before it writes the same bytes.
+                    const bool save = ring && p.displaced_out && j >= 1 && ctx + j - p.window >= 0;
+                    uint4 *dk = nullptr, *dv = nullptr;
+                    if (save) {
+                        const size_t row = (size_t)p.kv_heads * D;
+                        dk = reinterpret_cast<uint4 *>(p.displaced_out +
+                                                       ((size_t)b * (p.k - 1) + (j - 1)) * 2 * row +
+                                                       (size_t)c * D);
+                        dv = dk + row / 8;
+                    }
                     for (int e = lane; e < D / 8; e += 32) {
+                        if (save) {
+                            dk[e] = kd[e];
+                            dv[e] = vd[e];
+                        }
                         kd[e] = ks[e];
                         vd[e] = vs[e];
                     }

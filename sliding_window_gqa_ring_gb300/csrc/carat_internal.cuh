@@ -49,6 +49,7 @@ struct AttnParams {
     const uint16_t *v_new;
     uint16_t *k_dst;
     uint16_t *v_dst;
+    uint16_t *displaced_out;    // fused ring append: old rows saved here, or nullptr
     float scale_log2;           // softmax scale * log2(e)
     KeySource source;
 };
@@ -166,6 +167,8 @@ void count_launches(int n);
 // Host-side launchers (defined in the .cu files)
 // ---------------------------------------------------------------------------
 cudaError_t launch_ring_append(const AppendParams &p, cudaStream_t stream);
+cudaError_t launch_ring_rollback(const AppendParams &p, const int32_t *accepted,
+                                 cudaStream_t stream);
 cudaError_t launch_attention_simt(const AttnParams &p, cudaStream_t stream);
 cudaError_t launch_combine(const AttnParams &p, cudaStream_t stream);
 

@@ -59,6 +59,47 @@ __global__ void __launch_bounds__(256) ring_append_kernel(const AppendParams p) 
     }
 }
 
+// Rollback after a speculative append: one CTA per (rejected candidate row
+// j >= 1, request b).  The old rows come back from the displaced buffer the
+// append filled; rows of proposals that are kept, and slots that held no
+// token before the append, are left alone.
+__global__ void __launch_bounds__(256) ring_rollback_kernel(const AppendParams p,
+                                                            const int32_t *accepted) {
+    const int j = blockIdx.x + 1;
+    const int b = blockIdx.y;
+    const long long ctx = p.context_lengths[b];
+    const int id = p.ids ? p.ids[b] : b;
+    const int a = accepted[b];
+    if (ctx < 0 || id < 0 || id >= p.num_ids || a < 0 || a > p.k) {
+        if (threadIdx.x == 0 && j == 1)
+            set_status(p.dev_status, (id < 0 || id >= p.num_ids) ? CARAT_DEV_BAD_CACHE_ID
+                                                                   : CARAT_DEV_BAD_CONTEXT);
+        return;
+    }
+    if (j < a || ctx + j - p.window < 0) return;
+    const long long slot = (ctx + j) % p.window;
+    const size_t row_elems = (size_t)p.kv_heads * p.head_dim;
+    const int chunks = (int)(row_elems * 2 / 16);
+    uint4 *kdst = reinterpret_cast<uint4 *>(p.k_ring + ((size_t)id * p.window + slot) * row_elems);
+    uint4 *vdst = reinterpret_cast<uint4 *>(p.v_ring + ((size_t)id * p.window + slot) * row_elems);
+    const uint4 *src = reinterpret_cast<const uint4 *>(
+        p.displaced + (((size_t)b * (p.k - 1) + (j - 1)) * 2) * row_elems);
+    for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+        kdst[c] = src[c];
+        vdst[c] = src[chunks + c];
+    }
+}
+
+cudaError_t launch_ring_rollback(const AppendParams &p, const int32_t *accepted,
+                                 cudaStream_t stream) {
+    const int chunks = p.kv_heads * p.head_dim * 2 / 16;
+    int threads = chunks < 256 ? ((chunks + 31) / 32) * 32 : 256;
+    dim3 grid(p.k - 1, p.batch);
+    ring_rollback_kernel<<<grid, threads, 0, stream>>>(p, accepted);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_ring_append(const AppendParams &p, cudaStream_t stream) {
     const int chunks = p.kv_heads * p.head_dim * 2 / 16;
     int threads = chunks < 256 ? ((chunks + 31) / 32) * 32 : 256;

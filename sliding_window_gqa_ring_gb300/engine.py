@@ -68,10 +68,19 @@ class SlidingLayer:
                                   displaced=self.displaced, stream=stream)
         return out
 
+    def rollback(self, context_lengths, accepted, proposal_count, ring_ids=None, stream=None):
+        """After a verify step, keep only the first accepted[b] proposals of
+        each request: the rejected rows' slots get their old rows back (from
+        the displaced buffer the step filled)."""
+        carat.carat_ring_rollback(self.k_ring, self.v_ring, self.displaced, context_lengths,
+                                  accepted, proposal_count, ring_ids=ring_ids,
+                                  window=self.window, stream=stream)
+
     def step(self, queries, k_new, v_new, context_lengths, ring_ids=None, out=None, stream=None,
              fused=True):
         """This step's append then attention: one fused launch by default, or
-        carat_ring_append + carat_swa_attention (fused=False)."""
+        carat_ring_append + carat_swa_attention (fused=False).  Either way the
+        rows the append overwrites are saved for rollback() when k > 1."""
         if not fused:
             self.append(k_new, v_new, context_lengths, ring_ids=ring_ids, stream=stream)
             return self.attend(queries, context_lengths, ring_ids=ring_ids, out=out, stream=stream)
@@ -80,6 +89,7 @@ class SlidingLayer:
         carat.carat_swa_append_attention(out, queries, self.k_ring, self.v_ring, k_new, v_new,
                                          context_lengths, scale=self.scale,
                                          workspace=self.workspace, ring_ids=ring_ids,
+                                         displaced=self.displaced if k_new.shape[1] > 1 else None,
                                          stream=stream)
         return out
 

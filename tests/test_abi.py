@@ -138,6 +138,23 @@ def test_append_argument_checks(lib):
     assert _app(lib, B=0) == c.CARAT_OK
 
 
+def test_rollback_argument_checks(lib):
+    from sliding_window_gqa_ring_gb300 import carat as c
+
+    def rb(**kw):
+        a = dict(kr=FAKE, vr=FAKE, nr=4, ids=None, disp=FAKE, ctx=FAKE, acc=FAKE, k=4, B=4,
+                 hkv=8, d=256, w=1024)
+        a.update(kw)
+        return lib.carat_ring_rollback(a["kr"], a["vr"], a["nr"], a["ids"], a["disp"], a["ctx"],
+                                       a["acc"], a["k"], a["B"], a["hkv"], a["d"], a["w"], None)
+    assert rb(k=1) == c.CARAT_ERR_INVALID_ARG          # nothing can be rejected
+    assert rb(k=17) == c.CARAT_ERR_INVALID_ARG
+    assert rb(disp=None) == c.CARAT_ERR_INVALID_ARG
+    assert rb(acc=None) == c.CARAT_ERR_INVALID_ARG
+    assert rb(kr=MISALIGNED) == c.CARAT_ERR_INVALID_ARG
+    assert rb(B=0) == c.CARAT_OK
+
+
 def test_device_status_needs_output_pointer(lib):
     from sliding_window_gqa_ring_gb300 import carat as c
     assert lib.carat_get_device_status(None, 0, None) == c.CARAT_ERR_INVALID_ARG
