@@ -306,6 +306,69 @@ carat_status carat_global_append_verify_attention(float *out, const void *querie
                                                   float scale, void *workspace,
                                                   size_t workspace_bytes, void *stream);
 
+/*
+ * Paged global caches in a shared pool.
+ *
+ * "Improving Decode Throughput on Intel Gaudi 3", "Our approach": the ring
+ * buffers are allocated in the same HBM that backs the global-attention pages,
+ * as one shared pool, so ring space and page space follow the requests' mix.
+ * Here a pool is a bf16 array of num_pages pages; a global layer views it as
+ * [num_pages][page_rows][kv_heads][head_dim] and a sliding layer with the same
+ * page size in bytes views it as rings of window rows (a ring = an aligned run
+ * of pages, ring id = first page / pages per ring), so rings and pages of all
+ * layers can share one allocation (see carat_pool_*).  Position t of request
+ * b lives in row t % page_rows of page page_table[b][t / page_rows].
+ *
+ *   page_table  int32 [batch][max_pages], device memory; entries of pages the
+ *               request does not use are never read.  A page id outside
+ *               [0, num_pages) reads as zeros and sets CARAT_DEV_BAD_CACHE_ID.
+ *   page_rows   rows per page, a positive multiple of 128.
+ *   Capacity per request: max_pages * page_rows rows.
+ */
+
+/* carat_global_append_verify_attention over paged caches (same contract; the
+ * new rows are written through the page table).  workspace:
+ * carat_global_workspace_bytes(batch, proposal_count, q_heads, kv_heads,
+ * head_dim, max_pages * page_rows) bytes. */
+carat_status carat_global_append_verify_attention_paged(
+    float *out, const void *queries, void *key_pages, void *value_pages, int num_pages,
+    const int32_t *page_table, int max_pages, int page_rows, const void *k_new, const void *v_new,
+    const int32_t *context_lengths, int proposal_count, int batch, int q_heads, int kv_heads,
+    int head_dim, float scale, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Write rows for positions context_lengths[b] + j (j < proposal_count, which
+ * may be up to the capacity: e.g. a prompt after prefill) through the page
+ * table.  k_new, v_new: bf16 [batch][proposal_count][kv_heads][head_dim]. */
+carat_status carat_paged_append(void *key_pages, void *value_pages, int num_pages,
+                                const int32_t *page_table, int max_pages, int page_rows,
+                                const void *k_new, const void *v_new,
+                                const int32_t *context_lengths, int proposal_count, int batch,
+                                int kv_heads, int head_dim, void *stream);
+
+/*
+ * carat_pool_* -- host-side allocator of the page ids of one shared pool
+ * (no device memory involved; the caller owns the pool's memory).
+ *
+ * A ring is an aligned run of pages_per_ring pages; carat_pool_alloc_ring
+ * returns its ring id (first page / pages_per_ring), which is what the ring
+ * entry points take in ring_ids when k_ring / v_ring point at the pool.  A
+ * global-layer page is any single page.  Single pages come first from blocks
+ * that single pages already use, so whole blocks stay free for rings.
+ * Thread-safe.  Returns: alloc_ring -> ring id or -1 (no whole free block);
+ * alloc_pages -> n, writing n page ids to out_pages, or -1 (fewer than n free:
+ * nothing allocated); free_* -> 0, or -1 for an id that is not allocated (then
+ * nothing is freed); stats -> out4 = {free pages, whole free blocks, rings in
+ * use, single pages in use}.
+ */
+typedef struct carat_pool carat_pool;
+carat_pool *carat_pool_create(int num_pages, int pages_per_ring);
+void carat_pool_destroy(carat_pool *pool);
+int carat_pool_alloc_ring(carat_pool *pool);
+int carat_pool_free_ring(carat_pool *pool, int ring_id);
+int carat_pool_alloc_pages(carat_pool *pool, int n, int32_t *out_pages);
+int carat_pool_free_pages(carat_pool *pool, int n, const int32_t *pages);
+int carat_pool_stats(carat_pool *pool, int32_t *out4);
+
 /* Workspace bytes the attention calls need for these sizes (the same for the
  * plain and the fused-append entry points; 0 if the sizes are invalid, or if
  * the call needs no scratch).  Pure host arithmetic; no CUDA call. */

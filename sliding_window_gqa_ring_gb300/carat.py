@@ -40,7 +40,9 @@ EXPORTED = (
     "carat_status_string", "carat_abi_version", "carat_kernel_launches",
     "carat_swa_attention_noalloc", "carat_noalloc_scratch_bytes",
     "carat_swa_append_attention", "carat_global_append_verify_attention",
-    "carat_ring_rollback",
+    "carat_ring_rollback", "carat_global_append_verify_attention_paged", "carat_paged_append",
+    "carat_pool_create", "carat_pool_destroy", "carat_pool_alloc_ring", "carat_pool_free_ring",
+    "carat_pool_alloc_pages", "carat_pool_free_pages", "carat_pool_stats",
 )
 
 
@@ -86,6 +88,26 @@ def _declare(lib):
                                                i32, i32, i32, i32, f32, vp, sz, vp]
     lib.carat_ring_rollback.restype = i32
     lib.carat_ring_rollback.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
+    lib.carat_global_append_verify_attention_paged.restype = i32
+    lib.carat_global_append_verify_attention_paged.argtypes = [
+        vp, vp, vp, vp, i32, vp, i32, i32, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, sz, vp]
+    lib.carat_paged_append.restype = i32
+    lib.carat_paged_append.argtypes = [vp, vp, i32, vp, i32, i32, vp, vp, vp, i32, i32, i32, i32,
+                                       vp]
+    lib.carat_pool_create.restype = vp
+    lib.carat_pool_create.argtypes = [i32, i32]
+    lib.carat_pool_destroy.restype = None
+    lib.carat_pool_destroy.argtypes = [vp]
+    lib.carat_pool_alloc_ring.restype = i32
+    lib.carat_pool_alloc_ring.argtypes = [vp]
+    lib.carat_pool_free_ring.restype = i32
+    lib.carat_pool_free_ring.argtypes = [vp, i32]
+    lib.carat_pool_alloc_pages.restype = i32
+    lib.carat_pool_alloc_pages.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int32)]
+    lib.carat_pool_free_pages.restype = i32
+    lib.carat_pool_free_pages.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int32)]
+    lib.carat_pool_stats.restype = i32
+    lib.carat_pool_stats.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
     lib.carat_global_append_verify_attention.restype = i32
     lib.carat_global_append_verify_attention.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, i32,
                                                          i32, i32, i32, i32, i32, f32, vp, sz, vp]
@@ -276,6 +298,82 @@ def carat_global_append_verify_attention(out, queries, key_cache, value_cache, k
         kv_heads, head_dim, capacity, float(scale), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)),
         "carat_global_append_verify_attention")
+
+
+def carat_global_append_verify_attention_paged(out, queries, key_pages, value_pages, page_table,
+                                               k_new, v_new, context_lengths, *, scale,
+                                               workspace, stream=None):
+    """Fused append + grouped verify attention over paged global caches.
+
+    key_pages / value_pages bf16 [num_pages][page_rows][Hkv][D]; page_table
+    int32 [B][max_pages] (device)."""
+    _expect(queries, torch.bfloat16, "queries")
+    _expect(out, torch.float32, "out")
+    _expect(page_table, torch.int32, "page_table")
+    batch, k, q_heads, head_dim = queries.shape
+    num_pages, page_rows, kv_heads, _ = key_pages.shape
+    max_pages = page_table.shape[1]
+    _check(library().carat_global_append_verify_attention_paged(
+        _ptr(out), _ptr(queries), _ptr(key_pages), _ptr(value_pages), num_pages, _ptr(page_table),
+        max_pages, page_rows, _ptr(k_new), _ptr(v_new), _ptr(context_lengths), k, batch,
+        q_heads, kv_heads, head_dim, float(scale), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)),
+        "carat_global_append_verify_attention_paged")
+
+
+def carat_paged_append(key_pages, value_pages, page_table, k_new, v_new, context_lengths, *,
+                       stream=None):
+    """Write rows for positions context_lengths[b] + j through the page table."""
+    _expect(key_pages, torch.bfloat16, "key_pages")
+    _expect(k_new, torch.bfloat16, "k_new")
+    num_pages, page_rows, kv_heads, head_dim = key_pages.shape
+    batch, k = k_new.shape[0], k_new.shape[1]
+    _check(library().carat_paged_append(
+        _ptr(key_pages), _ptr(value_pages), num_pages, _ptr(page_table), page_table.shape[1],
+        page_rows, _ptr(k_new), _ptr(v_new), _ptr(context_lengths), k, batch, kv_heads,
+        head_dim, _stream(stream)), "carat_paged_append")
+
+
+class Pool:
+    """The library's host-side allocator of a shared pool's page ids."""
+
+    def __init__(self, num_pages: int, pages_per_ring: int):
+        self._lib = library()
+        self._h = self._lib.carat_pool_create(int(num_pages), int(pages_per_ring))
+        if not self._h:
+            raise CaratError(CARAT_ERR_INVALID_ARG, "carat_pool_create")
+        self.num_pages, self.pages_per_ring = int(num_pages), int(pages_per_ring)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            self._lib.carat_pool_destroy(h)
+            self._h = None
+
+    def alloc_ring(self) -> int:
+        """Ring id (first page / pages_per_ring) of a whole free block, or -1."""
+        return int(self._lib.carat_pool_alloc_ring(self._h))
+
+    def free_ring(self, ring_id: int) -> bool:
+        return self._lib.carat_pool_free_ring(self._h, int(ring_id)) == 0
+
+    def alloc_pages(self, n: int):
+        """n page ids, or None (nothing allocated) if fewer than n are free."""
+        buf = (ctypes.c_int32 * max(int(n), 1))()
+        got = self._lib.carat_pool_alloc_pages(self._h, int(n), buf)
+        return None if got < 0 else [int(buf[i]) for i in range(got)]
+
+    def free_pages(self, pages) -> bool:
+        pages = list(pages)
+        buf = (ctypes.c_int32 * max(len(pages), 1))(*pages)
+        return self._lib.carat_pool_free_pages(self._h, len(pages), buf) == 0
+
+    def stats(self) -> dict:
+        out = (ctypes.c_int32 * 4)()
+        _check(0 if self._lib.carat_pool_stats(self._h, out) == 0 else CARAT_ERR_INVALID_ARG,
+               "carat_pool_stats")
+        return {"free_pages": out[0], "whole_free_blocks": out[1], "rings": out[2],
+                "pages": out[3]}
 
 
 def carat_get_device_status(clear: bool = True, stream=None) -> int:

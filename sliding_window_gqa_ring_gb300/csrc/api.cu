@@ -361,6 +361,11 @@ carat_status carat_global_verify_attention(float *out, const void *queries, cons
 // before this step plus this step's rows, which are then written into the
 // caches (by the attention kernel itself, or by a ring append launched after
 // it when several CTAs read each ring tile).
+struct PagedArgs {
+    const int32_t *page_table = nullptr;
+    int max_pages = 0, page_rows = 0, num_pages = 0;
+};
+
 static carat_status append_attention(float *out, const void *queries, void *k_base, void *v_base,
                                      int num_ids, const int32_t *ids, void *displaced,
                                      const void *k_new,
@@ -368,7 +373,7 @@ static carat_status append_attention(float *out, const void *queries, void *k_ba
                                      int proposal_count, int batch, int q_heads, int kv_heads,
                                      int head_dim, int window, int capacity, float scale,
                                      void *workspace, size_t workspace_bytes, void *stream,
-                                     KeySource source) {
+                                     KeySource source, PagedArgs pg = PagedArgs()) {
     const bool ring = source == KeySource::kRing;
     if (!attention_shape_ok(batch, proposal_count, q_heads, kv_heads, head_dim) ||
         !std::isfinite(scale))
@@ -424,6 +429,10 @@ static carat_status append_attention(float *out, const void *queries, void *k_ba
     p.k_dst = static_cast<uint16_t *>(k_base);
     p.v_dst = static_cast<uint16_t *>(v_base);
     p.displaced_out = (ring && proposal_count > 1) ? static_cast<uint16_t *>(displaced) : nullptr;
+    p.page_table = pg.page_table;
+    p.max_pages = pg.max_pages;
+    p.page_rows = pg.page_rows;
+    p.num_pages = pg.num_pages;
     // Several row groups read every ring tile: none of them may overwrite a
     // slot, so a ring append follows the attention instead.
     p.fused_write = (!ring || row_groups_for(group, proposal_count) == 1) ? 1 : 0;
@@ -477,6 +486,69 @@ carat_status carat_global_append_verify_attention(float *out, const void *querie
                             k_new, v_new, context_lengths, proposal_count, batch, q_heads, kv_heads,
                             head_dim, 0, capacity, scale, workspace, workspace_bytes, stream,
                             KeySource::kLinear);
+}
+
+static bool paged_args_ok(int num_pages, const int32_t *page_table, int max_pages,
+                          int page_rows) {
+    return num_pages >= 1 && page_table && max_pages >= 1 && page_rows >= kTcTileKeys &&
+           page_rows % kTcTileKeys == 0 &&
+           (long long)num_pages * page_rows < (1LL << 31) &&
+           (long long)max_pages * page_rows < (1LL << 31);
+}
+
+carat_status carat_global_append_verify_attention_paged(
+    float *out, const void *queries, void *key_pages, void *value_pages, int num_pages,
+    const int32_t *page_table, int max_pages, int page_rows, const void *k_new, const void *v_new,
+    const int32_t *context_lengths, int proposal_count, int batch, int q_heads, int kv_heads,
+    int head_dim, float scale, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!paged_args_ok(num_pages, page_table, max_pages, page_rows)) return CARAT_ERR_INVALID_ARG;
+    PagedArgs pg;
+    pg.page_table = page_table;
+    pg.max_pages = max_pages;
+    pg.page_rows = page_rows;
+    pg.num_pages = num_pages;
+    // Requests address the pool only through the page table.
+    return append_attention(out, queries, key_pages, value_pages, batch > 0 ? batch : 1, nullptr,
+                            nullptr, k_new, v_new, context_lengths, proposal_count, batch,
+                            q_heads, kv_heads, head_dim, 0, max_pages * page_rows, scale,
+                            workspace, workspace_bytes, stream, KeySource::kPaged, pg);
+}
+
+carat_status carat_paged_append(void *key_pages, void *value_pages, int num_pages,
+                                const int32_t *page_table, int max_pages, int page_rows,
+                                const void *k_new, const void *v_new,
+                                const int32_t *context_lengths, int proposal_count, int batch,
+                                int kv_heads, int head_dim, void *stream) {
+    if (!paged_args_ok(num_pages, page_table, max_pages, page_rows)) return CARAT_ERR_INVALID_ARG;
+    if (batch < 0 || kv_heads < 1 || head_dim < 1 || proposal_count < 1 ||
+        (long long)proposal_count > (long long)max_pages * page_rows)
+        return CARAT_ERR_INVALID_ARG;
+    if (((long long)kv_heads * head_dim * 2) % 16 != 0) return CARAT_ERR_INVALID_ARG;
+    if (batch == 0) return CARAT_OK;
+    if (!key_pages || !value_pages || !k_new || !v_new || !context_lengths)
+        return CARAT_ERR_INVALID_ARG;
+    if (!aligned16(key_pages) || !aligned16(value_pages) || !aligned16(k_new) || !aligned16(v_new))
+        return CARAT_ERR_INVALID_ARG;
+    AppendParams p{};
+    p.k_ring = static_cast<uint16_t *>(key_pages);
+    p.v_ring = static_cast<uint16_t *>(value_pages);
+    p.ids = nullptr;
+    p.k_new = static_cast<const uint16_t *>(k_new);
+    p.v_new = static_cast<const uint16_t *>(v_new);
+    p.context_lengths = context_lengths;
+    p.displaced = nullptr;
+    p.dev_status = device_status_ptr();
+    p.num_ids = batch;
+    p.batch = batch;
+    p.k = proposal_count;
+    p.kv_heads = kv_heads;
+    p.head_dim = head_dim;
+    p.window = max_pages * page_rows;
+    p.page_table = page_table;
+    p.max_pages = max_pages;
+    p.page_rows = page_rows;
+    p.num_pages = num_pages;
+    return launch_status(launch_ring_append(p, static_cast<cudaStream_t>(stream)));
 }
 
 carat_status carat_ring_rollback(void *k_ring, void *v_ring, int num_rings,

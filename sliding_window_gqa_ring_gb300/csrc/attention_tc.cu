@@ -193,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     const bool ok = request_ok(p, b, &id, &ctx);
     const long long key_count = ctx + p.k;
     const bool ring = p.source == KeySource::kRing;
+    const bool paged = p.source == KeySource::kPaged;
     int special = -1;
     const int ntiles =
         ok ? tc_request_tiles(p.source, p.window, p.k, key_count, p.fused != 0, &special) : 0;
@@ -304,8 +305,22 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     tc::tma_load_3d(dst + box * kBoxBytes, is_v ? &maps.vnew : &maps.knew,
                                     d0 + box * 64, c, b * p.k, &full[s], pol);
                 } else {
-                    const long long row = ring ? (long long)id * p.window + (long long)i * kTileKeys
-                                               : (long long)id * p.capacity + (long long)i * kTileKeys;
+                    long long row;
+                    if (ring) {
+                        row = (long long)id * p.window + (long long)i * kTileKeys;
+                    } else if (paged) {
+                        // A tile never straddles pages (page_rows is a multiple of
+                        // 128).  A page id outside the pool loads the zero fill
+                        // past the tensor's end and is reported.
+                        row = paged_row(p.page_table, p.max_pages, p.page_rows, p.num_pages, b,
+                                        (long long)i * kTileKeys);
+                        if (row < 0) {
+                            set_status(p.dev_status, CARAT_DEV_BAD_CACHE_ID);
+                            row = (long long)p.num_pages * p.page_rows;
+                        }
+                    } else {
+                        row = (long long)id * p.capacity + (long long)i * kTileKeys;
+                    }
                     tc::tma_load_3d(dst + box * kBoxBytes, is_v ? &maps.v : &maps.k,
                                     d0 + box * 64, c, (int)row, &full[s], pol);
                 }
@@ -640,6 +655,14 @@ __global__ void __launch_bounds__(kThreads, MINB)
                         if (sj >= p.window) sj -= p.window;
                         writer = sj / kTileKeys < new_tile ? sj / kTileKeys : new_tile;
                         dst_row = (long long)id * p.window + sj;
+                    } else if (paged) {
+                        writer = new_tile;
+                        dst_row = paged_row(p.page_table, p.max_pages, p.page_rows, p.num_pages, b,
+                                            ctx + j);
+                        if (dst_row < 0) {
+                            if (lane == 0) set_status(p.dev_status, CARAT_DEV_BAD_CACHE_ID);
+                            continue;
+                        }
                     } else {
                         writer = new_tile;
                         dst_row = (long long)id * p.capacity + ctx + j;
@@ -802,8 +825,10 @@ cudaError_t launch_attention_tc(const AttnParams &p, int tiles_per_chunk, cudaSt
     const uint64_t D = (uint64_t)p.head_dim;
     const uint64_t row_bytes = (uint64_t)p.kv_heads * D * 2;
     const uint32_t box3[3] = {64, 1, (uint32_t)kTileKeys};
-    const uint64_t rows_total = (uint64_t)p.num_ids *
-                                (uint64_t)(p.source == KeySource::kRing ? p.window : p.capacity);
+    const uint64_t rows_total =
+        p.source == KeySource::kPaged
+            ? (uint64_t)p.num_pages * (uint64_t)p.page_rows
+            : (uint64_t)p.num_ids * (uint64_t)(p.source == KeySource::kRing ? p.window : p.capacity);
     const uint64_t dims3[3] = {D, (uint64_t)p.kv_heads, rows_total};
     const uint64_t strides3[2] = {D * 2, row_bytes};
     if (!make_bf16_tensor_map(&maps.k, p.k_base, 3, dims3, strides3, box3, true) ||

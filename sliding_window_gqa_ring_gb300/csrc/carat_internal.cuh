@@ -18,6 +18,8 @@ constexpr int kMaxTileRows = CARAT_MAX_TILE_ROWS;
 enum class KeySource : int {
     kRing = 0,    // sliding layer: `window` ring slots + (proposal_count - 1) displaced rows
     kLinear = 1,  // global layer: cache row t holds position t, t < key_count
+    kPaged = 2,   // global layer in pages: position t is row t % page_rows of page
+                  // page_table[b][t / page_rows]
 };
 
 // Everything an attention launch needs; passed by value as a kernel argument.
@@ -50,6 +52,12 @@ struct AttnParams {
     uint16_t *k_dst;
     uint16_t *v_dst;
     uint16_t *displaced_out;    // fused ring append: old rows saved here, or nullptr
+    // Paged global caches (kPaged): page table [B][max_pages], page_rows rows per
+    // page (a multiple of 128), num_pages pages in the pool.
+    const int32_t *page_table;
+    int max_pages;
+    int page_rows;
+    int num_pages;
     float scale_log2;           // softmax scale * log2(e)
     KeySource source;
 };
@@ -62,6 +70,9 @@ struct AppendParams {
     uint16_t *displaced;
     int *dev_status;
     int num_ids, batch, k, kv_heads, head_dim, window;
+    // Paged caches: rows go through the page table instead of a ring.
+    const int32_t *page_table;
+    int max_pages, page_rows, num_pages;
 };
 
 // ---------------------------------------------------------------------------
@@ -107,7 +118,7 @@ __device__ __forceinline__ bool request_ok(const AttnParams &p, int b, int *id_o
     long long ctx = p.context_lengths[b];
     int id = p.ids ? p.ids[b] : b;
     bool ok = true;
-    if (ctx < 0 || (p.source == KeySource::kLinear && ctx + p.k > p.capacity)) ok = false;
+    if (ctx < 0 || (p.source != KeySource::kRing && ctx + p.k > p.capacity)) ok = false;
     if (id < 0 || id >= p.num_ids) ok = false;
     *id_out = id;
     *ctx_out = ctx;
@@ -117,7 +128,7 @@ __device__ __forceinline__ bool request_ok(const AttnParams &p, int b, int *id_o
 // CARAT_DEV_* bits describing why request_ok rejected a request.
 __device__ __forceinline__ int request_error_bits(const AttnParams &p, int id, long long ctx) {
     int bits = 0;
-    if (ctx < 0 || (p.source == KeySource::kLinear && ctx + p.k > p.capacity))
+    if (ctx < 0 || (p.source != KeySource::kRing && ctx + p.k > p.capacity))
         bits |= CARAT_DEV_BAD_CONTEXT;
     if (id < 0 || id >= p.num_ids) bits |= CARAT_DEV_BAD_CACHE_ID;
     return bits;
@@ -152,6 +163,15 @@ __host__ __device__ __forceinline__ int tc_request_tiles(KeySource src, int wind
     }
     *special_tile = -1;
     return (int)((key_count + 127) / 128);
+}
+
+// Row of the paged pool that holds position t of request b, or -1 when the
+// page table entry is outside the pool.
+__device__ __forceinline__ long long paged_row(const int32_t *page_table, int max_pages,
+                                               int page_rows, int num_pages, int b, long long t) {
+    const int page = page_table[(size_t)b * max_pages + (size_t)(t / page_rows)];
+    if (page < 0 || page >= num_pages) return -1;
+    return (long long)page * page_rows + t % page_rows;
 }
 
 // Number of key slots scanned per (request, KV head).

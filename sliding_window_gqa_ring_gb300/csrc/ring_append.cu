@@ -26,12 +26,26 @@ __global__ void __launch_bounds__(256) ring_append_kernel(const AppendParams p) 
         return;
     }
     const long long t = ctx + j;                 // absolute position of new token j
-    const long long slot = t % p.window;
     const size_t row_elems = (size_t)p.kv_heads * p.head_dim;
     const int chunks = (int)(row_elems * 2 / 16);
+    long long dst_row;
+    if (p.page_table) {
+        // Paged cache: position t goes to its page's row; no ring, nothing displaced.
+        if (t >= (long long)p.max_pages * p.page_rows) {
+            if (threadIdx.x == 0) set_status(p.dev_status, CARAT_DEV_BAD_CONTEXT);
+            return;
+        }
+        dst_row = paged_row(p.page_table, p.max_pages, p.page_rows, p.num_pages, b, t);
+        if (dst_row < 0) {
+            if (threadIdx.x == 0) set_status(p.dev_status, CARAT_DEV_BAD_CACHE_ID);
+            return;
+        }
+    } else {
+        dst_row = (long long)id * p.window + t % p.window;
+    }
 
-    uint4 *kdst = reinterpret_cast<uint4 *>(p.k_ring + ((size_t)id * p.window + slot) * row_elems);
-    uint4 *vdst = reinterpret_cast<uint4 *>(p.v_ring + ((size_t)id * p.window + slot) * row_elems);
+    uint4 *kdst = reinterpret_cast<uint4 *>(p.k_ring + (size_t)dst_row * row_elems);
+    uint4 *vdst = reinterpret_cast<uint4 *>(p.v_ring + (size_t)dst_row * row_elems);
     const uint4 *ksrc =
         reinterpret_cast<const uint4 *>(p.k_new + ((size_t)b * p.k + j) * row_elems);
     const uint4 *vsrc =
@@ -39,7 +53,7 @@ __global__ void __launch_bounds__(256) ring_append_kernel(const AppendParams p) 
 
     // Old occupant of this slot: position t - window.  Token j >= 1 displaces a
     // row that query 0 .. j-1 of this step still needs, if it exists.
-    const bool save = p.displaced != nullptr && j >= 1 && t - p.window >= 0;
+    const bool save = p.displaced != nullptr && !p.page_table && j >= 1 && t - p.window >= 0;
     uint4 *ddst = nullptr;
     if (save)
         ddst = reinterpret_cast<uint4 *>(p.displaced +

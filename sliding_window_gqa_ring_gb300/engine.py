@@ -34,18 +34,23 @@ class SlidingLayer:
     def __init__(self, num_rings: int, *, window: int = 1024, q_heads: int = 16,
                  kv_heads: int = 8, head_dim: int = 256, max_batch: int | None = None,
                  max_proposals: int = 1, scale: float | None = None, device="cuda",
-                 fill: float | None = 0.0):
+                 fill: float | None = 0.0, rings=None):
+        """rings: optional (k_ring, v_ring) views to use instead of allocating
+        (e.g. SharedPool.rings()); their first dimension is the ring count."""
         self.window, self.q_heads, self.kv_heads, self.head_dim = window, q_heads, kv_heads, head_dim
         self.max_batch = max_batch or num_rings
         self.max_proposals = max_proposals
         self.scale = (1.0 / math.sqrt(head_dim)) if scale is None else scale
         self.device = torch.device(device)
-        shape = (num_rings, window, kv_heads, head_dim)
-        self.k_ring = torch.empty(shape, dtype=torch.bfloat16, device=self.device)
-        self.v_ring = torch.empty(shape, dtype=torch.bfloat16, device=self.device)
-        if fill is not None:
-            self.k_ring.fill_(fill)
-            self.v_ring.fill_(fill)
+        if rings is not None:
+            self.k_ring, self.v_ring = rings
+        else:
+            shape = (num_rings, window, kv_heads, head_dim)
+            self.k_ring = torch.empty(shape, dtype=torch.bfloat16, device=self.device)
+            self.v_ring = torch.empty(shape, dtype=torch.bfloat16, device=self.device)
+            if fill is not None:
+                self.k_ring.fill_(fill)
+                self.v_ring.fill_(fill)
         self.displaced = torch.zeros((self.max_batch, max(max_proposals - 1, 1), 2, kv_heads,
                                       head_dim), dtype=torch.bfloat16, device=self.device)
         self.workspace = carat.workspace_tensor(
@@ -91,6 +96,75 @@ class SlidingLayer:
                                          workspace=self.workspace, ring_ids=ring_ids,
                                          displaced=self.displaced if k_new.shape[1] > 1 else None,
                                          stream=stream)
+        return out
+
+
+class SharedPool:
+    """One K pool and one V pool of `num_pages` pages of `page_bytes` each,
+    shared by the rings of sliding layers and the pages of global layers
+    ("Improving Decode Throughput on Intel Gaudi 3", "Our approach").  The
+    library's allocator (carat.Pool) hands out ring ids and page ids; sliding
+    layers see the pools as rings, global layers as pages."""
+
+    def __init__(self, num_pages: int, page_bytes: int, pages_per_ring: int, device="cuda",
+                 fill: float | None = 0.0):
+        if page_bytes % 2:
+            raise ValueError("page_bytes must be even (bf16)")
+        self.num_pages, self.page_bytes, self.pages_per_ring = num_pages, page_bytes, pages_per_ring
+        self.device = torch.device(device)
+        n = num_pages * page_bytes // 2
+        self.k = torch.empty(n, dtype=torch.bfloat16, device=self.device)
+        self.v = torch.empty(n, dtype=torch.bfloat16, device=self.device)
+        if fill is not None:
+            self.k.fill_(fill)
+            self.v.fill_(fill)
+        self.alloc = carat.Pool(num_pages, pages_per_ring)
+
+    def rings(self, window: int, kv_heads: int, head_dim: int):
+        ring_bytes = window * kv_heads * head_dim * 2
+        if ring_bytes != self.pages_per_ring * self.page_bytes:
+            raise ValueError("a ring must fill exactly pages_per_ring pages")
+        nr = self.num_pages // self.pages_per_ring
+        shape = (nr, window, kv_heads, head_dim)
+        return (self.k[:nr * ring_bytes // 2].view(shape), self.v[:nr * ring_bytes // 2].view(shape))
+
+    def pages(self, kv_heads: int, head_dim: int):
+        row_bytes = kv_heads * head_dim * 2
+        if self.page_bytes % row_bytes or (self.page_bytes // row_bytes) % 128:
+            raise ValueError("a page must hold a multiple of 128 rows")
+        shape = (self.num_pages, self.page_bytes // row_bytes, kv_heads, head_dim)
+        return self.k.view(shape), self.v.view(shape)
+
+
+class PagedGlobalLayer:
+    """A global layer whose caches are pages of a SharedPool: request b's
+    position t is row t % page_rows of page page_table[b][t // page_rows]."""
+
+    def __init__(self, pool: SharedPool, page_table: torch.Tensor, *, q_heads: int = 16,
+                 kv_heads: int = 2, head_dim: int = 512, max_proposals: int = 4,
+                 scale: float | None = None):
+        self.key_pages, self.value_pages = pool.pages(kv_heads, head_dim)
+        self.page_rows = self.key_pages.shape[1]
+        self.page_table = page_table
+        self.q_heads, self.kv_heads, self.head_dim = q_heads, kv_heads, head_dim
+        self.capacity = page_table.shape[1] * self.page_rows
+        self.scale = (1.0 / math.sqrt(head_dim)) if scale is None else scale
+        self.device = pool.device
+        batch = page_table.shape[0]
+        self.workspace = carat.workspace_tensor(
+            max(carat.global_workspace_bytes(batch, p, q_heads, kv_heads, head_dim, self.capacity)
+                for p in range(1, max_proposals + 1)), self.device)
+
+    def append(self, k_new, v_new, context_lengths, stream=None):
+        carat.carat_paged_append(self.key_pages, self.value_pages, self.page_table, k_new, v_new,
+                                 context_lengths, stream=stream)
+
+    def step(self, queries, k_new, v_new, context_lengths, out=None, stream=None):
+        if out is None:
+            out = torch.empty(queries.shape, dtype=torch.float32, device=self.device)
+        carat.carat_global_append_verify_attention_paged(
+            out, queries, self.key_pages, self.value_pages, self.page_table, k_new, v_new,
+            context_lengths, scale=self.scale, workspace=self.workspace, stream=stream)
         return out
 
 
@@ -181,9 +255,11 @@ def _prefill(layer_append, k_rows, v_rows, first_position, b, device, window):
         done += cnt
 
 
-def stage_sliding(w: synth.Workload, layer_index: int, layer: SlidingLayer, requests=None):
+def stage_sliding(w: synth.Workload, layer_index: int, layer: SlidingLayer, requests=None,
+                  ring_ids=None):
     """Fill each request's ring with the `window` positions before its context
-    length and return the step's inputs.  Request b uses ring b."""
+    length and return the step's inputs.  Request b uses ring b, or
+    ring_ids[b] when given."""
     dev = layer.device
     B, k = w.batch, w.proposal_count
     ctx = w.context_lengths
@@ -197,7 +273,8 @@ def stage_sliding(w: synth.Workload, layer_index: int, layer: SlidingLayer, requ
         n_old = int(ctx[b]) - first
         if n_old > 0:
             _prefill(lambda kt, vt, c, r: layer.append(kt, vt, c, ring_ids=r, save_displaced=False),
-                     kh[:n_old], vh[:n_old], first, b, dev, w.window)
+                     kh[:n_old], vh[:n_old], first, b if ring_ids is None else int(ring_ids[b]),
+                     dev, w.window)
         kn[b], vn[b] = kh[n_old:n_old + k], vh[n_old:n_old + k]
         q_all[b] = synth.queries(w, layer_index, b)
         hist[b] = (first, kh, vh)
@@ -313,3 +390,35 @@ class DecodeStep:
             raise RuntimeError("capture() first")
         self.graph.replay()
         return self.outputs
+
+
+def stage_global_paged(w: synth.Workload, layer_index: int, layer: PagedGlobalLayer,
+                       keep_history=True):
+    """Write each request's rows [0, context_length) through its page table
+    (one carat_paged_append per request) and return the step's inputs."""
+    dev = layer.device
+    B, k = w.batch, w.proposal_count
+    ctx = w.context_lengths
+    q_all = np.zeros((B, k, w.q_heads, w.head_dim), np.uint16)
+    kn = np.zeros((B, k, w.kv_heads, w.head_dim), np.uint16)
+    vn = np.zeros_like(kn)
+    hist = {}
+
+    def gen(b):
+        return (synth.history(w, layer_index, b, 0, int(w.key_counts[b]), "k"),
+                synth.history(w, layer_index, b, 0, int(w.key_counts[b]), "v"))
+
+    for b, (kh, vh) in enumerate(_parallel(gen, list(range(B)))):
+        n_old = int(ctx[b])
+        if n_old > 0:
+            table = layer.page_table[b:b + 1]
+            carat.carat_paged_append(layer.key_pages, layer.value_pages, table,
+                                     _bf16_tensor(kh[:n_old], dev).unsqueeze(0),
+                                     _bf16_tensor(vh[:n_old], dev).unsqueeze(0),
+                                     _i32([0], dev))
+        kn[b], vn[b] = kh[n_old:n_old + k], vh[n_old:n_old + k]
+        q_all[b] = synth.queries(w, layer_index, b)
+        if keep_history:
+            hist[b] = (0, kh, vh)
+    return StepInputs(_bf16_tensor(q_all, dev), _bf16_tensor(kn, dev), _bf16_tensor(vn, dev),
+                      _i32(ctx, dev), {"q": q_all, "k_new": kn, "v_new": vn, "hist": hist})
