@@ -412,6 +412,54 @@ def run_carat(args, world, rank, local):
                            "timed region of up to 300 steps (the whole fused append+attention "
                            "call: one kernel, plus the combine kernel when it splits the keys)")}
 
+    # --- the same step with every cache in one shared pool: each sliding
+    # layer's rings and the global layer's pages are allocated from one K and
+    # one V pool by the library's allocator (pages of 512 KiB = a ring's 1/8)
+    pooled = None
+    if args.shared_pool:
+        page_bytes = 128 * sliding.kv_heads * sliding.head_dim * 2
+        g_rows = page_bytes // (glob.kv_heads * glob.head_dim * 2)
+        g_pages = [-(-int(kc) // g_rows) for kc in glob.key_counts]
+        npages = sliding.layers * B * 8 + sum(g_pages) + 8
+        spool = engine.SharedPool(npages, page_bytes, 8, device=dev)
+        p_layers, p_inputs = [], []
+        for li in range(sliding.layers):
+            ids = [spool.alloc.alloc_ring() for _ in range(B)]
+            lay = engine.SlidingLayer(npages // 8, window=sliding.window, q_heads=sliding.q_heads,
+                                      kv_heads=sliding.kv_heads, head_dim=sliding.head_dim,
+                                      max_batch=B, max_proposals=k, scale=sliding.scale,
+                                      device=dev, rings=spool.rings(sliding.window,
+                                                                    sliding.kv_heads,
+                                                                    sliding.head_dim))
+            lay.ring_ids = torch.as_tensor(np.array(ids, np.int32), device=dev)
+            pin = engine.stage_sliding(sliding, li, lay, ring_ids=ids)
+            p_layers.append(lay)
+            p_inputs.append((pin.queries, pin.k_new, pin.v_new, pin.context_lengths))
+        table = np.zeros((B, max(g_pages)), np.int32)
+        for b, n in enumerate(g_pages):
+            table[b, :n] = spool.alloc.alloc_pages(n)
+        pg = engine.PagedGlobalLayer(spool, torch.as_tensor(table, device=dev),
+                                     q_heads=glob.q_heads, kv_heads=glob.kv_heads,
+                                     head_dim=glob.head_dim, max_proposals=k, scale=glob.scale)
+        pgin = engine.stage_global_paged(glob, 0, pg, keep_history=False)
+        p_layers.append(pg)
+        p_inputs.append((pgin.queries, pgin.k_new, pgin.v_new, pgin.context_lengths))
+        pstep = engine.DecodeStep(p_layers, p_inputs)
+        for _ in range(3):
+            pstep.run()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(nrep):
+            pstep.run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        pool_ms = e0.elapsed_time(e1) / nrep
+        pooled = {"ms_per_step": round(pool_ms, 4),
+                  "gb_s": round(nbytes["step"] / (pool_ms * 1e6), 1),
+                  "pool_pages": npages, "page_bytes": page_bytes,
+                  "layout": "5 x 64 rings of 8 pages + paged global caches, one K and one V pool"}
+        del pstep, p_layers, p_inputs, spool
+
     # --- the step replayed from a CUDA graph (one host launch per step)
     dstep.capture()
     for _ in range(3):
@@ -475,6 +523,7 @@ def run_carat(args, world, rank, local):
         "per_call": per_call,
         "separate_calls": separate,
         "cuda_graph": graph,
+        "shared_pool": pooled,
         "cpu_baseline": cpu_baseline,
         "parity_sample": parity,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -546,6 +595,8 @@ def main():
     ap.add_argument("--sample-requests", type=int, default=16,
                     help="requests the oracle recomputes for the CPU baseline / parity sample")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-shared-pool", dest="shared_pool", action="store_false",
+                    help="skip timing the step with all caches in one shared pool")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

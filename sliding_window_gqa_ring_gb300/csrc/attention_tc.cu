@@ -54,6 +54,7 @@ constexpr int kTileKeys = 128;
 constexpr int kBoxBytes = 128 * 128;        // [128 keys][64 bf16]
 constexpr int kStageBytes = 2 * kBoxBytes;  // 128 keys x 128 d
 constexpr int kDispRows = 16;               // displaced rows loaded per tile (>= k - 1)
+constexpr int kMaxPagedTiles = 32;          // paged tiles whose rows a CTA resolves up front
 constexpr int kDispBoxBytes = kDispRows * 128;
 constexpr int kThreads = 192;
 constexpr uint32_t kFull = 0xffffffffu;
@@ -70,7 +71,8 @@ struct Layout {
     static constexpr int kOffBar = kOffRed + kRedFloats * 4;
     static constexpr int kNumBars = 2 * NS + 6;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr int kBytes = kOffMisc + 16;
+    static constexpr int kOffRows = kOffMisc + 16;         // paged: rows of the CTA's tiles
+    static constexpr int kBytes = kOffRows + kMaxPagedTiles * 8;
     static constexpr int kAlloc = kBytes + 1024;       // base alignment slack
     static constexpr int kTmemUsed = N * (2 + D / 128);   // two S^T buffers + O^T
     static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64
@@ -263,6 +265,28 @@ __global__ void __launch_bounds__(kThreads, MINB)
     // V(x) in that order (each part is KS stages):
     auto v_part = [n](int x) { return x == n - 1 ? 2 * n - 1 : 2 * x + 2; };
 
+    // Paged caches: warp 0 resolves the pool rows of the CTA's tiles through
+    // the page table in one parallel round trip, so the producer's issue path
+    // never waits on a page-table read.
+    long long *s_rows = reinterpret_cast<long long *>(smem + L::kOffRows);
+    const bool rows_cached = paged && n <= kMaxPagedTiles;
+    if (rows_cached && warp == 0) {
+        if (lane < n) {
+            const int i = t0 + lane;
+            long long row = -1;
+            if (i != new_tile) {
+                row = paged_row(p.page_table, p.max_pages, p.page_rows, p.num_pages, b,
+                                (long long)i * kTileKeys);
+                if (row < 0) {
+                    set_status(p.dev_status, CARAT_DEV_BAD_CACHE_ID);
+                    row = (long long)p.num_pages * p.page_rows;
+                }
+            }
+            s_rows[lane] = row;
+        }
+        __syncwarp();
+    }
+
     // Producer state (thread 0): the next stage load to issue.
     uint32_t cnt = 0;
     int ppart = 0, pks = 0;
@@ -312,11 +336,15 @@ __global__ void __launch_bounds__(kThreads, MINB)
                         // A tile never straddles pages (page_rows is a multiple of
                         // 128).  A page id outside the pool loads the zero fill
                         // past the tensor's end and is reported.
-                        row = paged_row(p.page_table, p.max_pages, p.page_rows, p.num_pages, b,
-                                        (long long)i * kTileKeys);
-                        if (row < 0) {
-                            set_status(p.dev_status, CARAT_DEV_BAD_CACHE_ID);
-                            row = (long long)p.num_pages * p.page_rows;
+                        if (rows_cached) {
+                            row = s_rows[i - t0];
+                        } else {
+                            row = paged_row(p.page_table, p.max_pages, p.page_rows, p.num_pages,
+                                            b, (long long)i * kTileKeys);
+                            if (row < 0) {
+                                set_status(p.dev_status, CARAT_DEV_BAD_CACHE_ID);
+                                row = (long long)p.num_pages * p.page_rows;
+                            }
                         }
                     } else {
                         row = (long long)id * p.capacity + (long long)i * kTileKeys;

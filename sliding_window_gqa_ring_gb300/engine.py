@@ -53,12 +53,15 @@ class SlidingLayer:
                 self.v_ring.fill_(fill)
         self.displaced = torch.zeros((self.max_batch, max(max_proposals - 1, 1), 2, kv_heads,
                                       head_dim), dtype=torch.bfloat16, device=self.device)
+        # ring of each request when a call passes none (None: ring b)
+        self.ring_ids = None
         self.workspace = carat.workspace_tensor(
             max(carat.swa_workspace_bytes(self.max_batch, p, q_heads, kv_heads, head_dim, window)
                 for p in range(1, max_proposals + 1)), self.device)
 
     def append(self, k_new, v_new, context_lengths, ring_ids=None, save_displaced=True,
                stream=None):
+        ring_ids = self.ring_ids if ring_ids is None else ring_ids
         k = k_new.shape[1]
         disp = self.displaced if (save_displaced and k > 1) else None
         carat.carat_ring_append(self.k_ring, self.v_ring, k_new, v_new, context_lengths,
@@ -66,6 +69,7 @@ class SlidingLayer:
                                 stream=stream)
 
     def attend(self, queries, context_lengths, ring_ids=None, out=None, stream=None):
+        ring_ids = self.ring_ids if ring_ids is None else ring_ids
         if out is None:
             out = torch.empty(queries.shape, dtype=torch.float32, device=self.device)
         carat.carat_swa_attention(out, queries, self.k_ring, self.v_ring, context_lengths,
@@ -77,6 +81,7 @@ class SlidingLayer:
         """After a verify step, keep only the first accepted[b] proposals of
         each request: the rejected rows' slots get their old rows back (from
         the displaced buffer the step filled)."""
+        ring_ids = self.ring_ids if ring_ids is None else ring_ids
         carat.carat_ring_rollback(self.k_ring, self.v_ring, self.displaced, context_lengths,
                                   accepted, proposal_count, ring_ids=ring_ids,
                                   window=self.window, stream=stream)
@@ -86,6 +91,7 @@ class SlidingLayer:
         """This step's append then attention: one fused launch by default, or
         carat_ring_append + carat_swa_attention (fused=False).  Either way the
         rows the append overwrites are saved for rollback() when k > 1."""
+        ring_ids = self.ring_ids if ring_ids is None else ring_ids
         if not fused:
             self.append(k_new, v_new, context_lengths, ring_ids=ring_ids, stream=stream)
             return self.attend(queries, context_lengths, ring_ids=ring_ids, out=out, stream=stream)
