@@ -4,9 +4,11 @@
 // sizes the caller's workspace, and the launches.  The kernels live in
 // ring_append.cu and attention_*.cu.
 #include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <random>
 
 #include "carat_internal.cuh"
 
@@ -42,23 +44,37 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool supported_head_dim(int d) { return d == 256 || d == 512; }
 
 struct SplitPlan {
-    bool tc = false;           // tensor-core kernel (else CUDA-core kernel)
-    bool direct = false;       // one split: the kernel writes the output, no combine
-    int chunk = 0;             // keys per split
-    int tiles_per_chunk = 0;   // tensor-core path: 128-key tiles per split
-    int nchunks = 0;
+    bool tc = false;           // tensor-core kernel (else CUDA-core kernel + combine)
+    bool unit_mode = false;    // tensor-core path: one CTA per unit (else stream-K)
+    int grid = 0;              // tensor-core path: CTAs launched
+    int chunk = 0;             // CUDA-core path: keys per split
+    int nchunks = 0;           // CUDA-core path: splits per (request, KV head)
     size_t ml_bytes = 0;
     size_t o_bytes = 0;
+    size_t ticket_bytes = 0;
     size_t total = 0;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-void size_workspace(SplitPlan &p, long long pairs, int rows, int head_dim) {
-    const size_t parts = (size_t)pairs * p.nchunks * rows;
-    p.ml_bytes = align256(parts * sizeof(float2));
-    p.o_bytes = align256(parts * (size_t)head_dim * sizeof(float));
-    p.total = p.ml_bytes + p.o_bytes;
+// SMs of the current device (looked up once per device); 152, a GB300's
+// count, when no device can be queried -- workspace sizes asked for without a
+// GPU assume that GPU, and a launch re-checks against its own device.
+int device_sm_count() {
+    static std::atomic<int> cached[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return 152;
+    }
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        return 152;
+    }
+    cached[dev].store(n, std::memory_order_relaxed);
+    return n;
 }
 
 // Largest number of splits the combine kernel merges per (request, KV head).
@@ -67,11 +83,11 @@ constexpr long long kMaxSplits = 1024;
 // CUDA-core path: the largest power-of-two chunk in [64, 4096] keys that still
 // gives about 8 CTAs per SM (never more than kMaxSplits chunks).
 SplitPlan simt_plan(long long pairs, long long keys, int rows, int head_dim) {
-    constexpr long long kTargetCtas = 8LL * 152;
+    const long long target_ctas = 8LL * device_sm_count();
     SplitPlan p;
     long long chunk = 64;
     for (int c = 4096; c >= 64; c >>= 1) {
-        if (pairs * ((keys + c - 1) / c) >= kTargetCtas) {
+        if (pairs * ((keys + c - 1) / c) >= target_ctas) {
             chunk = c;
             break;
         }
@@ -79,40 +95,57 @@ SplitPlan simt_plan(long long pairs, long long keys, int rows, int head_dim) {
     while ((keys + chunk - 1) / chunk > kMaxSplits) chunk *= 2;
     p.chunk = (int)chunk;
     p.nchunks = (int)((keys + chunk - 1) / chunk);
-    size_workspace(p, pairs, rows, head_dim);
+    const size_t parts = (size_t)pairs * p.nchunks * rows;
+    p.ml_bytes = align256(parts * sizeof(float2));
+    p.o_bytes = align256(parts * (size_t)head_dim * sizeof(float));
+    p.total = p.ml_bytes + p.o_bytes;
     return p;
 }
 
-// Tensor-core path: 128-key tiles, tiles_per_chunk of them per split.  When
-// the (request, KV head, row group) units alone fill every SM, one CTA takes
-// all of a unit's tiles and writes the output directly (no combine).  Else
-// splits are sized for about two waves of CTAs with every request as long as
-// the cache allows, at most max_tpc tiles each.
-SplitPlan tc_plan(long long pairs, int row_groups, long long max_tiles, int rows, int head_dim,
-                  int ctas_per_sm, int max_tpc) {
+// Tensor-core path.  Units (request, KV head, row group) that fill every
+// resident CTA slot and are all short (at most 16 tiles of 128 keys) run one
+// CTA each.  Otherwise one CTA per resident slot runs the stream-K schedule;
+// each keeps two partial slots (the first and last segment of its range), and
+// each unit a ticket.  The workspace is sized for stream-K either way.
+SplitPlan tc_plan(int batch, int group, int k, int kv_heads, int head_dim, long long max_tiles) {
     SplitPlan p;
     p.tc = true;
-    const long long units = pairs * row_groups;
-    const long long slots = (long long)ctas_per_sm * 152;
-    long long tpc;
-    if (units >= slots && max_tiles <= 16) {
-        tpc = max_tiles;
-    } else {
-        tpc = (units * max_tiles + 2 * slots - 1) / (2 * slots);
-        if (tpc > max_tpc) tpc = max_tpc;
-        if (tpc < 1) tpc = 1;
-    }
-    if ((max_tiles + tpc - 1) / tpc > kMaxSplits) tpc = (max_tiles + kMaxSplits - 1) / kMaxSplits;
-    p.tiles_per_chunk = (int)tpc;
-    p.chunk = (int)tpc * kTcTileKeys;
-    p.nchunks = (int)((max_tiles + tpc - 1) / tpc);
-    p.direct = p.nchunks == 1;
-    if (p.direct) {
-        p.total = 0;  // partials are never written
-        return p;
-    }
-    size_workspace(p, pairs, rows, head_dim);
+    const int n = tc_rows_per_tile(group, k);
+    const int slots_total = tc_ctas_per_sm(head_dim, n) * device_sm_count();
+    const long long units = (long long)batch * tc_units_per_request(group, k, kv_heads);
+    p.unit_mode = units >= slots_total && max_tiles <= 16;
+    p.grid = p.unit_mode ? (int)units : slots_total;
+    const size_t slots = (size_t)slots_total * 2 * n;
+    p.ml_bytes = align256(slots * sizeof(float2));
+    p.o_bytes = align256(slots * (size_t)head_dim * sizeof(float));
+    p.ticket_bytes =
+        align256((size_t)batch * tc_units_per_request(group, k, kv_heads) * sizeof(uint64_t));
+    p.total = p.ml_bytes + p.o_bytes + p.ticket_bytes;
     return p;
+}
+
+// Ticket tags: a random 48-bit start, one more per launch, so a ticket left by
+// another call (an aborted one, or another workspace's user) never matches.
+uint64_t next_epoch() {
+    static std::atomic<uint64_t> epoch{[] {
+        std::random_device rd;
+        const uint64_t t = (uint64_t)std::chrono::steady_clock::now().time_since_epoch().count();
+        return ((uint64_t)rd() << 20) ^ t;
+    }()};
+    return epoch.fetch_add(1, std::memory_order_relaxed) & ((1ull << 48) - 1);
+}
+
+// Point the call's parameters at its workspace.
+void set_split_fields(AttnParams &p, const SplitPlan &plan, void *workspace) {
+    char *w = static_cast<char *>(workspace);
+    p.part_ml = reinterpret_cast<float2 *>(w);
+    p.part_o = w ? reinterpret_cast<float *>(w + plan.ml_bytes) : nullptr;
+    p.tickets = (plan.tc && w)
+                    ? reinterpret_cast<unsigned long long *>(w + plan.ml_bytes + plan.o_bytes)
+                    : nullptr;
+    p.epoch = plan.tc ? next_epoch() : 0;
+    p.chunk = plan.chunk;
+    p.nchunks = plan.nchunks;
 }
 
 int row_groups_for(int group, int k) {
@@ -138,12 +171,10 @@ SplitPlan swa_plan(int batch, int proposal_count, int q_heads, int kv_heads, int
     const int group = q_heads / kv_heads;
     const int rows = group * proposal_count;
     const long long pairs = (long long)batch * kv_heads;
-    if (tc_supported(head_dim, group, proposal_count)) {
+    if (tc_supported(head_dim, group, proposal_count))
         // ring tiles + one tile of displaced rows or (fused append) new rows
-        const long long tiles = (window + kTcTileKeys - 1) / kTcTileKeys + 1;
-        return tc_plan(pairs, row_groups_for(group, proposal_count), tiles, rows, head_dim,
-                       tc_ctas_per_sm(head_dim, tc_rows_per_tile(group, proposal_count)), 4);
-    }
+        return tc_plan(batch, group, proposal_count, kv_heads, head_dim,
+                       (window + kTcTileKeys - 1) / kTcTileKeys + 1);
     return simt_plan(pairs, keys_scanned(KeySource::kRing, window, proposal_count, 0), rows,
                      head_dim);
 }
@@ -153,19 +184,17 @@ SplitPlan global_plan(int batch, int proposal_count, int q_heads, int kv_heads, 
     const int group = q_heads / kv_heads;
     const int rows = group * proposal_count;
     const long long pairs = (long long)batch * kv_heads;
-    if (tc_supported(head_dim, group, proposal_count)) {
+    if (tc_supported(head_dim, group, proposal_count))
         // cache tiles + one tile of new rows (fused append)
-        const long long tiles = (capacity + kTcTileKeys - 1) / kTcTileKeys + 1;
-        return tc_plan(pairs, row_groups_for(group, proposal_count), tiles, rows, head_dim,
-                       tc_ctas_per_sm(head_dim, tc_rows_per_tile(group, proposal_count)), 8);
-    }
+        return tc_plan(batch, group, proposal_count, kv_heads, head_dim,
+                       ((long long)capacity + kTcTileKeys - 1) / kTcTileKeys + 1);
     return simt_plan(pairs, capacity, rows, head_dim);
 }
 
 cudaError_t launch_attention(const AttnParams &p, const SplitPlan &plan, cudaStream_t stream) {
-    cudaError_t e = plan.tc ? launch_attention_tc(p, plan.tiles_per_chunk, stream)
-                            : launch_attention_simt(p, stream);
-    if (e != cudaSuccess || plan.direct) return e;
+    if (plan.tc) return launch_attention_tc(p, plan.grid, plan.unit_mode, stream);
+    cudaError_t e = launch_attention_simt(p, stream);
+    if (e != cudaSuccess) return e;
     return launch_combine(p, stream);
 }
 
@@ -285,8 +314,7 @@ carat_status carat_swa_attention(float *out, const void *queries, const void *k_
     p.displaced = proposal_count > 1 ? static_cast<const uint16_t *>(displaced) : nullptr;
     p.context_lengths = context_lengths;
     p.out = out;
-    p.part_ml = static_cast<float2 *>(workspace);
-    p.part_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.ml_bytes);
+    set_split_fields(p, plan, workspace);
     p.dev_status = device_status_ptr();
     p.num_ids = num_rings;
     p.batch = batch;
@@ -298,10 +326,6 @@ carat_status carat_swa_attention(float *out, const void *queries, const void *k_
     p.rows = p.group * proposal_count;
     p.window = window;
     p.capacity = 0;
-    p.chunk = plan.chunk;
-    p.nchunks = plan.nchunks;
-    p.tiles_per_chunk = plan.tc ? plan.tiles_per_chunk : 0;
-    p.direct = plan.direct ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.source = KeySource::kRing;
     return launch_status(launch_attention(p, plan, static_cast<cudaStream_t>(stream)));
@@ -335,8 +359,7 @@ carat_status carat_global_verify_attention(float *out, const void *queries, cons
     p.displaced = nullptr;
     p.context_lengths = context_lengths;
     p.out = out;
-    p.part_ml = static_cast<float2 *>(workspace);
-    p.part_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.ml_bytes);
+    set_split_fields(p, plan, workspace);
     p.dev_status = device_status_ptr();
     p.num_ids = num_caches;
     p.batch = batch;
@@ -348,10 +371,6 @@ carat_status carat_global_verify_attention(float *out, const void *queries, cons
     p.rows = p.group * proposal_count;
     p.window = 0;
     p.capacity = capacity;
-    p.chunk = plan.chunk;
-    p.nchunks = plan.nchunks;
-    p.tiles_per_chunk = plan.tc ? plan.tiles_per_chunk : 0;
-    p.direct = plan.direct ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.source = KeySource::kLinear;
     return launch_status(launch_attention(p, plan, static_cast<cudaStream_t>(stream)));
@@ -403,9 +422,7 @@ static carat_status append_attention(float *out, const void *queries, void *k_ba
     p.displaced = nullptr;
     p.context_lengths = context_lengths;
     p.out = out;
-    p.part_ml = static_cast<float2 *>(workspace);
-    p.part_o = plan.total ? reinterpret_cast<float *>(static_cast<char *>(workspace) + plan.ml_bytes)
-                          : nullptr;
+    set_split_fields(p, plan, workspace);
     p.dev_status = device_status_ptr();
     p.num_ids = num_ids;
     p.batch = batch;
@@ -417,10 +434,6 @@ static carat_status append_attention(float *out, const void *queries, void *k_ba
     p.rows = group * proposal_count;
     p.window = ring ? window : 0;
     p.capacity = ring ? 0 : capacity;
-    p.chunk = plan.chunk;
-    p.nchunks = plan.nchunks;
-    p.tiles_per_chunk = plan.tiles_per_chunk;
-    p.direct = plan.direct ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.source = source;
     p.fused = 1;

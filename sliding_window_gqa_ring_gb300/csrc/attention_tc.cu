@@ -1,5 +1,6 @@
-// attention_tc.cu -- split-K grouped-query attention on the 5th-generation
-// tensor cores (tcgen05 + TMEM) with TMA-staged K/V tiles.
+// attention_tc.cu -- grouped-query attention on the 5th-generation tensor
+// cores (tcgen05 + TMEM) with TMA-staged K/V tiles, scheduled stream-K over a
+// persistent grid.
 //
 // What it computes is what attention_simt.cu computes: for each request b and
 // KV head c, the rows r = j*g + h' (the g query heads sharing KV head c times
@@ -11,29 +12,51 @@
 // layer, with the tail past key_count masked ("More FLOPs can be faster").
 //
 // Tiles.  Keys come in tiles of 128 (ring slots 128i.., or cache rows 128i..,
-// plus one tile of displaced rows for a sliding verify with k > 1).  Keys are
-// the M dimension of both products, so any number of rows N in {16, 32, 64}
-// fits one tile without padding the keys:
+// plus one tile of displaced rows for a sliding verify with k > 1, or of this
+// step's rows for a fused append).  Keys are the M dimension of both
+// products, so any number of rows N in {16, 32, 64} fits one tile without
+// padding the keys:
 //     S^T [128 keys x N rows]  = K_tile [128 x D] . Q^T          (K-major A, B)
 //     O^T [128 d   x N rows]  += V_tile^T [d x 128 keys] . P^T   (MN-major A)
 // S^T and O^T live in tensor memory; P (bf16) is written to shared memory by
-// the softmax threads.  Rows beyond 64 are split into row groups (separate
-// CTAs).  The key-count tail is masked per key, never padded with work: a
-// tile that holds no token in some rows has those V rows zeroed in shared
-// memory so their contents (zero-initialised or not) cannot reach O.
+// the softmax threads.  Rows beyond 64 are split into row groups.  The
+// key-count tail is masked per key, never padded with work: a tile that holds
+// no token in some rows has those V rows zeroed in shared memory so their
+// contents (zero-initialised or not) cannot reach O.
+//
+// Schedule.  A unit is one (request, KV head, row group).  When there are at
+// least as many units as resident CTA slots and every unit is short (a
+// sliding window), CTA g simply takes unit g whole ("unit mode").  Otherwise
+// (stream-K): a unit's tiles are taken
+// in a fixed order (the small tile of this step's rows first).  All units'
+// tiles, request after request, form one flattened sequence of T tiles, and
+// the grid -- one CTA per resident slot, so every CTA starts at once -- cuts
+// it into equal contiguous ranges of ceil(T / grid) tiles (stream-K).  A CTA
+// walks its range as segments, one per unit it touches, streaming K/V through
+// one stage ring without a break between segments.  A segment that covers a
+// whole unit writes the normalised output; the at most two others (the
+// range's first and last) write a partial (row max, row sum, unnormalised O)
+// to the workspace and take a ticket on their unit, and the CTA that brings
+// the unit's last piece merges them all after its own range is done.  The
+// range is never shorter than 1/(kMaxPieces - 1) of the longest unit, so no
+// unit is cut into more than kMaxPieces pieces.  The CTAs never wait for one
+// another.
 //
 // Warp roles (192 threads):
-//   warp 0      TMA producer: Q once, then K and V tiles in 32 KB stages
-//               (128 keys x 128 d, two 64-d boxes with 128-byte swizzle)
-//               through an NS-deep ring of shared-memory stages.
+//   warp 0      computes the CTA's range (a scan over the requests' tile
+//               counts), then as TMA producer loads each segment's Q and its
+//               K and V tiles in 32 KB stages (128 keys x 128 d, two 64-d
+//               boxes with 128-byte swizzle) through an NS-deep stage ring.
 //   warp 1      allocates TMEM; one thread issues every tcgen05.mma and the
 //               commits that free stages and signal the softmax warps.
-//   warps 2-5   softmax: thread t owns key t of the tile (TMEM lane t): reads
+//   warps 2-5   write NaN outputs for rejected requests, then run the
+//               softmax: thread t owns key t of the tile (TMEM lane t): reads
 //               its N scores, masks by position, finds each row's tile maximum
 //               with a warp transpose-reduction and shared memory, updates the
-//               running max / sum (log2 domain), writes P, rescales O^T in TMEM
-//               when a row's maximum moved, and in the epilogue writes the
-//               chunk's partial (max, sum, unnormalised O) for attn_combine.
+//               running max / sum (log2 domain), writes P, rescales O^T in
+//               TMEM when a row's maximum moved; per segment they write the
+//               output or the partial, and at the end merge the units whose
+//               last piece this CTA brought.
 //
 // Every wait is bounded (mbar_wait): on a timeout the CTA records
 // CARAT_DEV_TIMEOUT, stops issuing work, waits (bounded) for its own copies
@@ -54,7 +77,7 @@ constexpr int kTileKeys = 128;
 constexpr int kBoxBytes = 128 * 128;        // [128 keys][64 bf16]
 constexpr int kStageBytes = 2 * kBoxBytes;  // 128 keys x 128 d
 constexpr int kDispRows = 16;               // displaced rows loaded per tile (>= k - 1)
-constexpr int kMaxPagedTiles = 32;          // paged tiles whose rows a CTA resolves up front
+constexpr int kMaxPieces = 16;              // CTAs one unit may be split across
 constexpr int kDispBoxBytes = kDispRows * 128;
 constexpr int kThreads = 192;
 constexpr uint32_t kFull = 0xffffffffu;
@@ -67,14 +90,18 @@ struct Layout {
     static constexpr int kOffP = kOffQ + (D / 64) * kQBlock;
     static constexpr int kPBlock = N * 128;            // 64 keys of P rows
     static constexpr int kOffRed = kOffP + 2 * kPBlock;
-    static constexpr int kRedFloats = 3 * 4 * N;       // 2 x max buffers + sum buffer
+    // 2 x max buffers + sum buffer (4 warps x N each), then one segment's
+    // row maxima and sums kept for its deferred epilogue
+    static constexpr int kRedFloats = 3 * 4 * N + 2 * N;
     static constexpr int kOffBar = kOffRed + kRedFloats * 4;
-    static constexpr int kNumBars = 2 * NS + 6;
-    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr int kOffRows = kOffMisc + 16;         // paged: rows of the CTA's tiles
-    static constexpr int kBytes = kOffRows + kMaxPagedTiles * 8;
+    static constexpr int kNumBars = 2 * NS + 7;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;   // SkShared
+    static constexpr int kBytes = kOffMisc + 128;
     static constexpr int kAlloc = kBytes + 1024;       // base alignment slack
-    static constexpr int kTmemUsed = N * (2 + D / 128);   // two S^T buffers + O^T
+    // Two S^T buffers and two O^T buffers when they fit the 512 columns, so one
+    // segment's output is written while the next accumulates; else one O^T.
+    static constexpr bool kDoubleO = N * (2 + 2 * KS) <= 512;
+    static constexpr int kTmemUsed = N * (2 + (kDoubleO ? 2 : 1) * KS);
     static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64
                                    : kTmemUsed <= 128 ? 128 : kTmemUsed <= 256 ? 256 : 512;
     static_assert(kAlloc <= 232448, "more dynamic shared memory than one CTA may use");
@@ -84,6 +111,10 @@ struct Layout {
     static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kPBlock % 1024 == 0 &&
                       kQBlock % 1024 == 0,
                   "operand blocks must be 1024-byte aligned for the 128-byte swizzle");
+    // The merge at the end stages (max, sum) pairs, weights and at least one
+    // row of every piece in the idle stage ring.
+    static_assert(kMaxPieces * N * 12 + 2 * kMaxPieces * D * 4 <= NS * kStageBytes,
+                  "merge buffers must fit the stages");
 };
 
 struct TcMaps {
@@ -96,10 +127,246 @@ struct TcMaps {
 };
 
 struct TcPlan {
-    int tiles_per_chunk;
     int row_groups;
     int pos_per_group;    // proposal positions per row group
+    int unit_mode;        // 1: CTA g takes unit g whole (grid = units); 0: stream-K
 };
+
+// Per-CTA schedule, written by warp 0 before the block-wide barrier and read
+// by every role; plus the merges this CTA owes.
+struct SkShared {
+    uint32_t tmem_slot;
+    int abort_flag;
+    int nduty;                 // units this CTA merges at the end (<= 2)
+    int b0, ur0, off0;         // first segment: request, unit within it, order offset
+    int duty_unit[2];
+    int duty_tiles[2];
+    int id0, ntiles0, special0;   // first request's id, tiles and special tile
+    long long ctx0;               // first request's context length
+    long long s, e, len;       // tile range [s, e) of the flattened order; range length
+    long long duty_start[2];   // flattened index of each owed unit's first tile
+};
+static_assert(sizeof(SkShared) <= 128, "SkShared must fit the misc area");
+
+// Tiles of request b (0 when request_ok rejects it) and its special tile.
+__device__ __forceinline__ int request_tiles(const AttnParams &p, int b, int *id, long long *ctx,
+                                             int *special) {
+    *special = -1;
+    if (!request_ok(p, b, id, ctx)) return 0;
+    return tc_request_tiles(p.source, p.window, p.k, *ctx + p.k, p.fused != 0, special);
+}
+
+// One unit's share of a CTA's range.
+struct Segment {
+    int b, id, c, rg, unit;
+    long long ctx;
+    int ntiles, special;       // tiles of the unit and its special tile (-1: none)
+    int x0, x1;                // order indices [x0, x1) of the unit's tiles covered here
+    long long start;           // flattened index of the segment's first tile
+    long long unit_start;      // flattened index of the unit's first tile
+};
+
+// Tile index of order index x: the special tile (this step's rows of a fused
+// append, or the displaced rows of a sliding verify; always the last tile
+// index) comes first.  It takes a single stage, held until its PV product.
+__device__ __forceinline__ int order_tile(const Segment &sg, int x) {
+    if (sg.special >= 0) return x == 0 ? sg.special : x - 1;
+    return x;
+}
+
+// Walks a CTA's range as segments.  Every role runs its own copy over the
+// same inputs, so all of them see the same sequence.
+struct SegIter {
+    long long pos, end;
+    int b, ur, off;
+    int id, ntiles, special;
+    long long ctx;
+
+    __device__ void init(const AttnParams &p, const SkShared *sk) {
+        pos = sk->s;
+        end = sk->e;
+        b = sk->b0;
+        ur = sk->ur0;
+        off = sk->off0;
+        id = sk->id0;
+        ctx = sk->ctx0;
+        ntiles = sk->ntiles0;
+        special = sk->special0;
+    }
+
+    __device__ bool next(const AttnParams &p, int upr, int row_groups, Segment &sg) {
+        if (pos >= end || ntiles <= off) return false;
+        const long long left = end - pos;
+        const int len = (long long)(ntiles - off) < left ? ntiles - off : (int)left;
+        sg.b = b;
+        sg.id = id;
+        sg.ctx = ctx;
+        sg.ntiles = ntiles;
+        sg.special = special;
+        sg.c = ur / row_groups;
+        sg.rg = ur % row_groups;
+        sg.unit = b * upr + ur;
+        sg.x0 = off;
+        sg.x1 = off + len;
+        sg.start = pos;
+        sg.unit_start = pos - off;
+        pos += len;
+        off += len;
+        if (off == ntiles && pos < end) {
+            off = 0;
+            if (++ur == upr) {
+                ur = 0;
+                ntiles = 0;
+                while (ntiles == 0 && b + 1 < p.batch) {
+                    ++b;
+                    ntiles = request_tiles(p, b, &id, &ctx, &special);
+                }
+            }
+        }
+        return true;
+    }
+};
+
+__device__ __forceinline__ long long warp_sum_ll(long long v) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ int warp_max_int(int v) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Warp 0: this CTA's tile range of the flattened order and where it starts.
+// Runs once per CTA from a cold instruction cache, so it is kept to two short
+// loops (32 requests per pass, the second pass re-reading through L2) rather
+// than unrolled code.
+__device__ __noinline__ void locate_range(const AttnParams &p, int upr, int lane, SkShared *sk) {
+    long long total = 0;
+    int nmax = 0;
+#pragma unroll 1
+    for (int base = 0; base < p.batch; base += 32) {
+        const int b = base + lane;
+        int v = 0;
+        if (b < p.batch) {
+            int id, sp;
+            long long ctx;
+            v = request_tiles(p, b, &id, &ctx, &sp);
+        }
+        total += v;
+        nmax = max(nmax, v);
+    }
+    total = warp_sum_ll(total) * upr;
+    nmax = warp_max_int(nmax);
+    const long long grid = gridDim.x;
+    long long len = (total + grid - 1) / grid;
+    const long long min_len = (nmax + kMaxPieces - 2) / (kMaxPieces - 1);
+    if (len < min_len) len = min_len;
+    if (len < 1) len = 1;
+    const long long s = (long long)blockIdx.x * len;
+    const long long e = s + len < total ? s + len : total;
+    // First request whose tiles reach past s; its id, context length and
+    // special tile come from the lane that read it.
+    int b0 = 0, ur0 = 0, off0 = 0, id0 = 0, nt0 = 0, sp0 = -1;
+    long long ctx0 = 0;
+    if (s < e) {
+        long long cum = 0;
+#pragma unroll 1
+        for (int base = 0; base < p.batch; base += 32) {
+            const int b = base + lane;
+            int v = 0, id = 0, sp = -1;
+            long long ctx = 0;
+            if (b < p.batch) v = request_tiles(p, b, &id, &ctx, &sp);
+            const long long vt = (long long)v * upr;
+            long long inc = vt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const long long y = __shfl_up_sync(kFull, inc, o);
+                if (lane >= o) inc += y;
+            }
+            const unsigned hit = __ballot_sync(kFull, cum + inc > s);
+            if (hit) {
+                const int src = __ffs(hit) - 1;
+                if (lane == src) {
+                    const long long roff = s - (cum + inc - vt);   // tiles into request b
+                    b0 = b;
+                    ur0 = (int)(roff / v);
+                    off0 = (int)(roff - (long long)ur0 * v);
+                    nt0 = v;
+                    id0 = id;
+                    ctx0 = ctx;
+                    sp0 = sp;
+                }
+                b0 = __shfl_sync(kFull, b0, src);
+                ur0 = __shfl_sync(kFull, ur0, src);
+                off0 = __shfl_sync(kFull, off0, src);
+                nt0 = __shfl_sync(kFull, nt0, src);
+                id0 = __shfl_sync(kFull, id0, src);
+                ctx0 = __shfl_sync(kFull, ctx0, src);
+                sp0 = __shfl_sync(kFull, sp0, src);
+                break;
+            }
+            cum += __shfl_sync(kFull, inc, 31);
+        }
+    }
+    if (lane == 0) {
+        sk->s = s;
+        sk->e = e;
+        sk->len = len;
+        sk->b0 = b0;
+        sk->ur0 = ur0;
+        sk->off0 = off0;
+        sk->nduty = 0;
+        sk->ntiles0 = nt0;
+        sk->special0 = sp0;
+        sk->id0 = id0;
+        sk->ctx0 = ctx0;
+    }
+    __syncwarp();
+}
+
+// Warp 0, unit mode: this CTA's range is unit blockIdx.x, whole (its own
+// frame: tiles [0, n)); nothing is split, so no partials and no merges.
+__device__ void locate_unit(const AttnParams &p, int upr, int lane, SkShared *sk) {
+    if (lane == 0) {
+        const int b = blockIdx.x / upr;
+        int id = 0, sp = -1;
+        long long ctx = 0;
+        const int nt = b < p.batch ? request_tiles(p, b, &id, &ctx, &sp) : 0;
+        sk->s = 0;
+        sk->e = nt;
+        sk->len = nt > 0 ? nt : 1;
+        sk->b0 = b;
+        sk->ur0 = blockIdx.x % upr;
+        sk->off0 = 0;
+        sk->nduty = 0;
+        sk->ntiles0 = nt;
+        sk->special0 = sp;
+        sk->id0 = id;
+        sk->ctx0 = ctx;
+    }
+    __syncwarp();
+}
+
+// 16-byte copy global -> shared through L2 only (cp.async.cg), and the wait
+// for all of this thread's copies.
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(smem_dst)),
+                 "l"(gsrc)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Wait until at most `pending` of this thread's committed groups are in flight.
+template <int pending>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(pending) : "memory");
+}
 
 // Barrier over the 128 softmax threads that also ORs a predicate across them,
 // so every thread takes the same abort decision.
@@ -184,55 +451,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
     attn_tc_kernel(const AttnParams p, const TcPlan plan, const __grid_constant__ TcMaps maps) {
     using L = Layout<D, N, NS>;
     constexpr int KS = L::KS;
-    const int chunk = blockIdx.x;
-    const int c = blockIdx.y / plan.row_groups;
-    const int rg = blockIdx.y % plan.row_groups;
-    const int b = blockIdx.z;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-
-    int id;
-    long long ctx;
-    const bool ok = request_ok(p, b, &id, &ctx);
-    const long long key_count = ctx + p.k;
+    const int upr = p.kv_heads * plan.row_groups;   // units per request
     const bool ring = p.source == KeySource::kRing;
     const bool paged = p.source == KeySource::kPaged;
-    int special = -1;
-    const int ntiles =
-        ok ? tc_request_tiles(p.source, p.window, p.k, key_count, p.fused != 0, &special) : 0;
-    const int disp_tile = p.fused ? -1 : special;   // displaced rows (append done before)
-    const int new_tile = p.fused ? special : -1;    // this step's rows (fused append)
-    // Tokens the caches hold for this call: all key_count of them, or with a
-    // fused append only the context_length older ones.
-    const long long held_tokens = p.fused ? ctx : key_count;
-    const int t0 = chunk * plan.tiles_per_chunk;
-    const int t1 = min(t0 + plan.tiles_per_chunk, ntiles);
-    const int pos0 = rg * plan.pos_per_group;                       // first position of the group
-    const int npos = min(plan.pos_per_group, p.k - pos0);
-    const int row0 = pos0 * p.group;                                // first row of the group
-    const int rows_here = npos * p.group;
-
-    const size_t part = ((size_t)b * p.kv_heads + c) * p.nchunks + chunk;
-    float2 *ml = p.part_ml + part * p.rows + row0;
-    float *po = p.part_o + (part * p.rows + row0) * D;
-    if (t0 >= t1) {
-        if (p.direct) {
-            // One split per request: no combine follows, so a request rejected
-            // on the device gets its NaN outputs and status bit here.
-            if (!ok && chunk == 0) {
-                if (c == 0 && rg == 0 && threadIdx.x == 0)
-                    set_status(p.dev_status, request_error_bits(p, id, ctx));
-                for (int x = threadIdx.x; x < rows_here * D; x += blockDim.x) {
-                    const int row = row0 + x / D, j = row / p.group, hp = row % p.group;
-                    p.out[(((size_t)b * p.k + j) * p.q_heads + (size_t)c * p.group + hp) * D + x % D] =
-                        __int_as_float(0x7fc00000);
-                }
-            }
-        } else {
-            for (int r = threadIdx.x; r < rows_here; r += blockDim.x)
-                ml[r] = make_float2(-INFINITY, 0.f);
-        }
-        return;
-    }
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -244,58 +466,78 @@ __global__ void __launch_bounds__(kThreads, MINB)
     uint64_t *p_full = s_full + 2;
     uint64_t *o_done = s_full + 3;
     uint64_t *q_full = s_full + 4;
-    uint64_t *fin = s_full + 5;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffMisc + 4);
+    uint64_t *q_empty = s_full + 5;
+    uint64_t *fin = s_full + 6;
+    SkShared *sk = reinterpret_cast<SkShared *>(smem + L::kOffMisc);
+    volatile int *abort_flag = &sk->abort_flag;
     float *red = reinterpret_cast<float *>(smem + L::kOffRed);
     uint8_t *s_q = smem + L::kOffQ;
     uint8_t *s_p = smem + L::kOffP;
 
-    const int n = t1 - t0;                 // tiles of this CTA
-    // Processing order of the CTA's tiles: the small tile of this step's rows
-    // (fused append; always the request's last tile index) goes first, so its
-    // work overlaps the first loads of the big tiles instead of ending the CTA.
-    const bool new_first = new_tile >= t0 && new_tile < t1;
-    auto tile_at = [t0, new_first, new_tile](int x) {
-        return new_first ? (x == 0 ? new_tile : t0 + x - 1) : t0 + x;
-    };
-    // Load / consume order of the 128-key tiles' K and V parts: K(0), then
+    // Load / consume order of a segment's n tiles' K and V parts: K(0), then
     // K(x+1) before V(x), then V(n-1), so the next tile's keys stream in and
     // its scores are computed while this tile's softmax runs.  Part index of
     // V(x) in that order (each part is KS stages):
-    auto v_part = [n](int x) { return x == n - 1 ? 2 * n - 1 : 2 * x + 2; };
+    auto v_part = [](int x, int n) { return x == n - 1 ? 2 * n - 1 : 2 * x + 2; };
 
-    // Paged caches: warp 0 resolves the pool rows of the CTA's tiles through
-    // the page table in one parallel round trip, so the producer's issue path
-    // never waits on a page-table read.
-    long long *s_rows = reinterpret_cast<long long *>(smem + L::kOffRows);
-    const bool rows_cached = paged && n <= kMaxPagedTiles;
-    if (rows_cached && warp == 0) {
-        if (lane < n) {
-            const int i = t0 + lane;
-            long long row = -1;
-            if (i != new_tile) {
-                row = paged_row(p.page_table, p.max_pages, p.page_rows, p.num_pages, b,
-                                (long long)i * kTileKeys);
-                if (row < 0) {
-                    set_status(p.dev_status, CARAT_DEV_BAD_CACHE_ID);
-                    row = (long long)p.num_pages * p.page_rows;
-                }
-            }
-            s_rows[lane] = row;
-        }
-        __syncwarp();
-    }
-
-    // Producer state (thread 0): the next stage load to issue.
+    // ------------------------------------------------------------ producer state
+    // (thread 0): the segment being loaded and the next stage load to issue.
+    SegIter pit;
+    Segment ps{};
+    bool p_have = false, p_qdone = false, alive_p = true;
+    int ppart = 0, pks = 0, psi = 0;
     uint32_t cnt = 0;
-    int ppart = 0, pks = 0;
-    bool alive_p = true;
     uint64_t pol = 0;
+    // Paged caches: the page-table entries of the two pages last used and one
+    // read ahead (the page after the newest), so a page-table read is in
+    // flight while earlier stages stream instead of stalling the issue path.
+    int pt_i0 = -1, pt_p0 = 0, pt_i1 = -1, pt_p1 = 0, pt_in = -1, pt_pn = 0;
+    auto page_of = [&](int b, int pi) -> int {
+        if (pi == pt_i0) return pt_p0;
+        if (pi == pt_i1) return pt_p1;
+        const int page = pi == pt_in ? pt_pn : p.page_table[(size_t)b * p.max_pages + pi];
+        pt_i1 = pt_i0;
+        pt_p1 = pt_p0;
+        pt_i0 = pi;
+        pt_p0 = page;
+        pt_in = -1;
+        if (pi + 1 < p.max_pages) {
+            pt_in = pi + 1;
+            pt_pn = p.page_table[(size_t)b * p.max_pages + pi + 1];
+        }
+        return page;
+    };
     // Issue stage loads in order until `limit` stages have been issued or the
-    // tiles run out; a stage is reused only after the MMA released it.
-    auto produce = [&](uint32_t limit) {
-        while (alive_p && ppart < 2 * n && cnt < limit) {
+    // range runs out; a stage is reused only after the MMA released it.  With
+    // first_only the producer stops at the end of the first segment (the
+    // next segment's Q waits for MMAs that start after the block barrier).
+    auto produce = [&](uint32_t limit, bool first_only) {
+        while (alive_p && cnt < limit) {
+            if (!p_have) {
+                if (first_only && psi > 0) return;
+                if (!pit.next(p, upr, plan.row_groups, ps)) return;
+                p_have = true;
+                p_qdone = false;
+                ppart = 0;
+                pks = 0;
+                pt_i0 = pt_i1 = pt_in = -1;
+            }
+            if (!p_qdone) {
+                // This segment's Q: the buffer is free once the previous
+                // segment's last QK product has finished.
+                if (psi > 0 &&
+                    !wait_or_abort(q_empty, (psi - 1) & 1, abort_flag, p.dev_status)) {
+                    alive_p = false;
+                    break;
+                }
+                tc::mbar_arrive_expect_tx(q_full, (D / 64) * 128 * p.group * plan.pos_per_group);
+#pragma unroll
+                for (int db = 0; db < D / 64; ++db)
+                    tc::tma_load_4d(s_q + db * L::kQBlock, &maps.q, db * 64, ps.c * p.group,
+                                    ps.rg * plan.pos_per_group, ps.b, q_full, pol);
+                p_qdone = true;
+            }
+            const int n = ps.x1 - ps.x0;
             int x;
             bool is_v;
             if (ppart == 0) {
@@ -308,101 +550,152 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 x = (ppart - 1) / 2 + ((ppart - 1) % 2 == 0 ? 1 : 0);
                 is_v = (ppart - 1) % 2 == 1;
             }
-            const int i = tile_at(x);
+            const int i = order_tile(ps, ps.x0 + x);
+            const bool special = i == ps.special;
+            if (special && is_v) {
+                // The special tile's V rows came in the stage of its K rows.
+                if (++ppart == 2 * n) {
+                    p_have = false;
+                    ++psi;
+                }
+                continue;
+            }
             const int s = cnt % NS;
             if (cnt >= NS &&
                 !wait_or_abort(&empty[s], ((cnt / NS) & 1) ^ 1, abort_flag, p.dev_status)) {
                 alive_p = false;
                 break;
             }
-            tc::mbar_arrive_expect_tx(&full[s], (i == disp_tile || i == new_tile)
-                                                    ? 2 * kDispBoxBytes
-                                                    : kStageBytes);
-            const int d0 = pks * 128;
             uint8_t *dst = smem + s * kStageBytes;
+            if (special) {
+                // One stage holds the whole special tile: D/64 boxes of 16 K
+                // rows, then D/64 boxes of 16 V rows (displaced rows of a
+                // sliding verify, or this step's rows of a fused append).
+                tc::mbar_arrive_expect_tx(&full[s], 2 * (D / 64) * kDispBoxBytes);
 #pragma unroll
-            for (int box = 0; box < 2; ++box) {
-                if (i == disp_tile) {
-                    tc::tma_load_4d(dst + box * kBoxBytes, &maps.disp, d0 + box * 64, c,
-                                    is_v ? 1 : 0, b * (p.k - 1), &full[s], pol);
-                } else if (i == new_tile) {
-                    tc::tma_load_3d(dst + box * kBoxBytes, is_v ? &maps.vnew : &maps.knew,
-                                    d0 + box * 64, c, b * p.k, &full[s], pol);
-                } else {
-                    long long row;
-                    if (ring) {
-                        row = (long long)id * p.window + (long long)i * kTileKeys;
-                    } else if (paged) {
-                        // A tile never straddles pages (page_rows is a multiple of
-                        // 128).  A page id outside the pool loads the zero fill
-                        // past the tensor's end and is reported.
-                        if (rows_cached) {
-                            row = s_rows[i - t0];
-                        } else {
-                            row = paged_row(p.page_table, p.max_pages, p.page_rows, p.num_pages,
-                                            b, (long long)i * kTileKeys);
-                            if (row < 0) {
-                                set_status(p.dev_status, CARAT_DEV_BAD_CACHE_ID);
-                                row = (long long)p.num_pages * p.page_rows;
-                            }
-                        }
+                for (int db = 0; db < D / 64; ++db) {
+                    uint8_t *kdst = dst + db * kDispBoxBytes;
+                    uint8_t *vdst = dst + (D / 64 + db) * kDispBoxBytes;
+                    if (p.fused) {
+                        tc::tma_load_3d(kdst, &maps.knew, db * 64, ps.c, ps.b * p.k, &full[s], pol);
+                        tc::tma_load_3d(vdst, &maps.vnew, db * 64, ps.c, ps.b * p.k, &full[s], pol);
                     } else {
-                        row = (long long)id * p.capacity + (long long)i * kTileKeys;
+                        tc::tma_load_4d(kdst, &maps.disp, db * 64, ps.c, 0, ps.b * (p.k - 1),
+                                        &full[s], pol);
+                        tc::tma_load_4d(vdst, &maps.disp, db * 64, ps.c, 1, ps.b * (p.k - 1),
+                                        &full[s], pol);
                     }
-                    tc::tma_load_3d(dst + box * kBoxBytes, is_v ? &maps.v : &maps.k,
-                                    d0 + box * 64, c, (int)row, &full[s], pol);
+                }
+                ++cnt;
+                if (++ppart == 2 * n) {
+                    p_have = false;
+                    ++psi;
+                }
+                continue;
+            }
+            long long row = 0;
+            {
+                if (ring) {
+                    row = (long long)ps.id * p.window + (long long)i * kTileKeys;
+                } else if (paged) {
+                    // A tile never straddles pages (page_rows is a multiple of
+                    // 128).  A page id outside the pool loads the zero fill
+                    // past the tensor's end and is reported.
+                    const long long t = (long long)i * kTileKeys;
+                    const int page = page_of(ps.b, (int)(t / p.page_rows));
+                    if (page < 0 || page >= p.num_pages) {
+                        set_status(p.dev_status, CARAT_DEV_BAD_CACHE_ID);
+                        row = (long long)p.num_pages * p.page_rows;
+                    } else {
+                        row = (long long)page * p.page_rows + t % p.page_rows;
+                    }
+                } else {
+                    row = (long long)ps.id * p.capacity + (long long)i * kTileKeys;
                 }
             }
+            tc::mbar_arrive_expect_tx(&full[s], kStageBytes);
+            const int d0 = pks * 128;
+#pragma unroll
+            for (int box = 0; box < 2; ++box)
+                tc::tma_load_3d(dst + box * kBoxBytes, is_v ? &maps.v : &maps.k, d0 + box * 64,
+                                ps.c, (int)row, &full[s], pol);
             ++cnt;
             if (++pks == KS) {
                 pks = 0;
-                ++ppart;
+                if (++ppart == 2 * n) {
+                    p_have = false;
+                    ++psi;
+                }
             }
         }
     };
 
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < NS; ++i) {
-            tc::mbar_init(&full[i], 1);
-            tc::mbar_init(&empty[i], 1);
+    // ------------------------------------------------------------ prologue
+    if (warp == 0) {
+        if (lane == 0) {
+            // descriptors first: their fetch overlaps the range computation
+            tc::tma_prefetch_map(&maps.q);
+            tc::tma_prefetch_map(&maps.k);
+            tc::tma_prefetch_map(&maps.v);
+            tc::tma_prefetch_map(p.fused ? &maps.knew : &maps.disp);
+            if (p.fused) tc::tma_prefetch_map(&maps.vnew);
+            for (int i = 0; i < NS; ++i) {
+                tc::mbar_init(&full[i], 1);
+                tc::mbar_init(&empty[i], 1);
+            }
+            tc::mbar_init(&s_full[0], 1);
+            tc::mbar_init(&s_full[1], 1);
+            tc::mbar_init(p_full, 128);
+            tc::mbar_init(o_done, 1);
+            tc::mbar_init(q_full, 1);
+            tc::mbar_init(q_empty, 1);
+            tc::mbar_init(fin, 1);
+            sk->abort_flag = 0;
+            tc::fence_mbar_init();
+            pol = tc::l2_evict_first_policy();
         }
-        tc::mbar_init(&s_full[0], 1);
-        tc::mbar_init(&s_full[1], 1);
-        tc::mbar_init(p_full, 128);
-        tc::mbar_init(o_done, 1);
-        tc::mbar_init(q_full, 1);
-        tc::mbar_init(fin, 1);
-        *abort_flag = 0;
-        tc::fence_mbar_init();
-        // Start streaming before the block-wide barrier: this thread made the
-        // barriers, and the first NS stages need no release.
-        pol = tc::l2_evict_first_policy();
-        tc::tma_prefetch_map(&maps.k);
-        tc::tma_prefetch_map(&maps.v);
-        tc::tma_prefetch_map(&maps.q);
-        tc::mbar_arrive_expect_tx(q_full, (D / 64) * 128 * p.group * plan.pos_per_group);
-#pragma unroll
-        for (int db = 0; db < D / 64; ++db)
-            tc::tma_load_4d(s_q + db * L::kQBlock, &maps.q, db * 64, c * p.group, pos0, b,
-                            q_full, pol);
-        produce(NS);
-    }
-    if (warp == 1) {
-        tc::tmem_alloc(tmem_slot, L::kTmemCols);
+        if (plan.unit_mode)
+            locate_unit(p, upr, lane, sk);
+        else
+            locate_range(p, upr, lane, sk);
+        if (lane == 0) {
+            // Start streaming before the block-wide barrier: this thread made
+            // the barriers, and the first NS stages need no release.
+            pit.init(p, sk);
+            produce(NS, true);
+        }
+    } else if (warp == 1) {
+        tc::tmem_alloc(&sk->tmem_slot, L::kTmemCols);
         tc::tmem_relinquish();
+    } else {
+        // Requests rejected on the device get NaN outputs and a status bit
+        // (requests b = blockIdx.x, blockIdx.x + grid, ...); their units have
+        // no tiles in the flattened order.
+        const int t = threadIdx.x - 64;
+        for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
+            int id;
+            long long ctx;
+            if (request_ok(p, b, &id, &ctx)) continue;
+            if (t == 0) set_status(p.dev_status, request_error_bits(p, id, ctx));
+            const size_t per = (size_t)p.k * p.q_heads * D;
+            float *o = p.out + (size_t)b * per;
+            for (size_t x = t; x < per; x += 128) o[x] = __int_as_float(0x7fc00000);
+        }
     }
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_o = tmem + 2 * N;  // O^T: KS blocks of N columns (S^T buffers: 0, N)
+    const uint32_t tmem = sk->tmem_slot;
+    // O^T buffer of segment si: KS blocks of N columns (S^T buffers: 0, N)
+    auto tmem_o_of = [&](int si) -> uint32_t {
+        return tmem + 2 * N + (L::kDoubleO ? (uint32_t)(si & 1) : 0u) * KS * N;
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            produce(0xffffffffu);
-            const bool alive = alive_p;
-            if (!alive) {
+            produce(0xffffffffu, false);
+            if (!alive_p) {
                 // Wait (bounded) for the copies already issued before leaving.
                 for (uint32_t x = cnt > (uint32_t)NS ? cnt - NS : 0; x < cnt; ++x)
                     tc::mbar_wait(&full[x % NS], (x / NS) & 1, 100000000ull);
@@ -415,66 +708,139 @@ __global__ void __launch_bounds__(kThreads, MINB)
             constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(128, N, true, false);
             const uint32_t q_base = tc::smem_u32(s_q);
             const uint32_t p_base = tc::smem_u32(s_p);
-            bool alive = wait_or_abort(q_full, 0, abort_flag, p.dev_status);
-            uint32_t cnt = 0;
-            for (int step = 0; step <= n && alive; ++step) {
-                if (step < n) {
-                    // S^T[step & 1] = K_tile . Q^T over D in steps of 16
-                    const uint32_t tmem_s = tmem + (step & 1) * N;
-                    for (int ks = 0; ks < KS && alive; ++ks) {
-                        const int s = cnt % NS;
-                        if (!wait_or_abort(&full[s], (cnt / NS) & 1, abort_flag, p.dev_status)) {
-                            alive = false;
-                            break;
-                        }
-                        tc::tc_fence_after();
-                        const uint32_t base = tc::smem_u32(smem + s * kStageBytes);
-#pragma unroll
-                        for (int box = 0; box < 2; ++box) {
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) {
-                                const uint64_t a =
-                                    tc::sdesc_sw128(base + box * kBoxBytes + kk * 32, 16, 1024);
-                                const uint64_t q = tc::sdesc_sw128(
-                                    q_base + (ks * 2 + box) * L::kQBlock + kk * 32, 16, 1024);
-                                tc::mma_bf16_ss(tmem_s, a, q, idesc_qk, (ks | box | kk) != 0);
+            SegIter it;
+            it.init(p, sk);
+            Segment sg;
+            bool alive = true;
+            uint32_t mcnt = 0, gt = 0;   // stages consumed, tiles before this segment
+            int si = 0;
+            while (alive && it.next(p, upr, plan.row_groups, sg)) {
+                const int n = sg.x1 - sg.x0;
+                if (!wait_or_abort(q_full, si & 1, abort_flag, p.dev_status)) {
+                    alive = false;
+                    break;
+                }
+                tc::tc_fence_after();
+                const uint32_t tmem_o = tmem_o_of(si);
+                int spec_stage = 0;   // stage holding the special tile's K and V rows
+                const bool sp0 = order_tile(sg, sg.x0) == sg.special;   // segment leads with it
+                for (int step = 0; step <= n && alive; ++step) {
+                    if (step < n) {
+                        // S^T[tile & 1] = K_tile . Q^T over D in steps of 16
+                        const uint32_t tmem_s = tmem + ((gt + step) & 1) * N;
+                        if (order_tile(sg, sg.x0 + step) == sg.special) {
+                            // 16 K rows per 64-d box, 2 KB apart; key rows past
+                            // 16 read other rows of the stage and are masked.
+                            const int s = mcnt % NS;
+                            if (!wait_or_abort(&full[s], (mcnt / NS) & 1, abort_flag,
+                                               p.dev_status)) {
+                                alive = false;
+                                break;
                             }
+                            tc::tc_fence_after();
+                            const uint32_t base = tc::smem_u32(smem + s * kStageBytes);
+#pragma unroll
+                            for (int db = 0; db < D / 64; ++db) {
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk) {
+                                    const uint64_t a = tc::sdesc_sw128(
+                                        base + db * kDispBoxBytes + kk * 32, 16, 1024);
+                                    const uint64_t q = tc::sdesc_sw128(
+                                        q_base + db * L::kQBlock + kk * 32, 16, 1024);
+                                    tc::mma_bf16_ss(tmem_s, a, q, idesc_qk, (db | kk) != 0);
+                                }
+                            }
+                            spec_stage = s;   // released after the tile's PV product
+                            ++mcnt;
                         }
-                        tc::mma_commit(&empty[s]);
-                        ++cnt;
+                        for (int ks = 0; ks < KS && alive &&
+                                         order_tile(sg, sg.x0 + step) != sg.special;
+                             ++ks) {
+                            const int s = mcnt % NS;
+                            if (!wait_or_abort(&full[s], (mcnt / NS) & 1, abort_flag,
+                                               p.dev_status)) {
+                                alive = false;
+                                break;
+                            }
+                            tc::tc_fence_after();
+                            const uint32_t base = tc::smem_u32(smem + s * kStageBytes);
+#pragma unroll
+                            for (int box = 0; box < 2; ++box) {
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk) {
+                                    const uint64_t a = tc::sdesc_sw128(
+                                        base + box * kBoxBytes + kk * 32, 16, 1024);
+                                    const uint64_t q = tc::sdesc_sw128(
+                                        q_base + (ks * 2 + box) * L::kQBlock + kk * 32, 16, 1024);
+                                    tc::mma_bf16_ss(tmem_s, a, q, idesc_qk, (ks | box | kk) != 0);
+                                }
+                            }
+                            tc::mma_commit(&empty[s]);
+                            ++mcnt;
+                        }
+                        if (!alive) break;
+                        tc::mma_commit(&s_full[(gt + step) & 1]);
+                        // the segment's last QK product: Q may be replaced
+                        if (step == n - 1) tc::mma_commit(q_empty);
                     }
-                    if (!alive) break;
-                    tc::mma_commit(&s_full[step & 1]);
-                }
-                if (step >= 1) {
-                    // O^T += V_tile^T . P^T over tile x's 128 keys in steps of 16
-                    const int x = step - 1;
-                    if (!wait_or_abort(p_full, x & 1, abort_flag, p.dev_status)) {
-                        alive = false;
-                        break;
-                    }
-                    tc::tc_fence_after();
-                    for (int vs = 0; vs < KS && alive; ++vs) {
-                        const int s = cnt % NS;
-                        if (!wait_or_abort(&full[s], (cnt / NS) & 1, abort_flag, p.dev_status)) {
+                    // O^T += V_tile^T . P^T over tile x's keys: at step s >= 1
+                    // that of tile s - 1.  When the ring holds only one K tile
+                    // (NS == KS) the special tile's stage must be free before the
+                    // next tile's K loads, so its product comes at step 0.
+                    constexpr bool kEarlySpecialPV = NS == KS;
+                    int x = -1;
+                    if (step == 0)
+                        x = (sp0 && kEarlySpecialPV) ? 0 : -1;
+                    else if (!(step == 1 && sp0 && kEarlySpecialPV))
+                        x = step - 1;
+                    if (x >= 0) {
+                        if (!wait_or_abort(p_full, (gt + x) & 1, abort_flag, p.dev_status)) {
                             alive = false;
                             break;
                         }
                         tc::tc_fence_after();
-                        const uint32_t base = tc::smem_u32(smem + s * kStageBytes);
+                        const bool special = order_tile(sg, sg.x0 + x) == sg.special;
+                        if (special) {
+                            // The 16 keys of the special tile: one K=16 product per
+                            // 128-d block; V boxes of 16 rows follow the K boxes.
+                            const uint32_t vbase = tc::smem_u32(smem + spec_stage * kStageBytes) +
+                                                   (D / 64) * kDispBoxBytes;
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint64_t a = tc::sdesc_sw128(base + kk * 2048, kBoxBytes, 1024);
-                            const uint64_t pp = tc::sdesc_sw128(
-                                p_base + (kk / 4) * L::kPBlock + (kk % 4) * 32, 16, 1024);
-                            tc::mma_bf16_ss(tmem_o + vs * N, a, pp, idesc_pv, (x > 0 || kk > 0));
+                            for (int vs = 0; vs < KS; ++vs) {
+                                const uint64_t a = tc::sdesc_sw128(
+                                    vbase + vs * 2 * kDispBoxBytes, kDispBoxBytes, 1024);
+                                const uint64_t pp = tc::sdesc_sw128(p_base, 16, 1024);
+                                tc::mma_bf16_ss(tmem_o + vs * N, a, pp, idesc_pv, x > 0);
+                            }
+                            tc::mma_commit(&empty[spec_stage]);
                         }
-                        tc::mma_commit(&empty[s]);
-                        ++cnt;
+                        for (int vs = 0; vs < KS && alive && !special; ++vs) {
+                            const int s = mcnt % NS;
+                            if (!wait_or_abort(&full[s], (mcnt / NS) & 1, abort_flag,
+                                               p.dev_status)) {
+                                alive = false;
+                                break;
+                            }
+                            tc::tc_fence_after();
+                            const uint32_t base = tc::smem_u32(smem + s * kStageBytes);
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint64_t a =
+                                    tc::sdesc_sw128(base + kk * 2048, kBoxBytes, 1024);
+                                const uint64_t pp = tc::sdesc_sw128(
+                                    p_base + (kk / 4) * L::kPBlock + (kk % 4) * 32, 16, 1024);
+                                tc::mma_bf16_ss(tmem_o + vs * N, a, pp, idesc_pv,
+                                                (x > 0 || kk > 0));
+                            }
+                            tc::mma_commit(&empty[s]);
+                            ++mcnt;
+                        }
+                        if (!alive) break;
+                        tc::mma_commit(o_done);
                     }
-                    if (!alive) break;
-                    tc::mma_commit(o_done);
                 }
+                gt += n;
+                ++si;
             }
             if (!alive) {
                 // Make sure every MMA this thread issued has finished.
@@ -487,301 +853,584 @@ __global__ void __launch_bounds__(kThreads, MINB)
         const int q4 = warp & 3;              // TMEM lane quadrant this warp may access
         const int t = q4 * 32 + lane;         // key of the tile / d within an O block
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-        float m_run[N], l_part[N];
-#pragma unroll
-        for (int r = 0; r < N; ++r) {
-            m_run[r] = -INFINITY;
-            l_part[r] = 0.f;
-        }
+        SegIter it;
+        it.init(p, sk);
+        Segment sg;
         bool alive = true;
-        int idx = 0;
-        // Slot that holds the newest token the caches hold (ring source).
-        const long long newest = held_tokens - 1;
-        const long long head_slot = (ring && newest >= 0) ? newest % p.window : 0;
-        // Fused append: slot of this step's first row (ring source).
-        const int base_slot = (ring && p.fused) ? (int)(ctx % p.window) : 0;
-        for (; idx < n; ++idx) {
-            const int i = tile_at(idx);
-            // warp-uniform: the TMEM load below is warp-collective
-            const bool w_ok = __all_sync(
-                kFull, wait_or_abort(&s_full[idx & 1], (idx >> 1) & 1, abort_flag, p.dev_status));
-            const uint32_t tmem_s = tmem + (idx & 1) * N;
-            float x[N];
-            if (w_ok) {
-                tc::tc_fence_after();
+        uint32_t gt = 0, cnt_base = 0;       // tiles and stages before this segment
+        int si = 0;                          // segments before this one
+        float *s_mrow = red + 12 * N;        // a finished segment's row maxima
+        float *s_lrow = red + 13 * N;        // and row sums
+        // The epilogue of a finished segment, run once the next segment's first
+        // tile is under way (or at once with a single O^T buffer).
+        struct PendingEpi {
+            bool on;
+            bool whole;
+            int si, b, c, pos0, row0, rows_here, unit, ntiles;
+            long long start, unit_start;
+        } pend{};
+        constexpr int kLdPair = N >= 32 ? 2 : 1;   // TMEM loads issued per wait
+        auto write_segment = [&](const PendingEpi &pe) {
+            const uint32_t tmo = tmem_o_of(pe.si);
+            if (pe.whole) {
+                // The segment saw every key of its rows: normalise and write.
+                // Row r = j * group + h' goes to out[b][j][c * group + h'].
+                float inv_l[N];
 #pragma unroll
-                for (int cb = 0; cb < N / 16; ++cb) {
-                    uint32_t r16[16];
-                    tc::tmem_ld16(tmem_s + lane_off + cb * 16, r16);
-                    tc::tmem_ld_wait();
+                for (int r = 0; r < N; ++r) inv_l[r] = 1.f / s_lrow[r];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) x[cb * 16 + e] = __uint_as_float(r16[e]);
-                }
-            } else {
+                for (int ob = 0; ob < KS; ++ob) {
+                    float *obase = p.out +
+                                   (((size_t)pe.b * p.k + pe.pos0) * p.q_heads +
+                                    (size_t)pe.c * p.group) * D + ob * 128 + t;
+                    int jr = 0, hp = 0;
 #pragma unroll
-                for (int r = 0; r < N; ++r) x[r] = 0.f;
-            }
-            // Position of key t of tile i and which rows may see it.
-            KeyInfo ki;
-            if (i == new_tile) {
-                ki.pos = t < p.k ? ctx + t : -1;
-                ki.data = t < p.k;
-            } else if (ring && i == disp_tile) {
-                ki.pos = (t < p.k - 1) ? ctx - p.window + 1 + t : -1;
-                ki.data = t < p.k - 1 && ki.pos >= 0;
-            } else if (ring) {
-                // Slot s holds the newest position congruent to s: head_slot - s
-                // (mod window) positions before the newest token.
-                const int slot = i * kTileKeys + t;
-                long long delta = head_slot - slot;
-                if (delta < 0) delta += p.window;
-                ki.pos = (slot < p.window && newest >= 0) ? newest - delta : -1;
-                ki.data = ki.pos >= 0;
-            } else {
-                const long long u = (long long)i * kTileKeys + t;
-                ki.pos = u < held_tokens ? u : -1;
-                ki.data = ki.pos >= 0;
-            }
-            // Query j of the group (position ctx + pos0 + j) sees the key iff
-            // j >= d0 and, for a sliding window, j < d0 + window.
-            uint64_t rowmask = 0;
-            if (ki.data) {
-                const long long d0 = ki.pos - (ctx + pos0);
-                const long long jlo = d0 < 0 ? 0 : d0;
-                long long jhi = ring ? d0 + p.window : npos;
-                if (jhi > npos) jhi = npos;
-                if (jlo < jhi) rowmask = low_bits((int)jhi * p.group) & ~low_bits((int)jlo * p.group);
-            }
-            float tmax[N];
+                    for (int cb = 0; cb < N / 16; cb += kLdPair) {
+                        // two 16-column loads in flight before one wait
+                        uint32_t r16[kLdPair][16];
 #pragma unroll
-            for (int r = 0; r < N; ++r) {
-                x[r] = ((rowmask >> r) & 1ull) ? x[r] * p.scale_log2 : -INFINITY;
-                tmax[r] = x[r];
-            }
-            const int rb = warp_transpose_reduce<N, true>(tmax, lane);
-            float *red_max = red + (idx & 1) * 4 * N;
-            constexpr int kHeld = N >= 32 ? N / 32 : 1;
+                        for (int h = 0; h < kLdPair; ++h)
+                            tc::tmem_ld16(tmo + ob * N + lane_off + (cb + h) * 16, r16[h]);
+                        tc::tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < kHeld; ++e) red_max[q4 * N + rb + e] = tmax[e];
-            if (named_bar_softmax_any(!w_ok || *abort_flag)) {
-                alive = false;
-                break;
-            }
+                        for (int h = 0; h < kLdPair; ++h) {
 #pragma unroll
-            for (int r = 0; r < N; r += 4) {
-                float4 a0 = *reinterpret_cast<const float4 *>(red_max + 0 * N + r);
-                float4 a1 = *reinterpret_cast<const float4 *>(red_max + 1 * N + r);
-                float4 a2 = *reinterpret_cast<const float4 *>(red_max + 2 * N + r);
-                float4 a3 = *reinterpret_cast<const float4 *>(red_max + 3 * N + r);
-                tmax[r + 0] = fmaxf(fmaxf(a0.x, a1.x), fmaxf(a2.x, a3.x));
-                tmax[r + 1] = fmaxf(fmaxf(a0.y, a1.y), fmaxf(a2.y, a3.y));
-                tmax[r + 2] = fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z));
-                tmax[r + 3] = fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w));
-            }
-            float alpha[N];
-            bool rescale = false;
-#pragma unroll
-            for (int r = 0; r < N; ++r) {
-                // Keep a stale running maximum unless the tile's maximum exceeds
-                // it by more than kRescaleSlack (log2 units): P stays below
-                // 2^kRescaleSlack and O^T is rescaled only when a row's maximum
-                // really moves.
-                const float mn = tmax[r] > m_run[r] + kRescaleSlack ? tmax[r] : m_run[r];
-                const float ms = mn == -INFINITY ? 0.f : mn;
-                alpha[r] = fast_exp2(m_run[r] - ms);
-                const float pr = fast_exp2(x[r] - ms);
-                l_part[r] = l_part[r] * alpha[r] + pr;
-                x[r] = pr;
-                rescale |= (mn != m_run[r]) && (m_run[r] != -INFINITY);
-                m_run[r] = mn;
-            }
-            // PV of the previous tile must be done before P and O are touched.
-            if (idx > 0) {
-                alive = __all_sync(kFull, wait_or_abort(o_done, (idx - 1) & 1, abort_flag,
-                                                        p.dev_status));
-                tc::tc_fence_after();
-            }
-            if (alive) {
-                // P^T as a K-major operand: row r, key t (two 64-key blocks).
-                uint8_t *pblk = s_p + (t / 64) * L::kPBlock;
-                const uint32_t col = t % 64;
-#pragma unroll
-                for (int r = 0; r < N; ++r) {
-                    const __nv_bfloat16 h = __float2bfloat16_rn(x[r]);
-                    *reinterpret_cast<__nv_bfloat16 *>(pblk + tc::sw128_offset(r, col)) = h;
-                }
-                if (idx > 0 && rescale) {
-#pragma unroll
-                    for (int ob = 0; ob < KS; ++ob) {
-#pragma unroll
-                        for (int cb = 0; cb < N / 16; ++cb) {
-                            uint32_t r16[16];
-                            const uint32_t addr = tmem_o + ob * N + lane_off + cb * 16;
-                            tc::tmem_ld16(addr, r16);
-                            tc::tmem_ld_wait();
-#pragma unroll
-                            for (int e = 0; e < 16; ++e)
-                                r16[e] = __float_as_uint(__uint_as_float(r16[e]) * alpha[cb * 16 + e]);
-                            tc::tmem_st16(addr, r16);
+                            for (int e = 0; e < 16; ++e) {
+                                const int r = (cb + h) * 16 + e;
+                                if (r < pe.rows_here)
+                                    obase[((size_t)jr * p.q_heads + hp) * D] =
+                                        __uint_as_float(r16[h][e]) * inv_l[r];
+                                if (++hp == p.group) {
+                                    hp = 0;
+                                    ++jr;
+                                }
+                            }
                         }
                     }
-                    tc::tmem_st_wait();
                 }
-                // Rows of the tile that hold no token of this request: zero their
-                // V rows so their contents cannot reach O through P = 0.
-                const bool tile_partial =
-                    i == disp_tile || i == new_tile ||
-                    (ring && ((long long)(i + 1) * kTileKeys > min((long long)p.window, held_tokens))) ||
-                    (!ring && (long long)(i + 1) * kTileKeys > held_tokens);
-                // Fused append into a ring: this CTA is the only one that loads
-                // tile i, and it overwrites slots of the tile once its own
-                // copies of the tile have landed.
-                bool tile_writes = false;
-                if (p.fused_write && ring && i != new_tile) {
-                    for (int j = 0; j < p.k; ++j) {
-                        int sj = base_slot + j;
-                        if (sj >= p.window) sj -= p.window;
-                        tile_writes |= sj / kTileKeys == i;
+                return;
+            }
+            // A piece of a split unit: its partial goes to this CTA's slot
+            // (0: the range's first segment, 1: its last).
+            const int slot = pe.start == sk->s ? 0 : 1;
+            const size_t base = ((size_t)blockIdx.x * 2 + slot) * N;
+            if (t == 0) {
+#pragma unroll
+                for (int r = 0; r < N; ++r)
+                    if (r < pe.rows_here) p.part_ml[base + r] = make_float2(s_mrow[r], s_lrow[r]);
+            }
+#pragma unroll
+            for (int ob = 0; ob < KS; ++ob) {
+#pragma unroll
+                for (int cb = 0; cb < N / 16; cb += kLdPair) {
+                    uint32_t r16[kLdPair][16];
+#pragma unroll
+                    for (int h = 0; h < kLdPair; ++h)
+                        tc::tmem_ld16(tmo + ob * N + lane_off + (cb + h) * 16, r16[h]);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int h = 0; h < kLdPair; ++h) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int r = (cb + h) * 16 + e;
+                            if (r < pe.rows_here)
+                                p.part_o[(base + r) * D + ob * 128 + t] = __uint_as_float(r16[h][e]);
+                        }
                     }
                 }
-                if (tile_partial || tile_writes) {
-                    for (int vs = 0; vs < KS; ++vs) {
-                        const uint32_t x_cnt = (uint32_t)v_part(idx) * KS + vs;
+            }
+            // Publish the partial, then count it: the ticket's low 16 bits
+            // count the unit's pieces that are in, its upper bits carry this
+            // call's epoch (a value from another call counts as none).
+            __threadfence();
+            named_bar_softmax_any(false);
+            if (t == 0) {
+                const long long len = sk->len;
+                const int pieces =
+                    (int)((pe.unit_start + pe.ntiles - 1) / len - pe.unit_start / len + 1);
+                unsigned long long *ticket = p.tickets + pe.unit;
+                const unsigned long long tag = p.epoch << 16;
+                unsigned long long old = *reinterpret_cast<volatile unsigned long long *>(ticket);
+                unsigned long long now;
+                while (true) {
+                    now = ((old & ~0xffffull) == tag) ? old + 1 : tag + 1;
+                    const unsigned long long seen = atomicCAS(ticket, old, now);
+                    if (seen == old) break;
+                    old = seen;
+                }
+                if ((int)(now & 0xffffull) == pieces) {
+                    const int d = sk->nduty++;
+                    sk->duty_unit[d] = pe.unit;
+                    sk->duty_tiles[d] = pe.ntiles;
+                    sk->duty_start[d] = pe.unit_start;
+                }
+            }
+        };
+        while (alive && it.next(p, upr, plan.row_groups, sg)) {
+            const uint32_t tmem_o = tmem_o_of(si);
+            const int n = sg.x1 - sg.x0;
+            const int b = sg.b, c = sg.c;
+            const long long ctx = sg.ctx;
+            const int disp_tile = p.fused ? -1 : sg.special;   // displaced rows (append done before)
+            const int new_tile = p.fused ? sg.special : -1;    // this step's rows (fused append)
+            // Tokens the caches hold for this call: all key_count of them, or
+            // with a fused append only the context_length older ones.
+            const long long held_tokens = p.fused ? ctx : ctx + p.k;
+            const int pos0 = sg.rg * plan.pos_per_group;       // first position of the group
+            const int npos = min(plan.pos_per_group, p.k - pos0);
+            const int row0 = pos0 * p.group;                   // first row of the group
+            const int rows_here = npos * p.group;
+            // Slot that holds the newest token the caches hold (ring source).
+            const long long newest = held_tokens - 1;
+            const long long head_slot = (ring && newest >= 0) ? newest % p.window : 0;
+            // Fused append: slot of this step's first row (ring source).
+            const int base_slot = (ring && p.fused) ? (int)(ctx % p.window) : 0;
+            // Segment-local index of the special tile (-1: not in this
+            // segment): its K part takes one stage and its V part none.
+            const int xs = (sg.special >= 0 && sg.x0 == 0) ? 0 : -1;
+            // Stages the producer issued for the segment's parts before part P.
+            auto stages_before = [&](int P) -> uint32_t {
+                uint32_t st = (uint32_t)P * KS;
+                if (xs >= 0) {
+                    if ((xs == 0 ? 0 : 2 * xs - 1) < P) st -= KS - 1;
+                    if (v_part(xs, n) < P) st -= KS;
+                }
+                return st;
+            };
+            float m_run[N], l_part[N];
+#pragma unroll
+            for (int r = 0; r < N; ++r) {
+                m_run[r] = -INFINITY;
+                l_part[r] = 0.f;
+            }
+            int idx = 0;
+            for (; idx < n; ++idx) {
+                const uint32_t tile = gt + idx;
+                const int i = order_tile(sg, sg.x0 + idx);
+                // warp-uniform: the TMEM load below is warp-collective
+                const bool w_ok = __all_sync(kFull, wait_or_abort(&s_full[tile & 1], (tile >> 1) & 1,
+                                                                  abort_flag, p.dev_status));
+                const uint32_t tmem_s = tmem + (tile & 1) * N;
+                float x[N];
+                if (w_ok) {
+                    tc::tc_fence_after();
+#pragma unroll
+                    for (int cb = 0; cb < N / 16; ++cb) {
+                        uint32_t r16[16];
+                        tc::tmem_ld16(tmem_s + lane_off + cb * 16, r16);
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) x[cb * 16 + e] = __uint_as_float(r16[e]);
+                    }
+                } else {
+#pragma unroll
+                    for (int r = 0; r < N; ++r) x[r] = 0.f;
+                }
+                // Position of key t of tile i and which rows may see it.
+                KeyInfo ki;
+                if (i == new_tile) {
+                    ki.pos = t < p.k ? ctx + t : -1;
+                    ki.data = t < p.k;
+                } else if (ring && i == disp_tile) {
+                    ki.pos = (t < p.k - 1) ? ctx - p.window + 1 + t : -1;
+                    ki.data = t < p.k - 1 && ki.pos >= 0;
+                } else if (ring) {
+                    // Slot s holds the newest position congruent to s: head_slot - s
+                    // (mod window) positions before the newest token.
+                    const int slot = i * kTileKeys + t;
+                    long long delta = head_slot - slot;
+                    if (delta < 0) delta += p.window;
+                    ki.pos = (slot < p.window && newest >= 0) ? newest - delta : -1;
+                    ki.data = ki.pos >= 0;
+                } else {
+                    const long long u = (long long)i * kTileKeys + t;
+                    ki.pos = u < held_tokens ? u : -1;
+                    ki.data = ki.pos >= 0;
+                }
+                // Query j of the group (position ctx + pos0 + j) sees the key iff
+                // j >= d0 and, for a sliding window, j < d0 + window.
+                uint64_t rowmask = 0;
+                if (ki.data) {
+                    const long long d0 = ki.pos - (ctx + pos0);
+                    const long long jlo = d0 < 0 ? 0 : d0;
+                    long long jhi = ring ? d0 + p.window : npos;
+                    if (jhi > npos) jhi = npos;
+                    if (jlo < jhi)
+                        rowmask = low_bits((int)jhi * p.group) & ~low_bits((int)jlo * p.group);
+                }
+                float tmax[N];
+#pragma unroll
+                for (int r = 0; r < N; ++r) {
+                    x[r] = ((rowmask >> r) & 1ull) ? x[r] * p.scale_log2 : -INFINITY;
+                    tmax[r] = x[r];
+                }
+                const int rb = warp_transpose_reduce<N, true>(tmax, lane);
+                float *red_max = red + (idx & 1) * 4 * N;
+                constexpr int kHeld = N >= 32 ? N / 32 : 1;
+#pragma unroll
+                for (int e = 0; e < kHeld; ++e) red_max[q4 * N + rb + e] = tmax[e];
+                if (named_bar_softmax_any(!w_ok || *abort_flag)) {
+                    alive = false;
+                    break;
+                }
+#pragma unroll
+                for (int r = 0; r < N; r += 4) {
+                    float4 a0 = *reinterpret_cast<const float4 *>(red_max + 0 * N + r);
+                    float4 a1 = *reinterpret_cast<const float4 *>(red_max + 1 * N + r);
+                    float4 a2 = *reinterpret_cast<const float4 *>(red_max + 2 * N + r);
+                    float4 a3 = *reinterpret_cast<const float4 *>(red_max + 3 * N + r);
+                    tmax[r + 0] = fmaxf(fmaxf(a0.x, a1.x), fmaxf(a2.x, a3.x));
+                    tmax[r + 1] = fmaxf(fmaxf(a0.y, a1.y), fmaxf(a2.y, a3.y));
+                    tmax[r + 2] = fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z));
+                    tmax[r + 3] = fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w));
+                }
+                float alpha[N];
+                bool rescale = false;
+#pragma unroll
+                for (int r = 0; r < N; ++r) {
+                    // Keep a stale running maximum unless the tile's maximum exceeds
+                    // it by more than kRescaleSlack (log2 units): P stays below
+                    // 2^kRescaleSlack and O^T is rescaled only when a row's maximum
+                    // really moves.
+                    const float mn = tmax[r] > m_run[r] + kRescaleSlack ? tmax[r] : m_run[r];
+                    const float ms = mn == -INFINITY ? 0.f : mn;
+                    alpha[r] = fast_exp2(m_run[r] - ms);
+                    const float pr = fast_exp2(x[r] - ms);
+                    l_part[r] = l_part[r] * alpha[r] + pr;
+                    x[r] = pr;
+                    rescale |= (mn != m_run[r]) && (m_run[r] != -INFINITY);
+                    m_run[r] = mn;
+                }
+                // PV of the previous tile (of this segment or the one before)
+                // must be done before P and O are touched.
+                if (tile > 0) {
+                    alive = __all_sync(kFull, wait_or_abort(o_done, (tile - 1) & 1, abort_flag,
+                                                            p.dev_status));
+                    tc::tc_fence_after();
+                }
+                if (alive) {
+                    // P^T as a K-major operand: row r, key t (two 64-key blocks).
+                    uint8_t *pblk = s_p + (t / 64) * L::kPBlock;
+                    const uint32_t col = t % 64;
+#pragma unroll
+                    for (int r = 0; r < N; ++r) {
+                        const __nv_bfloat16 h = __float2bfloat16_rn(x[r]);
+                        *reinterpret_cast<__nv_bfloat16 *>(pblk + tc::sw128_offset(r, col)) = h;
+                    }
+                    if (idx > 0 && rescale) {
+#pragma unroll
+                        for (int ob = 0; ob < KS; ++ob) {
+#pragma unroll
+                            for (int cb = 0; cb < N / 16; ++cb) {
+                                uint32_t r16[16];
+                                const uint32_t addr = tmem_o + ob * N + lane_off + cb * 16;
+                                tc::tmem_ld16(addr, r16);
+                                tc::tmem_ld_wait();
+#pragma unroll
+                                for (int e = 0; e < 16; ++e)
+                                    r16[e] = __float_as_uint(__uint_as_float(r16[e]) *
+                                                             alpha[cb * 16 + e]);
+                                tc::tmem_st16(addr, r16);
+                            }
+                        }
+                        tc::tmem_st_wait();
+                    }
+                    // Rows of the tile that hold no token of this request: zero their
+                    // V rows so their contents cannot reach O through P = 0.
+                    const bool tile_partial =
+                        i == disp_tile || i == new_tile ||
+                        (ring && ((long long)(i + 1) * kTileKeys >
+                                  min((long long)p.window, held_tokens))) ||
+                        (!ring && (long long)(i + 1) * kTileKeys > held_tokens);
+                    // Fused append into a ring: the one CTA that loads tile i
+                    // overwrites slots of the tile once its own copies of the
+                    // tile have landed.
+                    bool tile_writes = false;
+                    if (p.fused_write && ring && i != new_tile) {
+                        for (int j = 0; j < p.k; ++j) {
+                            int sj = base_slot + j;
+                            if (sj >= p.window) sj -= p.window;
+                            tile_writes |= sj / kTileKeys == i;
+                        }
+                    }
+                    if (idx == xs) {
+                        // The special tile's stage: zero its V rows that hold no
+                        // token (only the 16 rows its PV product reads).
+                        const uint32_t x_cnt =
+                            cnt_base + stages_before(idx == 0 ? 0 : 2 * idx - 1);
                         const int s = x_cnt % NS;
                         if (!wait_or_abort(&full[s], (x_cnt / NS) & 1, abort_flag, p.dev_status)) {
                             alive = false;
-                            break;
-                        }
-                        if (!ki.data && tile_partial) {
-                            uint8_t *row0p = smem + s * kStageBytes + t * 128;
+                        } else if (!ki.data && t < kDispRows) {
+                            uint8_t *vrow =
+                                smem + s * kStageBytes + (D / 64) * kDispBoxBytes + t * 128;
 #pragma unroll
-                            for (int box = 0; box < 2; ++box)
+                            for (int db = 0; db < D / 64; ++db)
 #pragma unroll
                                 for (int q = 0; q < 8; ++q)
-                                    *reinterpret_cast<uint4 *>(row0p + box * kBoxBytes + q * 16) =
-                                        make_uint4(0, 0, 0, 0);
+                                    *reinterpret_cast<uint4 *>(vrow + db * kDispBoxBytes +
+                                                               q * 16) = make_uint4(0, 0, 0, 0);
+                        }
+                    } else if (tile_partial || tile_writes) {
+                        for (int vs = 0; vs < KS; ++vs) {
+                            const uint32_t x_cnt = cnt_base + stages_before(v_part(idx, n)) + vs;
+                            const int s = x_cnt % NS;
+                            if (!wait_or_abort(&full[s], (x_cnt / NS) & 1, abort_flag,
+                                               p.dev_status)) {
+                                alive = false;
+                                break;
+                            }
+                            if (!ki.data && tile_partial) {
+                                uint8_t *row0p = smem + s * kStageBytes + t * 128;
+#pragma unroll
+                                for (int box = 0; box < 2; ++box)
+#pragma unroll
+                                    for (int q = 0; q < 8; ++q)
+                                        *reinterpret_cast<uint4 *>(row0p + box * kBoxBytes +
+                                                                   q * 16) = make_uint4(0, 0, 0, 0);
+                            }
                         }
                     }
                 }
-            }
-            tc::fence_proxy_async_smem();
-            tc::tc_fence_before();
-            if (named_bar_softmax_any(!alive || *abort_flag)) {
-                alive = false;
-                break;
-            }
-            tc::mbar_arrive(p_full);
-            if (p.fused_write && (ring || rg == 0)) {
-                // Write this step's rows whose slot this tile covers (ring), or
-                // that no loaded tile covers, or every row (cache), from the new
-                // rows to the caches: warp q4 takes rows j = q4, q4 + 4, ...
-                for (int j = q4; j < p.k; j += 4) {
-                    long long dst_row;
-                    int writer;
-                    if (ring) {
-                        int sj = base_slot + j;
-                        if (sj >= p.window) sj -= p.window;
-                        writer = sj / kTileKeys < new_tile ? sj / kTileKeys : new_tile;
-                        dst_row = (long long)id * p.window + sj;
-                    } else if (paged) {
-                        writer = new_tile;
-                        dst_row = paged_row(p.page_table, p.max_pages, p.page_rows, p.num_pages, b,
-                                            ctx + j);
-                        if (dst_row < 0) {
-                            if (lane == 0) set_status(p.dev_status, CARAT_DEV_BAD_CACHE_ID);
-                            continue;
+                tc::fence_proxy_async_smem();
+                tc::tc_fence_before();
+                if (named_bar_softmax_any(!alive || *abort_flag)) {
+                    alive = false;
+                    break;
+                }
+                tc::mbar_arrive(p_full);
+                if (p.fused_write && (ring || sg.rg == 0)) {
+                    // Write this step's rows whose slot this tile covers (ring), or
+                    // that no loaded tile covers, or every row (cache), from the new
+                    // rows to the caches: warp q4 takes rows j = q4, q4 + 4, ...
+                    for (int j = q4; j < p.k; j += 4) {
+                        long long dst_row;
+                        int writer;
+                        if (ring) {
+                            int sj = base_slot + j;
+                            if (sj >= p.window) sj -= p.window;
+                            writer = sj / kTileKeys < new_tile ? sj / kTileKeys : new_tile;
+                            dst_row = (long long)sg.id * p.window + sj;
+                        } else if (paged) {
+                            writer = new_tile;
+                            dst_row = paged_row(p.page_table, p.max_pages, p.page_rows,
+                                                p.num_pages, b, ctx + j);
+                            if (dst_row < 0) {
+                                if (lane == 0 && writer == i)
+                                    set_status(p.dev_status, CARAT_DEV_BAD_CACHE_ID);
+                                continue;
+                            }
+                        } else {
+                            writer = new_tile;
+                            dst_row = (long long)sg.id * p.capacity + ctx + j;
                         }
-                    } else {
-                        writer = new_tile;
-                        dst_row = (long long)id * p.capacity + ctx + j;
-                    }
-                    if (writer != i) continue;
-                    const size_t src = (((size_t)b * p.k + j) * p.kv_heads + c) * D;
-                    const size_t dst = ((size_t)dst_row * p.kv_heads + c) * D;
-                    const uint4 *ks = reinterpret_cast<const uint4 *>(p.k_new + src);
-                    const uint4 *vs = reinterpret_cast<const uint4 *>(p.v_new + src);
-                    uint4 *kd = reinterpret_cast<uint4 *>(p.k_dst + dst);
-                    uint4 *vd = reinterpret_cast<uint4 *>(p.v_dst + dst);
-                    // Save the row this one displaces (position ctx + j - window),
-                    // read by the same lane before it writes the same bytes.
-                    const bool save = ring && p.displaced_out && j >= 1 && ctx + j - p.window >= 0;
-                    uint4 *dk = nullptr, *dv = nullptr;
-                    if (save) {
-                        const size_t row = (size_t)p.kv_heads * D;
-                        dk = reinterpret_cast<uint4 *>(p.displaced_out +
-                                                       ((size_t)b * (p.k - 1) + (j - 1)) * 2 * row +
-                                                       (size_t)c * D);
-                        dv = dk + row / 8;
-                    }
-                    for (int e = lane; e < D / 8; e += 32) {
+                        if (writer != i) continue;
+                        const size_t src = (((size_t)b * p.k + j) * p.kv_heads + c) * D;
+                        const size_t dst = ((size_t)dst_row * p.kv_heads + c) * D;
+                        const uint4 *ks = reinterpret_cast<const uint4 *>(p.k_new + src);
+                        const uint4 *vs = reinterpret_cast<const uint4 *>(p.v_new + src);
+                        uint4 *kd = reinterpret_cast<uint4 *>(p.k_dst + dst);
+                        uint4 *vd = reinterpret_cast<uint4 *>(p.v_dst + dst);
+                        // Save the row this one displaces (position ctx + j - window),
+                        // read by the same lane before it writes the same bytes.
+                        const bool save =
+                            ring && p.displaced_out && j >= 1 && ctx + j - p.window >= 0;
+                        uint4 *dk = nullptr, *dv = nullptr;
                         if (save) {
-                            dk[e] = kd[e];
-                            dv[e] = vd[e];
+                            const size_t rowe = (size_t)p.kv_heads * D;
+                            dk = reinterpret_cast<uint4 *>(
+                                p.displaced_out + ((size_t)b * (p.k - 1) + (j - 1)) * 2 * rowe +
+                                (size_t)c * D);
+                            dv = dk + rowe / 8;
                         }
-                        kd[e] = ks[e];
-                        vd[e] = vs[e];
-                    }
-                }
-            }
-        }
-        // ------------------------------------------------------------ epilogue
-        if (alive) {
-            if (!wait_or_abort(o_done, (idx - 1) & 1, abort_flag, p.dev_status)) alive = false;
-            tc::tc_fence_after();
-        }
-        const int rbl = warp_transpose_reduce<N, false>(l_part, lane);
-        float *red_sum = red + 2 * 4 * N;
-        constexpr int kHeldL = N >= 32 ? N / 32 : 1;
-#pragma unroll
-        for (int e = 0; e < kHeldL; ++e) red_sum[q4 * N + rbl + e] = l_part[e];
-        alive = !named_bar_softmax_any(!alive || *abort_flag);
-        if (alive && p.direct) {
-            // This CTA saw every key of its rows: normalise and write the output.
-            float inv_l[N];
-#pragma unroll
-            for (int r = 0; r < N; ++r)
-                inv_l[r] = 1.f / (red_sum[r] + red_sum[N + r] + red_sum[2 * N + r] + red_sum[3 * N + r]);
-#pragma unroll
-            for (int ob = 0; ob < KS; ++ob) {
-#pragma unroll
-                for (int cb = 0; cb < N / 16; ++cb) {
-                    uint32_t r16[16];
-                    tc::tmem_ld16(tmem_o + ob * N + lane_off + cb * 16, r16);
-                    tc::tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int r = cb * 16 + e;
-                        if (r < rows_here) {
-                            const int row = row0 + r, j = row / p.group, hp = row % p.group;
-                            p.out[(((size_t)b * p.k + j) * p.q_heads + (size_t)c * p.group + hp) * D +
-                                  ob * 128 + t] = __uint_as_float(r16[e]) * inv_l[r];
+                        for (int e = lane; e < D / 8; e += 32) {
+                            if (save) {
+                                dk[e] = kd[e];
+                                dv[e] = vd[e];
+                            }
+                            kd[e] = ks[e];
+                            vd[e] = vs[e];
                         }
                     }
                 }
+                if (pend.on && (idx == 1 || n == 1)) {
+                    // The previous segment's last PV finished before this
+                    // segment's first P was written: its O^T buffer is final.
+                    // Written after this segment's second tile, while the
+                    // next tile's keys are still on their way.
+                    write_segment(pend);
+                    pend.on = false;
+                }
             }
-        } else if (alive) {
+            if (!alive) break;
+            // ------------------------------------------------ segment end
+            // Row sums over the 128 key lanes, then (max, sum) per row to
+            // shared memory for the epilogue.
+            const int rbl = warp_transpose_reduce<N, false>(l_part, lane);
+            float *red_sum = red + 2 * 4 * N;
+            constexpr int kHeldL = N >= 32 ? N / 32 : 1;
+#pragma unroll
+            for (int e = 0; e < kHeldL; ++e) red_sum[q4 * N + rbl + e] = l_part[e];
+            alive = !named_bar_softmax_any(!alive || *abort_flag);
+            if (!alive) break;
             if (t == 0) {
 #pragma unroll
                 for (int r = 0; r < N; ++r) {
-                    if (r < rows_here) {
-                        const float l = red_sum[r] + red_sum[N + r] + red_sum[2 * N + r] + red_sum[3 * N + r];
-                        ml[r] = make_float2(m_run[r], l);
-                    }
+                    s_lrow[r] = red_sum[r] + red_sum[N + r] + red_sum[2 * N + r] + red_sum[3 * N + r];
+                    s_mrow[r] = m_run[r];
                 }
             }
-#pragma unroll
-            for (int ob = 0; ob < KS; ++ob) {
-#pragma unroll
-                for (int cb = 0; cb < N / 16; ++cb) {
-                    uint32_t r16[16];
-                    tc::tmem_ld16(tmem_o + ob * N + lane_off + cb * 16, r16);
-                    tc::tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int r = cb * 16 + e;
-                        if (r < rows_here) po[(size_t)r * D + ob * 128 + t] = __uint_as_float(r16[e]);
+            pend.on = true;
+            pend.whole = sg.x0 == 0 && sg.x1 == sg.ntiles;
+            pend.si = si;
+            pend.b = b;
+            pend.c = c;
+            pend.pos0 = pos0;
+            pend.row0 = row0;
+            pend.rows_here = rows_here;
+            pend.unit = sg.unit;
+            pend.ntiles = sg.ntiles;
+            pend.start = sg.start;
+            pend.unit_start = sg.unit_start;
+            gt += n;
+            cnt_base += stages_before(2 * n);
+            ++si;
+            if (!L::kDoubleO) {
+                // One O^T buffer: the next segment's first PV overwrites it, so
+                // the output goes now.
+                alive = __all_sync(kFull, wait_or_abort(o_done, (gt - 1) & 1, abort_flag,
+                                                        p.dev_status));
+                tc::tc_fence_after();
+                if (named_bar_softmax_any(!alive || *abort_flag)) {
+                    alive = false;
+                    break;
+                }
+                write_segment(pend);
+                pend.on = false;
+            }
+        }
+        if (alive && pend.on) {
+            // The range's last segment.
+            alive = __all_sync(kFull, wait_or_abort(o_done, (gt - 1) & 1, abort_flag, p.dev_status));
+            tc::tc_fence_after();
+            if (!named_bar_softmax_any(!alive || *abort_flag)) write_segment(pend);
+            else alive = false;
+            pend.on = false;
+        }
+
+        // ------------------------------------------------ merges this CTA owes
+        // Every piece of such a unit is in: weight each piece's partial by
+        // 2^(m_piece - M) / L (M the row's maximum over pieces, L the weighted
+        // sum of the pieces' row sums) and add them up.  The stage ring is
+        // idle now: it takes the pieces' (max, sum) pairs, the weights, and
+        // blocks of the pieces' partial rows, all copied in with cp.async so
+        // that many copies are in flight at once.
+        alive = !named_bar_softmax_any(!alive || *abort_flag);
+        if (alive && sk->nduty > 0) {
+            __threadfence();
+            float2 *s_ml = reinterpret_cast<float2 *>(smem);                 // [piece][row]
+            float *s_w = reinterpret_cast<float *>(smem + kMaxPieces * N * 8); // [row][piece]
+            float4 *s_buf = reinterpret_cast<float4 *>(smem + kMaxPieces * N * 12);
+            constexpr int kBufBytes = NS * kStageBytes - kMaxPieces * N * 12;
+            constexpr int D4 = D / 4;
+            const long long len = sk->len;
+            for (int d = 0; d < sk->nduty; ++d) {
+                const int u = sk->duty_unit[d];
+                const long long u0 = sk->duty_start[d];
+                const int nt = sk->duty_tiles[d];
+                const int b = u / upr, ur = u % upr;
+                const int c = ur / plan.row_groups, rg = ur % plan.row_groups;
+                const int pos0 = rg * plan.pos_per_group;
+                const int npos = min(plan.pos_per_group, p.k - pos0);
+                const int rows_here = npos * p.group;
+                const long long g_first = u0 / len;
+                const int np = (int)((u0 + nt - 1) / len - g_first + 1);
+                // first partial row of piece q: the slot of CTA g_first + q
+                // (1 when the piece starts inside that CTA's range)
+                auto piece_base = [&](int q) -> size_t {
+                    const long long gq = g_first + q;
+                    return ((size_t)gq * 2 + (u0 > gq * len ? 1 : 0)) * N;
+                };
+                // Blocks of rb rows, two buffers: block i + 1 streams in while
+                // block i is summed.
+                int rb = kBufBytes / (2 * np * D * 4);
+                if (rb < 1) rb = 1;
+                if (rb > rows_here) rb = rows_here;
+                const int nblk = (rows_here + rb - 1) / rb;
+                auto load_block = [&](int blk) {
+                    const int r0 = blk * rb, nr = min(rb, rows_here - r0);
+                    const int chunk = nr * D4;
+                    float4 *dst = s_buf + (size_t)(blk & 1) * np * rb * D4;
+                    for (int e = t; e < np * chunk; e += 128) {
+                        const int q = e / chunk, off = e % chunk;
+                        cp_async16(&dst[e], reinterpret_cast<const float4 *>(
+                                                p.part_o + (piece_base(q) + r0) * D) + off);
+                    }
+                    cp_async_commit();
+                };
+                // the pieces' (max, sum) pairs and the first block together
+                for (int e = t; e < np * rows_here; e += 128) {
+                    const int q = e / rows_here, r = e % rows_here;
+                    if ((r & 1) == 0) {
+                        if (r + 1 < rows_here)
+                            cp_async16(&s_ml[q * N + r], &p.part_ml[piece_base(q) + r]);
+                        else
+                            s_ml[q * N + r] = __ldcg(&p.part_ml[piece_base(q) + r]);
                     }
                 }
+                cp_async_commit();
+                load_block(0);
+                cp_async_wait<1>();
+                named_bar_softmax_any(false);
+                for (int r = t; r < rows_here; r += 128) {
+                    float M = -INFINITY;
+                    for (int q = 0; q < np; ++q)
+                        if (s_ml[q * N + r].y > 0.f) M = fmaxf(M, s_ml[q * N + r].x);
+                    float lsum = 0.f;
+                    for (int q = 0; q < np; ++q) {
+                        const float2 v = s_ml[q * N + r];
+                        const float w = v.y > 0.f ? fast_exp2(v.x - M) : 0.f;
+                        s_w[r * kMaxPieces + q] = w;
+                        lsum += v.y * w;
+                    }
+                    const float inv = 1.f / lsum;
+                    for (int q = 0; q < np; ++q) s_w[r * kMaxPieces + q] *= inv;
+                }
+                for (int blk = 0; blk < nblk; ++blk) {
+                    if (blk + 1 < nblk) {
+                        load_block(blk + 1);
+                        cp_async_wait<1>();
+                    } else {
+                        cp_async_wait<0>();
+                    }
+                    named_bar_softmax_any(false);
+                    const int r0 = blk * rb, nr = min(rb, rows_here - r0);
+                    const int chunk = nr * D4;
+                    const float4 *src = s_buf + (size_t)(blk & 1) * np * rb * D4;
+                    // out row of block row rr: r = r0 + rr = j' * group + h'
+                    for (int e = t; e < chunk; e += 128) {
+                        const int rr = e / D4, d4 = e % D4, r = r0 + rr;
+                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int q = 0; q < np; ++q) {
+                            const float w = s_w[r * kMaxPieces + q];
+                            const float4 v = src[q * chunk + e];
+                            if (w != 0.f) {
+                                acc.x += v.x * w;
+                                acc.y += v.y * w;
+                                acc.z += v.z * w;
+                                acc.w += v.w * w;
+                            }
+                        }
+                        const int row = pos0 * p.group + r, j = row / p.group, hp = row - j * p.group;
+                        reinterpret_cast<float4 *>(
+                            p.out + (((size_t)b * p.k + j) * p.q_heads + (size_t)c * p.group + hp) *
+                                        D)[d4] = acc;
+                    }
+                    named_bar_softmax_any(false);
+                }
+                // The ticket is ready for the next call (a graph replay keeps
+                // its epoch, so a leftover count would be wrong).
+                if (t == 0) p.tickets[u] = 0ull;
             }
         }
     }
@@ -802,7 +1451,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
 namespace {
 
 template <int D, int N, int NS, int MINB>
-cudaError_t launch_tc(const AttnParams &p, const TcPlan &plan, const TcMaps &maps,
+cudaError_t launch_tc(const AttnParams &p, const TcPlan &plan, const TcMaps &maps, int grid,
                       cudaStream_t stream) {
     using L = Layout<D, N, NS>;
     static_assert(MINB == 1 || 2 * (L::kAlloc + 1024) <= 233472, "two CTAs must fit one SM");
@@ -816,7 +1465,6 @@ cudaError_t launch_tc(const AttnParams &p, const TcPlan &plan, const TcMaps &map
         if (e != cudaSuccess) return e;
         configured_devices[dev] = 1;
     }
-    dim3 grid(p.nchunks, p.kv_heads * plan.row_groups, p.batch);
     kernel<<<grid, kThreads, L::kAlloc, stream>>>(p, plan, maps);
     count_launches(1);
     return cudaGetLastError();
@@ -841,10 +1489,18 @@ bool tc_supported(int head_dim, int group, int k) {
     return group <= n;
 }
 
-cudaError_t launch_attention_tc(const AttnParams &p, int tiles_per_chunk, cudaStream_t stream) {
+int tc_units_per_request(int group, int k, int kv_heads) {
+    const int n = tc_rows_per_tile(group, k);
+    int ppg = n / group;
+    if (ppg > k) ppg = k;
+    return kv_heads * ((k + ppg - 1) / ppg);
+}
+
+cudaError_t launch_attention_tc(const AttnParams &p, int grid, bool unit_mode,
+                                cudaStream_t stream) {
     const int n = tc_rows_per_tile(p.group, p.k);
     TcPlan plan{};
-    plan.tiles_per_chunk = tiles_per_chunk;
+    plan.unit_mode = unit_mode ? 1 : 0;
     plan.pos_per_group = n / p.group;
     if (plan.pos_per_group > p.k) plan.pos_per_group = p.k;
     plan.row_groups = (p.k + plan.pos_per_group - 1) / plan.pos_per_group;
@@ -895,13 +1551,13 @@ cudaError_t launch_attention_tc(const AttnParams &p, int tiles_per_chunk, cudaSt
     // streaming; the others run one CTA per SM with the stage ring taking the
     // rest of shared memory.
     if (p.head_dim == 256) {
-        if (n == 16) return launch_tc<256, 16, 3, 2>(p, plan, maps, stream);
-        if (n == 32) return launch_tc<256, 32, 6, 1>(p, plan, maps, stream);
-        return launch_tc<256, 64, 5, 1>(p, plan, maps, stream);
+        if (n == 16) return launch_tc<256, 16, 3, 2>(p, plan, maps, grid, stream);
+        if (n == 32) return launch_tc<256, 32, 6, 1>(p, plan, maps, grid, stream);
+        return launch_tc<256, 64, 5, 1>(p, plan, maps, grid, stream);
     }
-    if (n == 16) return launch_tc<512, 16, 4, 1>(p, plan, maps, stream);
-    if (n == 32) return launch_tc<512, 32, 5, 1>(p, plan, maps, stream);
-    return launch_tc<512, 64, 4, 1>(p, plan, maps, stream);
+    if (n == 16) return launch_tc<512, 16, 4, 1>(p, plan, maps, grid, stream);
+    if (n == 32) return launch_tc<512, 32, 5, 1>(p, plan, maps, grid, stream);
+    return launch_tc<512, 64, 4, 1>(p, plan, maps, grid, stream);
 }
 
 }  // namespace carat

@@ -31,17 +31,20 @@ struct AttnParams {
     const uint16_t *displaced;  // [B][k-1][2][Hkv][D] (ring source, k > 1)
     const int32_t *context_lengths;
     float *out;                 // [B][k][Hq][D]
-    float2 *part_ml;            // [B][Hkv][nchunks][rows] (running max, sum) in log2 units
-    float *part_o;              // [B][Hkv][nchunks][rows][D] unnormalised
+    // Split partials (running max and sum in log2 units, unnormalised O).
+    // CUDA-core path: [B][Hkv][nchunks][rows].  Tensor-core path: two slots
+    // per CTA, [grid][2][rows per tile], with one ticket per unit.
+    float2 *part_ml;
+    float *part_o;
+    unsigned long long *tickets;   // tensor-core path: [B * units per request]
+    unsigned long long epoch;      // tensor-core path: tag of this call's tickets
     int *dev_status;
     int num_ids;                // rings / caches available
     int batch, k, q_heads, kv_heads, head_dim, group, rows;
     int window;                 // ring slots (kRing) -- positions older than p-window+1 hidden
     int capacity;               // cache rows (kLinear)
-    int chunk;                  // keys per split
-    int nchunks;                // splits per (request, KV head)
-    int tiles_per_chunk;        // tensor-core path: 128-key tiles per split (0: CUDA-core path)
-    int direct;                 // 1: one split covers every key, the kernel writes `out` itself
+    int chunk;                  // CUDA-core path: keys per split
+    int nchunks;                // CUDA-core path: splits per (request, KV head)
     // Fused append (tensor-core path): the caches hold the tokens before this
     // step and this step's rows come from k_new / v_new [B][k][Hkv][D]; when
     // fused_write is set the kernel also writes them into k_dst / v_dst.
@@ -111,18 +114,21 @@ __device__ __forceinline__ void set_status(int *status, int bits) {
     if (status) atomicOr(status, bits);
 }
 
-// Resolve request b: its cache/ring id and context length; false (and a
-// status bit) when either is out of range.
+// Whether a request's context length and cache/ring id are in range.
+__device__ __forceinline__ bool request_valid(const AttnParams &p, int id, long long ctx) {
+    if (ctx < 0 || (p.source != KeySource::kRing && ctx + p.k > p.capacity)) return false;
+    return id >= 0 && id < p.num_ids;
+}
+
+// Resolve request b: its cache/ring id and context length; false when either
+// is out of range (request_error_bits says which).
 __device__ __forceinline__ bool request_ok(const AttnParams &p, int b, int *id_out,
                                            long long *ctx_out) {
-    long long ctx = p.context_lengths[b];
-    int id = p.ids ? p.ids[b] : b;
-    bool ok = true;
-    if (ctx < 0 || (p.source != KeySource::kRing && ctx + p.k > p.capacity)) ok = false;
-    if (id < 0 || id >= p.num_ids) ok = false;
+    const long long ctx = p.context_lengths[b];
+    const int id = p.ids ? p.ids[b] : b;
     *id_out = id;
     *ctx_out = ctx;
-    return ok;
+    return request_valid(p, id, ctx);
 }
 
 // CARAT_DEV_* bits describing why request_ok rejected a request.
@@ -193,12 +199,16 @@ cudaError_t launch_attention_simt(const AttnParams &p, cudaStream_t stream);
 cudaError_t launch_combine(const AttnParams &p, cudaStream_t stream);
 
 // Tensor-core path (attention_tc.cu): rows per tile (16, 32 or 64) for a
-// group size and proposal count, whether the shape is supported, and the
-// launch of the split-K partial kernel over tiles of 128 keys.
+// group size and proposal count, CTAs resident per SM, whether the shape is
+// supported, (request, KV head, row group) units per request, and the launch
+// over tiles of 128 keys on `grid` CTAs: one CTA per unit (unit_mode, grid =
+// units) or the persistent stream-K schedule (grid = resident slots).
 constexpr int kTcTileKeys = 128;
 int tc_rows_per_tile(int group, int k);
 int tc_ctas_per_sm(int head_dim, int rows_per_tile);
 bool tc_supported(int head_dim, int group, int k);
-cudaError_t launch_attention_tc(const AttnParams &p, int tiles_per_chunk, cudaStream_t stream);
+int tc_units_per_request(int group, int k, int kv_heads);
+cudaError_t launch_attention_tc(const AttnParams &p, int grid, bool unit_mode,
+                                cudaStream_t stream);
 
 }  // namespace carat

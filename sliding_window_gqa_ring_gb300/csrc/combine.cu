@@ -1,4 +1,5 @@
-// combine.cu -- merge the split-K partial results of an attention call.
+// combine.cu -- merge the split-K partial results of a CUDA-core attention
+// call (the tensor-core kernel merges its own).
 //
 // Each key chunk c of a (request, KV head) left, per row, its running maximum
 // m_c (log2 units), its sum l_c = sum 2^(s - m_c) and its unnormalised output
@@ -30,14 +31,7 @@ __global__ void __launch_bounds__(kCombineThreads) attn_combine(const AttnParams
         for (int d = threadIdx.x; d < D; d += blockDim.x) orow[d] = __int_as_float(0x7fc00000);
         return;
     }
-    // Chunks this request actually filled.
-    int nch = p.nchunks;
-    if (p.tiles_per_chunk > 0) {
-        int disp;
-        const int tiles = tc_request_tiles(p.source, p.window, p.k, ctx + p.k, p.fused != 0, &disp);
-        nch = min(nch, (tiles + p.tiles_per_chunk - 1) / p.tiles_per_chunk);
-    }
-    nch = min(nch, kMaxCombineChunks);
+    const int nch = min(p.nchunks, kMaxCombineChunks);
 
     __shared__ float s_w[kMaxCombineChunks];
     __shared__ int s_idx[kMaxCombineChunks];

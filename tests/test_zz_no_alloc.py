@@ -63,8 +63,9 @@ def test_noalloc_matches_workspace_entry_point(which):
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
-    # 8 requests x 16 proposals x 8 query heads per KV head at head_dim 512 need
-    # about 36 MiB of split-K scratch, more than the array holds.
+    # 16 proposals x 8 query heads per KV head at head_dim 512 take 64-row
+    # tiles: two partial slots of 64 x 512 floats for each of a GB300's 152
+    # CTAs is about 40 MB of scratch, more than the array holds.
     need = carat.swa_workspace_bytes(8, 16, 16, 2, 512, 1024)
     assert need > carat.noalloc_scratch_bytes()
     q = torch.zeros((8, 16, 16, 512), dtype=torch.bfloat16, device="cuda")
