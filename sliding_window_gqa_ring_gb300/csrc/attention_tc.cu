@@ -117,12 +117,16 @@ struct Layout {
                   "merge buffers must fit the stages");
 };
 
+// K/V tensors are mapped with the head dimension cut into 64-element slabs
+// as a dimension of its own, so one copy fills a whole stage (two slabs of
+// 128 rows) or a whole special tile (every slab of 16 rows): in shared memory
+// a box lands slab after slab, each slab its rows of 128 bytes.
 struct TcMaps {
-    CUtensorMap k;     // (D, Hkv, rows)          ring slots or cache rows
+    CUtensorMap k;     // (64, rows, D/64, Hkv)            ring slots or cache rows
     CUtensorMap v;
-    CUtensorMap disp;  // (D, Hkv, 2, B*(k-1))    displaced rows, K (0) / V (1)
-    CUtensorMap q;     // (D, Hq, k, B)           queries
-    CUtensorMap knew;  // (D, Hkv, B*k)           this step's rows (fused append)
+    CUtensorMap disp;  // (64, B*(k-1), D/64, 2, Hkv)      displaced rows, K (0) / V (1)
+    CUtensorMap q;     // (D, Hq, k, B)                    queries
+    CUtensorMap knew;  // (64, B*k, D/64, Hkv)             this step's rows (fused append)
     CUtensorMap vnew;
 };
 
@@ -572,19 +576,14 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 // rows, then D/64 boxes of 16 V rows (displaced rows of a
                 // sliding verify, or this step's rows of a fused append).
                 tc::mbar_arrive_expect_tx(&full[s], 2 * (D / 64) * kDispBoxBytes);
-#pragma unroll
-                for (int db = 0; db < D / 64; ++db) {
-                    uint8_t *kdst = dst + db * kDispBoxBytes;
-                    uint8_t *vdst = dst + (D / 64 + db) * kDispBoxBytes;
-                    if (p.fused) {
-                        tc::tma_load_3d(kdst, &maps.knew, db * 64, ps.c, ps.b * p.k, &full[s], pol);
-                        tc::tma_load_3d(vdst, &maps.vnew, db * 64, ps.c, ps.b * p.k, &full[s], pol);
-                    } else {
-                        tc::tma_load_4d(kdst, &maps.disp, db * 64, ps.c, 0, ps.b * (p.k - 1),
-                                        &full[s], pol);
-                        tc::tma_load_4d(vdst, &maps.disp, db * 64, ps.c, 1, ps.b * (p.k - 1),
-                                        &full[s], pol);
-                    }
+                uint8_t *vdst = dst + (D / 64) * kDispBoxBytes;
+                if (p.fused) {
+                    tc::tma_load_4d(dst, &maps.knew, 0, ps.b * p.k, 0, ps.c, &full[s], pol);
+                    tc::tma_load_4d(vdst, &maps.vnew, 0, ps.b * p.k, 0, ps.c, &full[s], pol);
+                } else {
+                    tc::tma_load_5d(dst, &maps.disp, 0, ps.b * (p.k - 1), 0, 0, ps.c, &full[s], pol);
+                    tc::tma_load_5d(vdst, &maps.disp, 0, ps.b * (p.k - 1), 0, 1, ps.c, &full[s],
+                                    pol);
                 }
                 ++cnt;
                 if (++ppart == 2 * n) {
@@ -614,11 +613,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 }
             }
             tc::mbar_arrive_expect_tx(&full[s], kStageBytes);
-            const int d0 = pks * 128;
-#pragma unroll
-            for (int box = 0; box < 2; ++box)
-                tc::tma_load_3d(dst + box * kBoxBytes, is_v ? &maps.v : &maps.k, d0 + box * 64,
-                                ps.c, (int)row, &full[s], pol);
+            // two 64-d slabs (d = 128 pks ..) of the tile's 128 rows
+            tc::tma_load_4d(dst, is_v ? &maps.v : &maps.k, 0, (int)row, 2 * pks, ps.c, &full[s], pol);
             ++cnt;
             if (++pks == KS) {
                 pks = 0;
@@ -1508,30 +1504,34 @@ cudaError_t launch_attention_tc(const AttnParams &p, int grid, bool unit_mode,
     TcMaps maps{};
     const uint64_t D = (uint64_t)p.head_dim;
     const uint64_t row_bytes = (uint64_t)p.kv_heads * D * 2;
-    const uint32_t box3[3] = {64, 1, (uint32_t)kTileKeys};
+    const uint64_t slabs = D / 64;
     const uint64_t rows_total =
         p.source == KeySource::kPaged
             ? (uint64_t)p.num_pages * (uint64_t)p.page_rows
             : (uint64_t)p.num_ids * (uint64_t)(p.source == KeySource::kRing ? p.window : p.capacity);
-    const uint64_t dims3[3] = {D, (uint64_t)p.kv_heads, rows_total};
-    const uint64_t strides3[2] = {D * 2, row_bytes};
-    if (!make_bf16_tensor_map(&maps.k, p.k_base, 3, dims3, strides3, box3, true) ||
-        !make_bf16_tensor_map(&maps.v, p.v_base, 3, dims3, strides3, box3, true))
+    // (64 d, rows, slab, head): rows row_bytes apart, slabs 128 bytes, heads D * 2
+    const uint64_t dims_kv[4] = {64, rows_total, slabs, (uint64_t)p.kv_heads};
+    const uint64_t strides_kv[3] = {row_bytes, 128, D * 2};
+    const uint32_t box_kv[4] = {64, (uint32_t)kTileKeys, 2, 1};
+    if (!make_bf16_tensor_map(&maps.k, p.k_base, 4, dims_kv, strides_kv, box_kv, true) ||
+        !make_bf16_tensor_map(&maps.v, p.v_base, 4, dims_kv, strides_kv, box_kv, true))
         return cudaErrorInvalidValue;
     if (p.source == KeySource::kRing && p.k > 1) {
-        const uint64_t dims4[4] = {D, (uint64_t)p.kv_heads, 2, (uint64_t)p.batch * (p.k - 1)};
-        const uint64_t strides4[3] = {D * 2, row_bytes, 2 * row_bytes};
-        const uint32_t box4[4] = {64, 1, 1, (uint32_t)kDispRows};
-        if (!make_bf16_tensor_map(&maps.disp, p.displaced, 4, dims4, strides4, box4, true))
+        // displaced [B*(k-1)][2][Hkv][D]: (64 d, row, slab, K/V, head)
+        const uint64_t dims5[5] = {64, (uint64_t)p.batch * (p.k - 1), slabs, 2,
+                                   (uint64_t)p.kv_heads};
+        const uint64_t strides5[4] = {2 * row_bytes, 128, row_bytes, D * 2};
+        const uint32_t box5[5] = {64, (uint32_t)kDispRows, (uint32_t)slabs, 1, 1};
+        if (!make_bf16_tensor_map(&maps.disp, p.displaced, 5, dims5, strides5, box5, true))
             return cudaErrorInvalidValue;
     } else {
         maps.disp = maps.k;
     }
     if (p.fused) {
-        const uint64_t dimsn[3] = {D, (uint64_t)p.kv_heads, (uint64_t)p.batch * p.k};
-        const uint32_t boxn[3] = {64, 1, (uint32_t)kDispRows};
-        if (!make_bf16_tensor_map(&maps.knew, p.k_new, 3, dimsn, strides3, boxn, true) ||
-            !make_bf16_tensor_map(&maps.vnew, p.v_new, 3, dimsn, strides3, boxn, true))
+        const uint64_t dimsn[4] = {64, (uint64_t)p.batch * p.k, slabs, (uint64_t)p.kv_heads};
+        const uint32_t boxn[4] = {64, (uint32_t)kDispRows, (uint32_t)slabs, 1};
+        if (!make_bf16_tensor_map(&maps.knew, p.k_new, 4, dimsn, strides_kv, boxn, true) ||
+            !make_bf16_tensor_map(&maps.vnew, p.v_new, 4, dimsn, strides_kv, boxn, true))
             return cudaErrorInvalidValue;
     } else {
         maps.knew = maps.k;
