@@ -410,7 +410,7 @@ def run_carat(args, world, rank, local):
                 "algorithmic_bytes_per_launch": nbytes[dominant],
                 "timing": ("mean of CUDA events around every call of this kind over a second "
                            "timed region of up to 300 steps (the whole fused append+attention "
-                           "call: one kernel, plus the combine kernel when it splits the keys)")}
+                           "call: one kernel launch)")}
 
     # --- the same step with every cache in one shared pool: each sliding
     # layer's rings and the global layer's pages are allocated from one K and

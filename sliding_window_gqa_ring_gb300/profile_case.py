@@ -6,8 +6,8 @@ The layer is staged from the seeded workloads in ``synth`` (rings or caches
 written with carat_ring_append), then the step's fused append+attention call
 repeats ``--calls`` times (with ``--separate``: one carat_ring_append, then the
 attention call alone repeats), so a profiler filtered on the attention kernel
-sees exactly ``--calls`` launches.  Every case keeps a few GB or less on the
-device and reads more than the 129 MB L2 per call.
+sees exactly ``--calls`` launches.  Every case but global_mixed keeps a few
+GB or less on the device; every case reads more than the 129 MB L2 per call.
 """
 from __future__ import annotations
 
@@ -24,6 +24,8 @@ CASES = {
     "global_single": lambda: synth.global_single(),
     "global_sweep4": lambda: synth.global_sweep(4),
     "global_sweep15": lambda: synth.global_sweep(15),
+    # the mixed step's global layer: about 9 GB of caches, for one-pass captures only
+    "global_mixed": lambda: synth.mixed_step()[1],
 }
 
 
