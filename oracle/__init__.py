@@ -62,6 +62,19 @@ def _declare(lib):
     lib.oracle_ring_expected.argtypes = [vp, vp, vp, i64, i64, i64, i64, i32, i32]
     lib.oracle_displaced_expected.restype = i32
     lib.oracle_displaced_expected.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i64, i32, i32]
+    lib.oracle_attention_request_f64.restype = i32
+    lib.oracle_attention_request_f64.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i32, i32,
+                                                 i32, i64, dbl]
+    lib.oracle_e4m3_decode.restype = dbl
+    lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.oracle_e4m3_encode.argtypes = [dbl]
+    lib.oracle_quantize_bf16.restype = None
+    lib.oracle_quantize_bf16.argtypes = [vp, vp, i64, ctypes.c_float]
+    lib.oracle_ring_expected_bytes.restype = i32
+    lib.oracle_ring_expected_bytes.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64]
+    lib.oracle_displaced_expected_bytes.restype = i32
+    lib.oracle_displaced_expected_bytes.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, i64, i64]
     return lib
 
 
@@ -181,6 +194,78 @@ class Oracle:
                                                 context_length, proposal_count, window,
                                                 kv_heads, head_dim)
         _check(rc, "displaced_expected")
+        return out[:n], valid[:n].astype(bool)
+
+    # ------------------------------------------------------------- FP8 KV cache
+    def e4m3_decode(self, codes) -> np.ndarray:
+        """float64 value of each e4m3 code (NaN for the NaN codes)."""
+        codes = np.asarray(codes, dtype=np.uint8)
+        flat = [self.lib.oracle_e4m3_decode(int(c)) for c in codes.ravel()]
+        return np.asarray(flat, dtype=np.float64).reshape(codes.shape)
+
+    def e4m3_encode(self, values) -> np.ndarray:
+        """Nearest e4m3 code of each value (ties to even, saturating at 448)."""
+        values = np.asarray(values, dtype=np.float64)
+        flat = [self.lib.oracle_e4m3_encode(float(v)) for v in values.ravel()]
+        return np.asarray(flat, dtype=np.uint8).reshape(values.shape)
+
+    def quantize_bf16(self, bits, scale: float) -> np.ndarray:
+        """FP8 cache codes of bf16 values for dequantisation scale `scale`."""
+        bits = _u16(bits)
+        out = np.empty(bits.shape, dtype=np.uint8)
+        self.lib.oracle_quantize_bf16(_ptr(out), _ptr(bits), bits.size, float(scale))
+        return out
+
+    def dequantize(self, codes, scale: float) -> np.ndarray:
+        """Values an FP8 cache holds: e4m3 value x scale (float64)."""
+        table = self.e4m3_decode(np.arange(256, dtype=np.uint8)) * float(np.float32(scale))
+        return table[np.asarray(codes, dtype=np.uint8)]
+
+    def attention_request_f64(self, q, k_hist, v_hist, hist_base, context_length, window, scale):
+        """attention_request with float64 K/V histories (e.g. a dequantised FP8 cache)."""
+        q = _u16(q)
+        k_hist = np.ascontiguousarray(k_hist, dtype=np.float64)
+        v_hist = np.ascontiguousarray(v_hist, dtype=np.float64)
+        proposal_count, q_heads, head_dim = q.shape
+        hist_len, kv_heads, head_dim_k = k_hist.shape
+        if head_dim_k != head_dim or v_hist.shape != k_hist.shape:
+            raise ValueError("shape mismatch")
+        out = np.empty(q.shape, dtype=np.float64)
+        rc = self.lib.oracle_attention_request_f64(_ptr(out), _ptr(q), _ptr(k_hist),
+                                                   _ptr(v_hist), hist_base, hist_len,
+                                                   context_length, proposal_count, q_heads,
+                                                   kv_heads, head_dim, window, float(scale))
+        _check(rc, "attention_request_f64")
+        return out
+
+    def ring_expected_bytes(self, hist, hist_base, key_count, window):
+        """Expected FP8 ring [window][...row bytes] after positions [0, key_count)."""
+        hist = np.ascontiguousarray(hist, dtype=np.uint8)
+        hist_len = hist.shape[0]
+        row_bytes = int(np.prod(hist.shape[1:]))
+        ring = np.zeros((window,) + hist.shape[1:], dtype=np.uint8)
+        slot_valid = np.zeros(window, dtype=np.uint8)
+        rc = self.lib.oracle_ring_expected_bytes(_ptr(ring), _ptr(slot_valid), _ptr(hist),
+                                                 hist_base, hist_len, key_count, window,
+                                                 row_bytes)
+        _check(rc, "ring_expected_bytes")
+        return ring, slot_valid.astype(bool)
+
+    def displaced_expected_bytes(self, k_hist, v_hist, hist_base, context_length,
+                                 proposal_count, window):
+        """Expected FP8 displaced rows [proposal_count-1][2][...row] and validity."""
+        k_hist = np.ascontiguousarray(k_hist, dtype=np.uint8)
+        v_hist = np.ascontiguousarray(v_hist, dtype=np.uint8)
+        hist_len = k_hist.shape[0]
+        row_bytes = int(np.prod(k_hist.shape[1:]))
+        n = max(proposal_count - 1, 0)
+        out = np.zeros((max(n, 1), 2) + k_hist.shape[1:], dtype=np.uint8)
+        valid = np.zeros(max(n, 1), dtype=np.uint8)
+        rc = self.lib.oracle_displaced_expected_bytes(_ptr(out), _ptr(valid), _ptr(k_hist),
+                                                      _ptr(v_hist), hist_base, hist_len,
+                                                      context_length, proposal_count, window,
+                                                      row_bytes)
+        _check(rc, "displaced_expected_bytes")
         return out[:n], valid[:n].astype(bool)
 
 

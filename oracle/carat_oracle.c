@@ -44,6 +44,11 @@
  *   history  [hist_len][kv_heads][head_dim], row i holds position hist_base+i
  *   out      [proposal_count][q_heads][head_dim], double
  *
+ *  - FP8 KV cache: the cache holds e4m3 codes ("Announcing Carat ...",
+ *    section "Server": lossy FP8 e4m3 KV), here with one dequantisation
+ *    scale per tensor; the attention of such a cache is the attention of its
+ *    dequantised values (oracle_attention_request_f64).
+ *
  * Return codes: 0 = success, -1 = a needed position is not in the supplied
  * history, -2 = bad argument.
  */
@@ -83,12 +88,20 @@ int64_t oracle_window_first(int64_t position, int64_t window)
     return first > 0 ? first : 0;
 }
 
+/* Element i of a K or V history: bf16 bits (kind 0) or float64 (kind 1). */
+static double hist_value(const void *hist, int64_t i, int kind)
+{
+    if (kind == 0)
+        return bf16_value(((const uint16_t *)hist)[i]);
+    return ((const double *)hist)[i];
+}
+
 /*
  * One output row: softmax over keys t in [first, position] of
  * scale * <q, K[t]>, applied to V[t].  K and V are read for KV head `kv_head`.
  */
-int oracle_attention_row(double *out_row, const uint16_t *q_row,
-                         const uint16_t *k_hist, const uint16_t *v_hist,
+static int attention_row(double *out_row, const uint16_t *q_row,
+                         const void *k_hist, const void *v_hist, int kind,
                          int64_t hist_base, int64_t hist_len,
                          int kv_heads, int head_dim, int kv_head,
                          int64_t position, int64_t window, double scale)
@@ -107,10 +120,10 @@ int oracle_attention_row(double *out_row, const uint16_t *q_row,
 
     /* scores s_t = scale * sum_d q[d] * K[t][d] */
     for (int64_t t = first; t <= last; ++t) {
-        const uint16_t *k_row = k_hist + ((t - hist_base) * kv_heads + kv_head) * (int64_t)head_dim;
+        int64_t k_row = ((t - hist_base) * kv_heads + kv_head) * (int64_t)head_dim;
         double dot = 0.0;
         for (int d = 0; d < head_dim; ++d)
-            dot += bf16_value(q_row[d]) * bf16_value(k_row[d]);
+            dot += bf16_value(q_row[d]) * hist_value(k_hist, k_row + d, kind);
         score[t - first] = scale * dot;
     }
 
@@ -126,9 +139,9 @@ int oracle_attention_row(double *out_row, const uint16_t *q_row,
     for (int64_t t = first; t <= last; ++t) {
         double w = exp(score[t - first] - max_score);
         denom += w;
-        const uint16_t *v_row = v_hist + ((t - hist_base) * kv_heads + kv_head) * (int64_t)head_dim;
+        int64_t v_row = ((t - hist_base) * kv_heads + kv_head) * (int64_t)head_dim;
         for (int d = 0; d < head_dim; ++d)
-            out_row[d] += w * bf16_value(v_row[d]);
+            out_row[d] += w * hist_value(v_hist, v_row + d, kind);
     }
     for (int d = 0; d < head_dim; ++d)
         out_row[d] /= denom;
@@ -137,13 +150,23 @@ int oracle_attention_row(double *out_row, const uint16_t *q_row,
     return 0;
 }
 
+int oracle_attention_row(double *out_row, const uint16_t *q_row,
+                         const uint16_t *k_hist, const uint16_t *v_hist,
+                         int64_t hist_base, int64_t hist_len,
+                         int kv_heads, int head_dim, int kv_head,
+                         int64_t position, int64_t window, double scale)
+{
+    return attention_row(out_row, q_row, k_hist, v_hist, 0, hist_base, hist_len, kv_heads,
+                         head_dim, kv_head, position, window, scale);
+}
+
 /*
  * All rows of one request: proposal_count query positions x q_heads heads.
  * Query j sits at position context_length + j; query head h reads KV head
  * h / (q_heads / kv_heads).  window <= 0: global attention.
  */
-int oracle_attention_request(double *out, const uint16_t *q,
-                             const uint16_t *k_hist, const uint16_t *v_hist,
+static int attention_request(double *out, const uint16_t *q,
+                             const void *k_hist, const void *v_hist, int kind,
                              int64_t hist_base, int64_t hist_len,
                              int64_t context_length, int proposal_count,
                              int q_heads, int kv_heads, int head_dim,
@@ -157,15 +180,39 @@ int oracle_attention_request(double *out, const uint16_t *q,
         int64_t position = context_length + j;
         for (int h = 0; h < q_heads; ++h) {
             int64_t row = (int64_t)j * q_heads + h;
-            int rc = oracle_attention_row(out + row * head_dim, q + row * head_dim,
-                                          k_hist, v_hist, hist_base, hist_len,
-                                          kv_heads, head_dim, h / group,
-                                          position, window, scale);
+            int rc = attention_row(out + row * head_dim, q + row * head_dim,
+                                   k_hist, v_hist, kind, hist_base, hist_len,
+                                   kv_heads, head_dim, h / group,
+                                   position, window, scale);
             if (rc != 0)
                 return rc;
         }
     }
     return 0;
+}
+
+int oracle_attention_request(double *out, const uint16_t *q,
+                             const uint16_t *k_hist, const uint16_t *v_hist,
+                             int64_t hist_base, int64_t hist_len,
+                             int64_t context_length, int proposal_count,
+                             int q_heads, int kv_heads, int head_dim,
+                             int64_t window, double scale)
+{
+    return attention_request(out, q, k_hist, v_hist, 0, hist_base, hist_len, context_length,
+                             proposal_count, q_heads, kv_heads, head_dim, window, scale);
+}
+
+/* The same with K and V histories given as float64 values (a dequantised
+ * FP8 cache: every element is its e4m3 value times the tensor's scale). */
+int oracle_attention_request_f64(double *out, const uint16_t *q,
+                                 const double *k_hist, const double *v_hist,
+                                 int64_t hist_base, int64_t hist_len,
+                                 int64_t context_length, int proposal_count,
+                                 int q_heads, int kv_heads, int head_dim,
+                                 int64_t window, double scale)
+{
+    return attention_request(out, q, k_hist, v_hist, 1, hist_base, hist_len, context_length,
+                             proposal_count, q_heads, kv_heads, head_dim, window, scale);
 }
 
 /*
@@ -228,6 +275,117 @@ int oracle_displaced_expected(uint16_t *displaced, uint8_t *row_valid,
         memcpy(dst, k_hist + (t - hist_base) * row_elems, (size_t)row_elems * sizeof(uint16_t));
         memcpy(dst + row_elems, v_hist + (t - hist_base) * row_elems,
                (size_t)row_elems * sizeof(uint16_t));
+        row_valid[i] = 1;
+    }
+    return 0;
+}
+
+/*
+ * FP8 e4m3 (the KV-cache format of "Announcing Carat: An inference engine
+ * designed for Gemma 4", section "Server": the cache is stored in e4m3 and
+ * is lossy).  The format: 1 sign bit, 4 exponent bits with bias 7, 3
+ * mantissa bits; exponent field 0 holds subnormals m/8 * 2^-6; there is no
+ * infinity; S.1111.111 is NaN, so the largest finite value is
+ * S.1111.110 = 1.75 * 2^8 = 448.
+ */
+double oracle_e4m3_decode(uint8_t code)
+{
+    int sign = code >> 7;
+    int e = (code >> 3) & 0xf;
+    int m = code & 0x7;
+    if (e == 0xf && m == 0x7)
+        return NAN;
+    double mag = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+/*
+ * Nearest e4m3 value to x, ties to the even code (mantissa LSB 0), and
+ * magnitudes beyond 448 clamped to 448 (saturating conversion).  Written as
+ * a search over the 127 non-negative finite codes, which are increasing in
+ * value, so the rounding rule can be checked by eye.
+ */
+uint8_t oracle_e4m3_encode(double x)
+{
+    if (isnan(x))
+        return 0x7f;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs(x);
+    if (a >= 448.0)
+        return sign | 0x7e;
+    /* largest code whose value is <= a */
+    int lo = 0;
+    for (int c = 0; c <= 0x7e; ++c)
+        if (oracle_e4m3_decode((uint8_t)c) <= a)
+            lo = c;
+    if (oracle_e4m3_decode((uint8_t)lo) == a)
+        return sign | (uint8_t)lo;
+    int hi = lo + 1;
+    double dlo = a - oracle_e4m3_decode((uint8_t)lo);
+    double dhi = oracle_e4m3_decode((uint8_t)hi) - a;
+    int c;
+    if (dlo < dhi)
+        c = lo;
+    else if (dhi < dlo)
+        c = hi;
+    else
+        c = (lo & 1) == 0 ? lo : hi;
+    return sign | (uint8_t)c;
+}
+
+/*
+ * Quantise n bf16 values for an FP8 cache with dequantisation scale `scale`
+ * (value = e4m3 * scale).  Reading taken where the pages are silent: one
+ * scale per tensor (K, V), and each element is mapped as
+ * e4m3_rn(fp32(x * fp32(1 / scale))) -- the reciprocal and the product each
+ * rounded once to binary32, then one rounding to e4m3 with saturation.
+ */
+void oracle_quantize_bf16(uint8_t *dst, const uint16_t *src, int64_t n, float scale)
+{
+    float inv = 1.0f / scale;
+    for (int64_t i = 0; i < n; ++i) {
+        float prod = (float)(bf16_value(src[i]) * (double)inv); /* exact, then one rounding */
+        dst[i] = oracle_e4m3_encode((double)prod);
+    }
+}
+
+/* oracle_ring_expected for rows of `row_bytes` bytes (an FP8 ring). */
+int oracle_ring_expected_bytes(uint8_t *ring, uint8_t *slot_valid, const uint8_t *hist,
+                               int64_t hist_base, int64_t hist_len, int64_t key_count,
+                               int64_t window, int64_t row_bytes)
+{
+    if (window <= 0 || key_count < 0 || row_bytes <= 0)
+        return -2;
+    int64_t first = key_count - window > 0 ? key_count - window : 0;
+    if (key_count > 0 && (first < hist_base || key_count - 1 >= hist_base + hist_len))
+        return -1;
+    for (int64_t t = first; t < key_count; ++t) {
+        int64_t s = oracle_ring_slot(t, window);
+        memcpy(ring + s * row_bytes, hist + (t - hist_base) * row_bytes, (size_t)row_bytes);
+        slot_valid[s] = 1;
+    }
+    return 0;
+}
+
+/* oracle_displaced_expected for rows of `row_bytes` bytes (an FP8 ring). */
+int oracle_displaced_expected_bytes(uint8_t *displaced, uint8_t *row_valid,
+                                    const uint8_t *k_hist, const uint8_t *v_hist,
+                                    int64_t hist_base, int64_t hist_len, int64_t context_length,
+                                    int proposal_count, int64_t window, int64_t row_bytes)
+{
+    if (proposal_count < 1 || window <= 0 || row_bytes <= 0)
+        return -2;
+    for (int i = 0; i < proposal_count - 1; ++i) {
+        int64_t t = context_length - window + 1 + i;
+        uint8_t *dst = displaced + (int64_t)i * 2 * row_bytes;
+        if (t < 0) {
+            row_valid[i] = 0;
+            continue;
+        }
+        if (t < hist_base || t >= hist_base + hist_len)
+            return -1;
+        memcpy(dst, k_hist + (t - hist_base) * row_bytes, (size_t)row_bytes);
+        memcpy(dst + row_bytes, v_hist + (t - hist_base) * row_bytes, (size_t)row_bytes);
         row_valid[i] = 1;
     }
     return 0;

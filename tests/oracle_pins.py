@@ -368,9 +368,130 @@ def pin_displaced_covers_windows(orc):
         assert sum(dvalid) == len(lost)
 
 
+# ---------------------------------------------------------------------------
+# FP8 (e4m3) KV cache ("Announcing Carat ...", section "Server": the KV cache
+# is stored as FP8 e4m3 and is lossy)
+# ---------------------------------------------------------------------------
+
+def _torch_e4m3_value(codes):
+    """Library route: PyTorch's float8_e4m3fn reinterpretation of the bytes."""
+    t = torch.from_numpy(np.asarray(codes, dtype=np.uint8).copy())
+    return t.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def _torch_e4m3_code(values_f32):
+    """Library route: PyTorch's float32 -> float8_e4m3fn conversion (round to
+    nearest even; used only for values inside the finite range)."""
+    t = torch.from_numpy(np.asarray(values_f32, dtype=np.float32).copy())
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def pin_e4m3_format_values(orc):
+    """Values the e4m3 format fixes: 1.0 = 0x38, the largest finite 448 =
+    0x7e, the smallest normal 2^-6 = 0x08, the smallest subnormal 2^-9 = 0x01,
+    the largest subnormal 7 * 2^-9 = 0x07, NaN = 0x7f, sign in bit 7; and the
+    decoded value of every code agrees with PyTorch's float8_e4m3fn."""
+    known = {0x00: 0.0, 0x38: 1.0, 0xB8: -1.0, 0x7E: 448.0, 0xFE: -448.0, 0x08: 2.0 ** -6,
+             0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x40: 2.0, 0x3C: 1.5, 0x77: 240.0}
+    for c, v in known.items():
+        assert orc.e4m3_decode([c])[0] == v, (hex(c), v)
+    assert np.isnan(orc.e4m3_decode([0x7F, 0xFF])).all()
+    codes = np.arange(256, dtype=np.uint8)
+    mine = orc.e4m3_decode(codes)
+    lib = _torch_e4m3_value(codes)
+    both_nan = np.isnan(mine) & np.isnan(lib)
+    assert np.array_equal(mine[~both_nan], lib[~both_nan])
+    assert both_nan.sum() == 2
+
+
+def pin_e4m3_rounding(orc):
+    """Encoding rounds to the nearest value with ties to the even code (as
+    PyTorch's conversion does inside the finite range), saturates beyond 448,
+    and every finite code round-trips."""
+    assert list(orc.e4m3_encode([1.0625, 1.1875, 2.0 ** -10, 3 * 2.0 ** -10, -1.0625])) == \
+        [0x38, 0x3A, 0x00, 0x02, 0xB8]
+    assert list(orc.e4m3_encode([449.0, 464.0, 1e9, -500.0, 447.0])) == [0x7E, 0x7E, 0x7E, 0xFE,
+                                                                        0x7E]
+    rng = np.random.default_rng(30)
+    x = np.concatenate([rng.standard_normal(3000) * 8, rng.standard_normal(1000) * 0.01,
+                        rng.uniform(-448, 448, 1000)]).astype(np.float32)
+    assert np.array_equal(orc.e4m3_encode(x.astype(np.float64)), _torch_e4m3_code(x))
+    codes = np.arange(256, dtype=np.uint8)
+    vals = orc.e4m3_decode(codes)
+    fin = ~np.isnan(vals)
+    assert np.array_equal(orc.e4m3_encode(vals[fin]), codes[fin])
+
+
+def pin_quantize_bf16(orc):
+    """FP8 cache codes: with scale 1 (or a power of two, where the product is
+    exact) they are the e4m3 codes of the scaled values; with any scale they
+    equal PyTorch's float32 product by float32(1/scale) converted to
+    float8_e4m3fn (inside the finite range)."""
+    rng = np.random.default_rng(31)
+    bits = _rand_bf16(rng, (4000,), scale=3.0)
+    vals = _val(bits)
+    assert np.array_equal(orc.quantize_bf16(bits, 1.0), orc.e4m3_encode(vals))
+    assert np.array_equal(orc.quantize_bf16(bits, 0.25), orc.e4m3_encode(vals * 4.0))
+    for scale in (0.0123, 0.37, 1.7):
+        inv = np.float32(1.0) / np.float32(scale)
+        prod = (synth.bf16_to_float(bits).astype(np.float32) * inv).astype(np.float32)
+        inside = np.abs(prod) < 448
+        mine = orc.quantize_bf16(bits, scale)
+        assert np.array_equal(mine[inside], _torch_e4m3_code(prod[inside]))
+        assert (mine[~inside] & 0x7F == 0x7E).all()
+
+
+def pin_attention_f64(orc):
+    """The float64-history attention equals the bf16 one on bf16-exact values
+    and PyTorch's float64 scaled_dot_product_attention on dequantised FP8
+    values."""
+    rng = np.random.default_rng(32)
+    q = _rand_bf16(rng, (3, 4, 8))
+    kh = _rand_bf16(rng, (20, 2, 8))
+    vh = _rand_bf16(rng, (20, 2, 8))
+    a = orc.attention_request(q, kh, vh, 0, 17, 8, 0.35)
+    b = orc.attention_request_f64(q, _val(kh), _val(vh), 0, 17, 8, 0.35)
+    assert np.array_equal(a, b)
+    kd = orc.dequantize(orc.quantize_bf16(kh, 0.05), 0.05)
+    vd = orc.dequantize(orc.quantize_bf16(vh, 0.02), 0.02)
+    got = orc.attention_request_f64(q, kd, vd, 0, 17, 8, 0.35)
+    kq, hq, d = q.shape
+    qt = torch.from_numpy(_val(q)).permute(1, 0, 2).unsqueeze(0)
+    kt = torch.from_numpy(kd).permute(1, 0, 2).unsqueeze(0).repeat_interleave(2, dim=1)
+    vt = torch.from_numpy(vd).permute(1, 0, 2).unsqueeze(0).repeat_interleave(2, dim=1)
+    mask = torch.zeros(kq, 20, dtype=torch.bool)
+    for j in range(kq):
+        p = 17 + j
+        mask[j, max(0, p - 7):p + 1] = True
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=0.35)
+    ref = ref.squeeze(0).permute(1, 0, 2).numpy()
+    assert np.allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def pin_ring_bytes_match_rows(orc):
+    """The byte-row ring and displaced rows place whole rows exactly as the
+    bf16 versions do (checked on the same data viewed as bytes)."""
+    rng = np.random.default_rng(33)
+    window = 8
+    for (ctx, k) in [(20, 4), (5, 3), (13, 1)]:
+        n = ctx + k
+        kh = _rand_bf16(rng, (n, 2, 4))
+        vh = _rand_bf16(rng, (n, 2, 4))
+        ring16, valid16 = orc.ring_expected(kh, 0, n, window)
+        ring8, valid8 = orc.ring_expected_bytes(kh.view(np.uint8), 0, n, window)
+        assert np.array_equal(valid16, valid8)
+        assert np.array_equal(ring16.view(np.uint8)[valid16], ring8[valid8])
+        d16, dv16 = orc.displaced_expected(kh, vh, 0, ctx, k, window)
+        d8, dv8 = orc.displaced_expected_bytes(kh.view(np.uint8), vh.view(np.uint8), 0, ctx, k,
+                                               window)
+        assert np.array_equal(dv16, dv8)
+        assert np.array_equal(d16.view(np.uint8)[dv16], d8[dv8])
+
+
 ALL_PINS = [
     pin_sdpa_sliding, pin_sdpa_global, pin_single_key, pin_uniform_window_golden,
     pin_two_keys, pin_saturated, pin_permutation_invariance, pin_padded_tail, pin_causal,
     pin_window_covers_context, pin_gqa_repeat, pin_row_matches_request, pin_ring_golden,
-    pin_ring_is_rotated_window, pin_displaced_covers_windows,
+    pin_ring_is_rotated_window, pin_displaced_covers_windows, pin_e4m3_format_values,
+    pin_e4m3_rounding, pin_quantize_bf16, pin_attention_f64, pin_ring_bytes_match_rows,
 ]

@@ -29,9 +29,10 @@ MUTATIONS = {
                          "int64_t position = context_length + proposal_count - 1 - j;"),
     "bf16_shift": ("uint32_t word = ((uint32_t)bits) << 16;",
                    "uint32_t word = ((uint32_t)bits) << 15;"),
-    "reversed_dim": ("dot += bf16_value(q_row[d]) * bf16_value(k_row[d]);",
-                     "dot += bf16_value(q_row[d]) * bf16_value(k_row[head_dim - 1 - d]);"),
-    "v_from_k": ("const uint16_t *v_row = v_hist +", "const uint16_t *v_row = k_hist +"),
+    "reversed_dim": ("dot += bf16_value(q_row[d]) * hist_value(k_hist, k_row + d, kind);",
+                     "dot += bf16_value(q_row[d]) * hist_value(k_hist, k_row + head_dim - 1 - d, kind);"),
+    "v_from_k": ("out_row[d] += w * hist_value(v_hist, v_row + d, kind);",
+                 "out_row[d] += w * hist_value(k_hist, v_row + d, kind);"),
     "slot_rule": ("return position % window;", "return (position + 1) % window;"),
     "key_count_rule": ("return context_length + proposal_count;",
                        "return context_length + proposal_count - 1;"),
@@ -39,6 +40,14 @@ MUTATIONS = {
                         "int64_t first = key_count - window + 1 > 0 ? key_count - window + 1 : 0;"),
     "displaced_offset": ("int64_t t = context_length - window + 1 + i;",
                          "int64_t t = context_length - window + i;"),
+    "e4m3_bias": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
+    "e4m3_subnormal_exponent": ("ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
+    "e4m3_ties_up": ("c = (lo & 1) == 0 ? lo : hi;", "c = hi;"),
+    "e4m3_overflow_to_nan": ("return sign | 0x7e;", "return 0x7f;"),
+    "e4m3_sign_dropped": ("return sign ? -mag : mag;", "return mag;"),
+    "quantize_no_reciprocal": ("float inv = 1.0f / scale;", "float inv = scale;"),
+    "f64_history_reads_bf16": ("return ((const double *)hist)[i];",
+                               "return bf16_value(((const uint16_t *)hist)[i]);"),
 }
 
 
