@@ -369,9 +369,57 @@ int carat_pool_alloc_pages(carat_pool *pool, int n, int32_t *out_pages);
 int carat_pool_free_pages(carat_pool *pool, int n, const int32_t *pages);
 int carat_pool_stats(carat_pool *pool, int32_t *out4);
 
+/*
+ * FP8 (e4m3) sliding-window rings -- "Announcing Carat: An inference engine
+ * designed for Gemma 4", section "Server": the KV cache is stored as FP8
+ * e4m3, which is lossy (outside the bit-exact comparison).  The pages give
+ * no scaling scheme; here each ring tensor has one dequantisation scale:
+ * the value of a stored byte is e4m3(byte) * k_scale (K) or * v_scale (V).
+ *
+ * carat_ring_append_fp8 -- carat_ring_append for e4m3 rings.  k_ring, v_ring
+ *   are uint8 [num_rings][window][kv_heads][head_dim]; k_new, v_new stay bf16
+ *   [batch][proposal_count][kv_heads][head_dim]; each element x is stored as
+ *   e4m3_rn_satfinite(fp32(x * fp32(1 / scale))) (one binary32 product, then
+ *   round to nearest even, magnitudes past 448 saturate).  displaced, when
+ *   given, is uint8 [batch][proposal_count-1][2][kv_heads][head_dim] and
+ *   receives the overwritten rows' bytes.  k_scale, v_scale: finite, > 0,
+ *   with a finite reciprocal.  kv_heads * head_dim must be a multiple of 16.
+ *
+ * carat_ring_rollback_fp8 -- carat_ring_rollback for e4m3 rings and their
+ *   uint8 displaced rows (the bytes are copied back unchanged).
+ *
+ * carat_swa_attention_fp8 -- carat_swa_attention over e4m3 rings: the
+ *   attention of the dequantised K and V (bf16 queries, fp32 out).  Each e4m3
+ *   value is widened exactly to bf16 on chip; k_scale scales the scores and
+ *   v_scale the output.  head_dim 256 only (CARAT_ERR_UNSUPPORTED else).  The
+ *   workspace it needs is at most carat_swa_workspace_bytes for the same
+ *   sizes.  Other arguments, limits and device-side error handling as in
+ *   carat_swa_attention.
+ */
+carat_status carat_ring_append_fp8(void *k_ring, void *v_ring, int num_rings,
+                                   const int32_t *ring_ids, const void *k_new,
+                                   const void *v_new, const int32_t *context_lengths,
+                                   int proposal_count, void *displaced, int batch,
+                                   int kv_heads, int head_dim, int window, float k_scale,
+                                   float v_scale, void *stream);
+carat_status carat_ring_rollback_fp8(void *k_ring, void *v_ring, int num_rings,
+                                     const int32_t *ring_ids, const void *displaced,
+                                     const int32_t *context_lengths, const int32_t *accepted,
+                                     int proposal_count, int batch, int kv_heads, int head_dim,
+                                     int window, void *stream);
+carat_status carat_swa_attention_fp8(float *out, const void *queries, const void *k_ring,
+                                     const void *v_ring, int num_rings,
+                                     const int32_t *ring_ids, const void *displaced,
+                                     const int32_t *context_lengths, int proposal_count,
+                                     int batch, int q_heads, int kv_heads, int head_dim,
+                                     int window, float scale, float k_scale, float v_scale,
+                                     void *workspace, size_t workspace_bytes, void *stream);
+
 /* Workspace bytes the attention calls need for these sizes (the same for the
  * plain and the fused-append entry points; 0 if the sizes are invalid, or if
- * the call needs no scratch).  Pure host arithmetic; no CUDA call. */
+ * the call needs no scratch).  Host arithmetic and a query of the current
+ * device's SM count (a GB300's 152 when no device is visible); a launch on a
+ * device with more SMs checks the size again and returns CARAT_ERR_WORKSPACE. */
 size_t carat_swa_workspace_bytes(int batch, int proposal_count, int q_heads, int kv_heads,
                                  int head_dim, int window);
 size_t carat_global_workspace_bytes(int batch, int proposal_count, int q_heads,

@@ -43,6 +43,7 @@ EXPORTED = (
     "carat_ring_rollback", "carat_global_append_verify_attention_paged", "carat_paged_append",
     "carat_pool_create", "carat_pool_destroy", "carat_pool_alloc_ring", "carat_pool_free_ring",
     "carat_pool_alloc_pages", "carat_pool_free_pages", "carat_pool_stats",
+    "carat_ring_append_fp8", "carat_ring_rollback_fp8", "carat_swa_attention_fp8",
 )
 
 
@@ -108,6 +109,15 @@ def _declare(lib):
     lib.carat_pool_free_pages.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int32)]
     lib.carat_pool_stats.restype = i32
     lib.carat_pool_stats.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+    lib.carat_ring_append_fp8.restype = i32
+    lib.carat_ring_append_fp8.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
+                                          f32, f32, vp]
+    lib.carat_ring_rollback_fp8.restype = i32
+    lib.carat_ring_rollback_fp8.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                            vp]
+    lib.carat_swa_attention_fp8.restype = i32
+    lib.carat_swa_attention_fp8.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, i32, i32, i32, i32,
+                                            i32, i32, f32, f32, f32, vp, sz, vp]
     lib.carat_global_append_verify_attention.restype = i32
     lib.carat_global_append_verify_attention.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, i32,
                                                          i32, i32, i32, i32, i32, f32, vp, sz, vp]
@@ -391,3 +401,55 @@ def kernel_launches() -> int:
 def workspace_tensor(nbytes: int, device=None) -> torch.Tensor:
     """A 256-byte aligned uint8 CUDA tensor of at least nbytes (torch owns it)."""
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+# ---------------------------------------------------------------------------
+# FP8 (e4m3) rings: uint8 tensors, one dequantisation scale per tensor
+# ---------------------------------------------------------------------------
+
+def carat_ring_append_fp8(k_ring, v_ring, k_new, v_new, context_lengths, *, k_scale, v_scale,
+                          ring_ids=None, displaced=None, window=None, stream=None):
+    """carat_ring_append into e4m3 rings (uint8 [num_rings][window][Hkv][D]);
+    new rows stay bf16 and are quantised as e4m3(fp32(x * fp32(1/scale)))."""
+    _expect(k_ring, torch.uint8, "k_ring")
+    _expect(v_ring, torch.uint8, "v_ring")
+    _expect(k_new, torch.bfloat16, "k_new")
+    _expect(context_lengths, torch.int32, "context_lengths")
+    if displaced is not None:
+        _expect(displaced, torch.uint8, "displaced")
+    num_rings, ring_window, kv_heads, head_dim = k_ring.shape
+    batch, k = k_new.shape[0], k_new.shape[1]
+    _check(library().carat_ring_append_fp8(
+        _ptr(k_ring), _ptr(v_ring), num_rings, _ptr(ring_ids), _ptr(k_new), _ptr(v_new),
+        _ptr(context_lengths), k, _ptr(displaced), batch, kv_heads, head_dim,
+        ring_window if window is None else window, float(k_scale), float(v_scale),
+        _stream(stream)), "carat_ring_append_fp8")
+
+
+def carat_ring_rollback_fp8(k_ring, v_ring, displaced, context_lengths, accepted,
+                            proposal_count, *, ring_ids=None, window=None, stream=None):
+    """carat_ring_rollback for e4m3 rings and their uint8 displaced rows."""
+    _expect(k_ring, torch.uint8, "k_ring")
+    _expect(accepted, torch.int32, "accepted")
+    num_rings, ring_window, kv_heads, head_dim = k_ring.shape
+    batch = context_lengths.shape[0]
+    _check(library().carat_ring_rollback_fp8(
+        _ptr(k_ring), _ptr(v_ring), num_rings, _ptr(ring_ids), _ptr(displaced),
+        _ptr(context_lengths), _ptr(accepted), int(proposal_count), batch, kv_heads, head_dim,
+        ring_window if window is None else window, _stream(stream)), "carat_ring_rollback_fp8")
+
+
+def carat_swa_attention_fp8(out, queries, k_ring, v_ring, context_lengths, *, scale, k_scale,
+                            v_scale, workspace, ring_ids=None, displaced=None, stream=None):
+    """Sliding-window attention over e4m3 rings (dequantised: byte value x scale)."""
+    _expect(queries, torch.bfloat16, "queries")
+    _expect(out, torch.float32, "out")
+    _expect(k_ring, torch.uint8, "k_ring")
+    batch, k, q_heads, head_dim = queries.shape
+    num_rings, window, kv_heads, _ = k_ring.shape
+    _check(library().carat_swa_attention_fp8(
+        _ptr(out), _ptr(queries), _ptr(k_ring), _ptr(v_ring), num_rings, _ptr(ring_ids),
+        _ptr(displaced), _ptr(context_lengths), k, batch, q_heads, kv_heads, head_dim, window,
+        float(scale), float(k_scale), float(v_scale), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)),
+        "carat_swa_attention_fp8")

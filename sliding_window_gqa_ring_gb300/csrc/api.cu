@@ -46,6 +46,7 @@ bool supported_head_dim(int d) { return d == 256 || d == 512; }
 struct SplitPlan {
     bool tc = false;           // tensor-core kernel (else CUDA-core kernel + combine)
     bool unit_mode = false;    // tensor-core path: one CTA per unit (else stream-K)
+    bool fp8 = false;          // tensor-core path: FP8 e4m3 rings
     int grid = 0;              // tensor-core path: CTAs launched
     int chunk = 0;             // CUDA-core path: keys per split
     int nchunks = 0;           // CUDA-core path: splits per (request, KV head)
@@ -107,11 +108,13 @@ SplitPlan simt_plan(long long pairs, long long keys, int rows, int head_dim) {
 // CTA each.  Otherwise one CTA per resident slot runs the stream-K schedule;
 // each keeps two partial slots (the first and last segment of its range), and
 // each unit a ticket.  The workspace is sized for stream-K either way.
-SplitPlan tc_plan(int batch, int group, int k, int kv_heads, int head_dim, long long max_tiles) {
+SplitPlan tc_plan(int batch, int group, int k, int kv_heads, int head_dim, long long max_tiles,
+                  bool fp8 = false) {
     SplitPlan p;
     p.tc = true;
+    p.fp8 = fp8;
     const int n = tc_rows_per_tile(group, k);
-    const int slots_total = tc_ctas_per_sm(head_dim, n) * device_sm_count();
+    const int slots_total = tc_ctas_per_sm(head_dim, n, fp8) * device_sm_count();
     const long long units = (long long)batch * tc_units_per_request(group, k, kv_heads);
     p.unit_mode = units >= slots_total && max_tiles <= 16;
     p.grid = p.unit_mode ? (int)units : slots_total;
@@ -192,7 +195,7 @@ SplitPlan global_plan(int batch, int proposal_count, int q_heads, int kv_heads, 
 }
 
 cudaError_t launch_attention(const AttnParams &p, const SplitPlan &plan, cudaStream_t stream) {
-    if (plan.tc) return launch_attention_tc(p, plan.grid, plan.unit_mode, stream);
+    if (plan.tc) return launch_attention_tc(p, plan.grid, plan.unit_mode, plan.fp8, stream);
     cudaError_t e = launch_attention_simt(p, stream);
     if (e != cudaSuccess) return e;
     return launch_combine(p, stream);
@@ -593,6 +596,136 @@ carat_status carat_ring_rollback(void *k_ring, void *v_ring, int num_rings,
     p.head_dim = head_dim;
     p.window = window;
     return launch_status(launch_ring_rollback(p, accepted, static_cast<cudaStream_t>(stream)));
+}
+
+// ---------------------------------------------------------------------------
+// FP8 (e4m3) rings: "Announcing Carat ...", section "Server" (the KV cache is
+// FP8 e4m3; lossy).  One dequantisation scale per tensor (K, V).
+// ---------------------------------------------------------------------------
+
+static bool fp8_scale_ok(float s) { return std::isfinite(s) && s > 0.f && std::isfinite(1.f / s); }
+
+carat_status carat_ring_append_fp8(void *k_ring, void *v_ring, int num_rings,
+                                   const int32_t *ring_ids, const void *k_new, const void *v_new,
+                                   const int32_t *context_lengths, int proposal_count,
+                                   void *displaced, int batch, int kv_heads, int head_dim,
+                                   int window, float k_scale, float v_scale, void *stream) {
+    if (batch < 0 || kv_heads < 1 || head_dim < 1 || window < 1 || proposal_count < 1 ||
+        proposal_count > window || num_rings < 1 || !fp8_scale_ok(k_scale) ||
+        !fp8_scale_ok(v_scale))
+        return CARAT_ERR_INVALID_ARG;
+    if (((long long)kv_heads * head_dim) % 16 != 0) return CARAT_ERR_INVALID_ARG;
+    if (displaced && proposal_count > kMaxProposals) return CARAT_ERR_INVALID_ARG;
+    if (!ring_ids && num_rings < batch) return CARAT_ERR_INVALID_ARG;
+    if (batch == 0) return CARAT_OK;
+    if (!k_ring || !v_ring || !k_new || !v_new || !context_lengths) return CARAT_ERR_INVALID_ARG;
+    if (!aligned16(k_ring) || !aligned16(v_ring) || !aligned16(k_new) || !aligned16(v_new) ||
+        (displaced && !aligned16(displaced)))
+        return CARAT_ERR_INVALID_ARG;
+    AppendParams p{};
+    p.k_ring = static_cast<uint16_t *>(k_ring);
+    p.v_ring = static_cast<uint16_t *>(v_ring);
+    p.ids = ring_ids;
+    p.k_new = static_cast<const uint16_t *>(k_new);
+    p.v_new = static_cast<const uint16_t *>(v_new);
+    p.context_lengths = context_lengths;
+    p.displaced = (proposal_count > 1) ? static_cast<uint16_t *>(displaced) : nullptr;
+    p.dev_status = device_status_ptr();
+    p.num_ids = num_rings;
+    p.batch = batch;
+    p.k = proposal_count;
+    p.kv_heads = kv_heads;
+    p.head_dim = head_dim;
+    p.window = window;
+    p.elem_bytes = 1;
+    p.k_inv = 1.f / k_scale;
+    p.v_inv = 1.f / v_scale;
+    return launch_status(launch_ring_append_fp8(p, static_cast<cudaStream_t>(stream)));
+}
+
+carat_status carat_ring_rollback_fp8(void *k_ring, void *v_ring, int num_rings,
+                                     const int32_t *ring_ids, const void *displaced,
+                                     const int32_t *context_lengths, const int32_t *accepted,
+                                     int proposal_count, int batch, int kv_heads, int head_dim,
+                                     int window, void *stream) {
+    if (batch < 0 || kv_heads < 1 || head_dim < 1 || window < 1 || proposal_count < 2 ||
+        proposal_count > kMaxProposals || proposal_count > window || num_rings < 1)
+        return CARAT_ERR_INVALID_ARG;
+    if (((long long)kv_heads * head_dim) % 16 != 0) return CARAT_ERR_INVALID_ARG;
+    if (!ring_ids && num_rings < batch) return CARAT_ERR_INVALID_ARG;
+    if (batch == 0) return CARAT_OK;
+    if (!k_ring || !v_ring || !displaced || !context_lengths || !accepted)
+        return CARAT_ERR_INVALID_ARG;
+    if (!aligned16(k_ring) || !aligned16(v_ring) || !aligned16(displaced))
+        return CARAT_ERR_INVALID_ARG;
+    AppendParams p{};
+    p.k_ring = static_cast<uint16_t *>(k_ring);
+    p.v_ring = static_cast<uint16_t *>(v_ring);
+    p.ids = ring_ids;
+    p.context_lengths = context_lengths;
+    p.displaced = static_cast<uint16_t *>(const_cast<void *>(displaced));
+    p.dev_status = device_status_ptr();
+    p.num_ids = num_rings;
+    p.batch = batch;
+    p.k = proposal_count;
+    p.kv_heads = kv_heads;
+    p.head_dim = head_dim;
+    p.window = window;
+    p.elem_bytes = 1;
+    return launch_status(launch_ring_rollback(p, accepted, static_cast<cudaStream_t>(stream)));
+}
+
+carat_status carat_swa_attention_fp8(float *out, const void *queries, const void *k_ring,
+                                     const void *v_ring, int num_rings, const int32_t *ring_ids,
+                                     const void *displaced, const int32_t *context_lengths,
+                                     int proposal_count, int batch, int q_heads, int kv_heads,
+                                     int head_dim, int window, float scale, float k_scale,
+                                     float v_scale, void *workspace, size_t workspace_bytes,
+                                     void *stream) {
+    if (!attention_shape_ok(batch, proposal_count, q_heads, kv_heads, head_dim) || window < 1 ||
+        proposal_count > window || !std::isfinite(scale) || !fp8_scale_ok(k_scale) ||
+        !fp8_scale_ok(v_scale))
+        return CARAT_ERR_INVALID_ARG;
+    carat_status st = attention_unsupported(proposal_count, q_heads, kv_heads, head_dim);
+    if (st != CARAT_OK) return st;
+    const int group = q_heads / kv_heads;
+    if (!tc_fp8_supported(head_dim, group, proposal_count)) return CARAT_ERR_UNSUPPORTED;
+    if (batch == 0) return CARAT_OK;
+    st = check_attention_common(out, queries, k_ring, v_ring, num_rings, ring_ids, context_lengths,
+                                batch);
+    if (st != CARAT_OK) return st;
+    if (proposal_count > 1 && (!displaced || !aligned16(displaced))) return CARAT_ERR_INVALID_ARG;
+    const SplitPlan plan = tc_plan(batch, group, proposal_count, kv_heads, head_dim,
+                                   (window + kTcTileKeys - 1) / kTcTileKeys + 1, true);
+    if (plan.total > 0 && (!workspace || workspace_bytes < plan.total || !aligned16(workspace)))
+        return CARAT_ERR_WORKSPACE;
+
+    AttnParams p{};
+    p.q = static_cast<const uint16_t *>(queries);
+    p.k_base = static_cast<const uint16_t *>(k_ring);
+    p.v_base = static_cast<const uint16_t *>(v_ring);
+    p.ids = ring_ids;
+    p.displaced = proposal_count > 1 ? static_cast<const uint16_t *>(displaced) : nullptr;
+    p.context_lengths = context_lengths;
+    p.out = out;
+    set_split_fields(p, plan, workspace);
+    p.dev_status = device_status_ptr();
+    p.num_ids = num_rings;
+    p.batch = batch;
+    p.k = proposal_count;
+    p.q_heads = q_heads;
+    p.kv_heads = kv_heads;
+    p.head_dim = head_dim;
+    p.group = group;
+    p.rows = group * proposal_count;
+    p.window = window;
+    p.capacity = 0;
+    // dequantised K = e4m3 * k_scale: the K scale joins the softmax scale;
+    // dequantised V = e4m3 * v_scale: the V scale multiplies the output
+    p.scale_log2 = scale * k_scale * 1.4426950408889634f;
+    p.out_scale = v_scale;
+    p.source = KeySource::kRing;
+    return launch_status(launch_attention(p, plan, static_cast<cudaStream_t>(stream)));
 }
 
 carat_status carat_get_device_status(int32_t *host_out, int clear, void *stream) {

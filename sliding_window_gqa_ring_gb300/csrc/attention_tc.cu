@@ -82,11 +82,15 @@ constexpr int kDispBoxBytes = kDispRows * 128;
 constexpr int kThreads = 192;
 constexpr uint32_t kFull = 0xffffffffu;
 
-template <int D, int N, int NS>
+template <int D, int N, int NS, int NR = 0>
 struct Layout {
     static constexpr int KS = D / 128;                 // stages per K (or V) tile
     static constexpr int kQBlock = N * 128;            // one 64-d block of Q rows
-    static constexpr int kOffQ = NS * kStageBytes;
+    // FP8 caches (NR > 0): NR raw stages of e4m3 bytes (128 keys x 128 d) in
+    // front of the bf16 stages the tensor core reads.
+    static constexpr int kRawBytes = 128 * 128;
+    static constexpr int kOffRaw = NS * kStageBytes;
+    static constexpr int kOffQ = kOffRaw + NR * kRawBytes;
     static constexpr int kOffP = kOffQ + (D / 64) * kQBlock;
     static constexpr int kPBlock = N * 128;            // 64 keys of P rows
     static constexpr int kOffRed = kOffP + 2 * kPBlock;
@@ -94,7 +98,7 @@ struct Layout {
     // row maxima and sums kept for its deferred epilogue
     static constexpr int kRedFloats = 3 * 4 * N + 2 * N;
     static constexpr int kOffBar = kOffRed + kRedFloats * 4;
-    static constexpr int kNumBars = 2 * NS + 7;
+    static constexpr int kNumBars = 2 * NS + 7 + 2 * NR;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;   // SkShared
     static constexpr int kBytes = kOffMisc + 128;
     static constexpr int kAlloc = kBytes + 1024;       // base alignment slack
@@ -108,7 +112,8 @@ struct Layout {
     // The softmax warps zero masked V rows while all KS stages of a V tile are
     // resident, before the tile's PV product releases any of them.
     static_assert(NS >= KS, "the stage ring must hold a whole V tile");
-    static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kPBlock % 1024 == 0 &&
+    static_assert(kOffRaw % 1024 == 0 && kOffQ % 1024 == 0 && kOffP % 1024 == 0 &&
+                      kPBlock % 1024 == 0 &&
                       kQBlock % 1024 == 0,
                   "operand blocks must be 1024-byte aligned for the 128-byte swizzle");
     // The merge at the end stages (max, sum) pairs, weights and at least one
@@ -372,6 +377,47 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(pending) : "memory");
 }
 
+// Two e4m3 values (low 16 bits of `two`, first value in the low byte) -> two
+// bf16 values (first in the low half).  Exact: e4m3 -> f16 -> f32 -> bf16
+// never rounds, as every e4m3 value is an f16 and a bf16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two));
+    float lo, hi;
+    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\t"
+        "cvt.f32.f16 %1, b;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h2));
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// 16 e4m3 bytes -> 16 bf16 values (two 16-byte chunks, in order).
+__device__ __forceinline__ void e4m3x16_to_bf16(uint4 v, uint4 &o0, uint4 &o1) {
+    o0 = make_uint4(e4m3x2_to_bf16x2(v.x), e4m3x2_to_bf16x2(v.x >> 16), e4m3x2_to_bf16x2(v.y),
+                    e4m3x2_to_bf16x2(v.y >> 16));
+    o1 = make_uint4(e4m3x2_to_bf16x2(v.z), e4m3x2_to_bf16x2(v.z >> 16), e4m3x2_to_bf16x2(v.w),
+                    e4m3x2_to_bf16x2(v.w >> 16));
+}
+
+// One 128-byte row of e4m3 (a 128-d block, 128-byte swizzle at row `row`)
+// -> its bf16 image: 16-byte chunk c' of 64-d slab (c / 4) of the
+// destination, each slab a 128-byte swizzled row; zero: write zeros.
+__device__ __forceinline__ void convert_row(const uint8_t *src, uint8_t *dst0, uint8_t *dst1,
+                                            int row, bool zero) {
+    const int sw = row & 7;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
+        if (!zero) e4m3x16_to_bf16(*reinterpret_cast<const uint4 *>(src + ((c ^ sw) << 4)), o0, o1);
+        uint8_t *d = (c < 4) ? dst0 : dst1;
+        const int cc = 2 * (c & 3);
+        *reinterpret_cast<uint4 *>(d + ((cc ^ sw) << 4)) = o0;
+        *reinterpret_cast<uint4 *>(d + (((cc + 1) ^ sw) << 4)) = o1;
+    }
+}
+
 // Barrier over the 128 softmax threads that also ORs a predicate across them,
 // so every thread takes the same abort decision.
 __device__ __forceinline__ bool named_bar_softmax_any(bool pred) {
@@ -450,11 +496,15 @@ struct KeyInfo {
 
 }  // namespace
 
-template <int D, int N, int NS, int MINB>
+template <int D, int N, int NS, int MINB, int NR = 0>
 __global__ void __launch_bounds__(kThreads, MINB)
     attn_tc_kernel(const AttnParams p, const TcPlan plan, const __grid_constant__ TcMaps maps) {
-    using L = Layout<D, N, NS>;
+    using L = Layout<D, N, NS, NR>;
     constexpr int KS = L::KS;
+    // FP8 caches: the producer fills raw e4m3 stages, the softmax warps
+    // convert each into a bf16 stage (exactly: every e4m3 value is a bf16
+    // value), and the tensor core reads the bf16 stages as for a bf16 cache.
+    constexpr bool F8 = NR > 0;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int upr = p.kv_heads * plan.row_groups;   // units per request
     const bool ring = p.source == KeySource::kRing;
@@ -472,6 +522,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
     uint64_t *q_full = s_full + 4;
     uint64_t *q_empty = s_full + 5;
     uint64_t *fin = s_full + 6;
+    uint64_t *raw_full = s_full + 7;     // [NR] FP8: e4m3 stage landed
+    uint64_t *raw_empty = raw_full + NR; // [NR] FP8: e4m3 stage converted
+    uint8_t *s_raw = smem + L::kOffRaw;
     SkShared *sk = reinterpret_cast<SkShared *>(smem + L::kOffMisc);
     volatile int *abort_flag = &sk->abort_flag;
     float *red = reinterpret_cast<float *>(smem + L::kOffRed);
@@ -564,6 +617,44 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 }
                 continue;
             }
+            if constexpr (F8) {
+                // raw e4m3 stage; its slot is free once converted
+                const int r = cnt % NR;
+                if (cnt >= NR && !wait_or_abort(&raw_empty[r], ((cnt / NR) & 1) ^ 1, abort_flag,
+                                                p.dev_status)) {
+                    alive_p = false;
+                    break;
+                }
+                uint8_t *rdst = s_raw + r * L::kRawBytes;
+                if (special) {
+                    // displaced rows: 16 rows x D bytes of K, then of V
+                    tc::mbar_arrive_expect_tx(&raw_full[r], 2 * (D / 128) * kDispRows * 128);
+                    tc::tma_load_5d(rdst, &maps.disp, 0, ps.b * (p.k - 1), 0, 0, ps.c, &raw_full[r],
+                                    pol);
+                    tc::tma_load_5d(rdst + (D / 128) * kDispRows * 128, &maps.disp, 0,
+                                    ps.b * (p.k - 1), 0, 1, ps.c, &raw_full[r], pol);
+                    ++cnt;
+                    if (++ppart == 2 * n) {
+                        p_have = false;
+                        ++psi;
+                    }
+                    continue;
+                }
+                const long long row = ring ? (long long)ps.id * p.window + (long long)i * kTileKeys
+                                           : (long long)ps.id * p.capacity + (long long)i * kTileKeys;
+                tc::mbar_arrive_expect_tx(&raw_full[r], L::kRawBytes);
+                tc::tma_load_4d(rdst, is_v ? &maps.v : &maps.k, 0, (int)row, pks, ps.c, &raw_full[r],
+                                pol);
+                ++cnt;
+                if (++pks == KS) {
+                    pks = 0;
+                    if (++ppart == 2 * n) {
+                        p_have = false;
+                        ++psi;
+                    }
+                }
+                continue;
+            }
             const int s = cnt % NS;
             if (cnt >= NS &&
                 !wait_or_abort(&empty[s], ((cnt / NS) & 1) ^ 1, abort_flag, p.dev_status)) {
@@ -636,8 +727,14 @@ __global__ void __launch_bounds__(kThreads, MINB)
             tc::tma_prefetch_map(p.fused ? &maps.knew : &maps.disp);
             if (p.fused) tc::tma_prefetch_map(&maps.vnew);
             for (int i = 0; i < NS; ++i) {
-                tc::mbar_init(&full[i], 1);
+                // bf16 stage filled by TMA (one arrival with its bytes), or
+                // with FP8 caches by the 128 converting threads
+                tc::mbar_init(&full[i], F8 ? 128 : 1);
                 tc::mbar_init(&empty[i], 1);
+            }
+            for (int i = 0; i < NR; ++i) {
+                tc::mbar_init(&raw_full[i], 1);
+                tc::mbar_init(&raw_empty[i], 128);
             }
             tc::mbar_init(&s_full[0], 1);
             tc::mbar_init(&s_full[1], 1);
@@ -658,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
             // Start streaming before the block-wide barrier: this thread made
             // the barriers, and the first NS stages need no release.
             pit.init(p, sk);
-            produce(NS, true);
+            produce(F8 ? NR : NS, true);
         }
     } else if (warp == 1) {
         tc::tmem_alloc(&sk->tmem_slot, L::kTmemCols);
@@ -693,8 +790,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
             produce(0xffffffffu, false);
             if (!alive_p) {
                 // Wait (bounded) for the copies already issued before leaving.
-                for (uint32_t x = cnt > (uint32_t)NS ? cnt - NS : 0; x < cnt; ++x)
-                    tc::mbar_wait(&full[x % NS], (x / NS) & 1, 100000000ull);
+                if constexpr (F8) {
+                    for (uint32_t x = cnt > (uint32_t)NR ? cnt - NR : 0; x < cnt; ++x)
+                        tc::mbar_wait(&raw_full[x % NR], (x / NR) & 1, 100000000ull);
+                } else {
+                    for (uint32_t x = cnt > (uint32_t)NS ? cnt - NS : 0; x < cnt; ++x)
+                        tc::mbar_wait(&full[x % NS], (x / NS) & 1, 100000000ull);
+                }
             }
         }
     } else if (warp == 1) {
@@ -855,6 +957,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         bool alive = true;
         uint32_t gt = 0, cnt_base = 0;       // tiles and stages before this segment
         int si = 0;                          // segments before this one
+        uint32_t ccnt = 0;                   // FP8: stages converted so far
         float *s_mrow = red + 12 * N;        // a finished segment's row maxima
         float *s_lrow = red + 13 * N;        // and row sums
         // The epilogue of a finished segment, run once the next segment's first
@@ -873,7 +976,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 // Row r = j * group + h' goes to out[b][j][c * group + h'].
                 float inv_l[N];
 #pragma unroll
-                for (int r = 0; r < N; ++r) inv_l[r] = 1.f / s_lrow[r];
+                for (int r = 0; r < N; ++r) inv_l[r] = p.out_scale / s_lrow[r];
 #pragma unroll
                 for (int ob = 0; ob < KS; ++ob) {
                     float *obase = p.out +
@@ -930,7 +1033,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
                         for (int e = 0; e < 16; ++e) {
                             const int r = (cb + h) * 16 + e;
                             if (r < pe.rows_here)
-                                p.part_o[(base + r) * D + ob * 128 + t] = __uint_as_float(r16[h][e]);
+                                p.part_o[(base + r) * D + ob * 128 + t] =
+                                    __uint_as_float(r16[h][e]) * p.out_scale;
                         }
                     }
                 }
@@ -993,6 +1097,73 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 }
                 return st;
             };
+            // FP8: convert the segment's raw stages, in load order, until
+            // `target` stages are done.  Thread t converts key row t (rows
+            // t < 16 of a special tile); V rows of keys that hold no token
+            // (zero_v) are written as zeros.  Returns false on a timeout.
+            int cv_part = 0, cv_pks = 0;
+            auto convert_through = [&](uint32_t target, bool zero_v) -> bool {
+                if constexpr (F8) {
+                    while (ccnt < target) {
+                        int x;
+                        bool is_v;
+                        if (cv_part == 0) {
+                            x = 0;
+                            is_v = false;
+                        } else if (cv_part == 2 * n - 1) {
+                            x = n - 1;
+                            is_v = true;
+                        } else {
+                            x = (cv_part - 1) / 2 + ((cv_part - 1) % 2 == 0 ? 1 : 0);
+                            is_v = (cv_part - 1) % 2 == 1;
+                        }
+                        const bool special = order_tile(sg, sg.x0 + x) == sg.special;
+                        if (special && is_v) {
+                            ++cv_part;
+                            continue;
+                        }
+                        const int sidx = ccnt % NS, r = ccnt % NR;
+                        if (ccnt >= NS && !wait_or_abort(&empty[sidx], ((ccnt / NS) & 1) ^ 1,
+                                                         abort_flag, p.dev_status))
+                            return false;
+                        if (!wait_or_abort(&raw_full[r], (ccnt / NR) & 1, abort_flag, p.dev_status))
+                            return false;
+                        const uint8_t *raw = s_raw + r * L::kRawBytes;
+                        uint8_t *stg = smem + sidx * kStageBytes;
+                        if (special) {
+                            // 16 displaced rows: K slabs then V slabs (2 KB each)
+                            if (t < kDispRows) {
+                                const long long pos = ctx - p.window + 1 + t;
+                                const bool valid = t < p.k - 1 && pos >= 0;
+#pragma unroll
+                                for (int sl = 0; sl < D / 128; ++sl) {
+                                    convert_row(raw + sl * 2048 + t * 128,
+                                                stg + (2 * sl) * kDispBoxBytes + t * 128,
+                                                stg + (2 * sl + 1) * kDispBoxBytes + t * 128, t,
+                                                false);
+                                    convert_row(raw + (D / 128 + sl) * 2048 + t * 128,
+                                                stg + (D / 64 + 2 * sl) * kDispBoxBytes + t * 128,
+                                                stg + (D / 64 + 2 * sl + 1) * kDispBoxBytes + t * 128,
+                                                t, !valid);
+                                }
+                            }
+                            ++cv_part;
+                        } else {
+                            convert_row(raw + t * 128, stg + t * 128, stg + kBoxBytes + t * 128, t,
+                                        is_v && zero_v);
+                            if (++cv_pks == KS) {
+                                cv_pks = 0;
+                                ++cv_part;
+                            }
+                        }
+                        tc::fence_proxy_async_smem();
+                        tc::mbar_arrive(&raw_empty[r]);
+                        tc::mbar_arrive(&full[sidx]);
+                        ++ccnt;
+                    }
+                }
+                return true;
+            };
             float m_run[N], l_part[N];
 #pragma unroll
             for (int r = 0; r < N; ++r) {
@@ -1003,9 +1174,18 @@ __global__ void __launch_bounds__(kThreads, MINB)
             for (; idx < n; ++idx) {
                 const uint32_t tile = gt + idx;
                 const int i = order_tile(sg, sg.x0 + idx);
+                if constexpr (F8) {
+                    // K of this tile and the next, before their QK products
+                    const int xk = idx + 1 < n ? idx + 1 : idx;
+                    if (!convert_through(cnt_base + stages_before((xk == 0 ? 0 : 2 * xk - 1) + 1),
+                                         false))
+                        alive = false;
+                }
                 // warp-uniform: the TMEM load below is warp-collective
-                const bool w_ok = __all_sync(kFull, wait_or_abort(&s_full[tile & 1], (tile >> 1) & 1,
-                                                                  abort_flag, p.dev_status));
+                const bool w_ok = __all_sync(kFull, alive && wait_or_abort(&s_full[tile & 1],
+                                                                           (tile >> 1) & 1,
+                                                                           abort_flag,
+                                                                           p.dev_status));
                 const uint32_t tmem_s = tmem + (tile & 1) * N;
                 float x[N];
                 if (w_ok) {
@@ -1149,7 +1329,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
                             tile_writes |= sj / kTileKeys == i;
                         }
                     }
-                    if (idx == xs) {
+                    if constexpr (F8) {
+                        // V of this tile, its no-token rows as zeros
+                        if (!convert_through(cnt_base + stages_before(v_part(idx, n) + 1),
+                                             tile_partial && !ki.data))
+                            alive = false;
+                    } else if (idx == xs) {
                         // The special tile's stage: zero its V rows that hold no
                         // token (only the 16 rows its PV product reads).
                         const uint32_t x_cnt =
@@ -1446,12 +1631,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
 
 namespace {
 
-template <int D, int N, int NS, int MINB>
+template <int D, int N, int NS, int MINB, int NR = 0>
 cudaError_t launch_tc(const AttnParams &p, const TcPlan &plan, const TcMaps &maps, int grid,
                       cudaStream_t stream) {
-    using L = Layout<D, N, NS>;
+    using L = Layout<D, N, NS, NR>;
     static_assert(MINB == 1 || 2 * (L::kAlloc + 1024) <= 233472, "two CTAs must fit one SM");
-    auto kernel = attn_tc_kernel<D, N, NS, MINB>;
+    auto kernel = attn_tc_kernel<D, N, NS, MINB, NR>;
     static int configured_devices[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1475,8 +1660,12 @@ int tc_rows_per_tile(int group, int k) {
     return 64;
 }
 
-int tc_ctas_per_sm(int head_dim, int rows_per_tile) {
-    return (head_dim == 256 && rows_per_tile == 16) ? 2 : 1;
+int tc_ctas_per_sm(int head_dim, int rows_per_tile, bool fp8) {
+    return (!fp8 && head_dim == 256 && rows_per_tile == 16) ? 2 : 1;
+}
+
+bool tc_fp8_supported(int head_dim, int group, int k) {
+    return head_dim == 256 && tc_supported(head_dim, group, k);
 }
 
 bool tc_supported(int head_dim, int group, int k) {
@@ -1492,7 +1681,7 @@ int tc_units_per_request(int group, int k, int kv_heads) {
     return kv_heads * ((k + ppg - 1) / ppg);
 }
 
-cudaError_t launch_attention_tc(const AttnParams &p, int grid, bool unit_mode,
+cudaError_t launch_attention_tc(const AttnParams &p, int grid, bool unit_mode, bool fp8,
                                 cudaStream_t stream) {
     const int n = tc_rows_per_tile(p.group, p.k);
     TcPlan plan{};
@@ -1503,6 +1692,42 @@ cudaError_t launch_attention_tc(const AttnParams &p, int grid, bool unit_mode,
 
     TcMaps maps{};
     const uint64_t D = (uint64_t)p.head_dim;
+    if (fp8) {
+        // e4m3 rings: (128 d bytes, rows, 128-d block, head); a box is one raw
+        // stage of 128 rows x 128 d, or 16 displaced rows x every block.
+        if (p.head_dim != 256 || p.source != KeySource::kRing || p.fused)
+            return cudaErrorNotSupported;
+        const uint64_t row8 = (uint64_t)p.kv_heads * D;
+        const uint64_t rows_total = (uint64_t)p.num_ids * (uint64_t)p.window;
+        const uint64_t dims_kv[4] = {128, rows_total, D / 128, (uint64_t)p.kv_heads};
+        const uint64_t strides_kv[3] = {row8, 128, D};
+        const uint32_t box_kv[4] = {128, (uint32_t)kTileKeys, 1, 1};
+        if (!make_u8_tensor_map(&maps.k, p.k_base, 4, dims_kv, strides_kv, box_kv, true) ||
+            !make_u8_tensor_map(&maps.v, p.v_base, 4, dims_kv, strides_kv, box_kv, true))
+            return cudaErrorInvalidValue;
+        if (p.k > 1) {
+            const uint64_t dims5[5] = {128, (uint64_t)p.batch * (p.k - 1), D / 128, 2,
+                                       (uint64_t)p.kv_heads};
+            const uint64_t strides5[4] = {2 * row8, 128, row8, D};
+            const uint32_t box5[5] = {128, (uint32_t)kDispRows, (uint32_t)(D / 128), 1, 1};
+            if (!make_u8_tensor_map(&maps.disp, p.displaced, 5, dims5, strides5, box5, true))
+                return cudaErrorInvalidValue;
+        } else {
+            maps.disp = maps.k;
+        }
+        maps.knew = maps.k;
+        maps.vnew = maps.v;
+        const uint64_t dimsq[4] = {D, (uint64_t)p.q_heads, (uint64_t)p.k, (uint64_t)p.batch};
+        const uint64_t stridesq[3] = {D * 2, (uint64_t)p.q_heads * D * 2,
+                                      (uint64_t)p.k * p.q_heads * D * 2};
+        const uint32_t boxq[4] = {64, (uint32_t)p.group, (uint32_t)plan.pos_per_group, 1};
+        if (!make_bf16_tensor_map(&maps.q, p.q, 4, dimsq, stridesq, boxq, true))
+            return cudaErrorInvalidValue;
+        // one CTA per SM: 3 bf16 stages and 6 (or 4) raw stages in flight
+        if (n == 16) return launch_tc<256, 16, 3, 1, 6>(p, plan, maps, grid, stream);
+        if (n == 32) return launch_tc<256, 32, 3, 1, 6>(p, plan, maps, grid, stream);
+        return launch_tc<256, 64, 3, 1, 4>(p, plan, maps, grid, stream);
+    }
     const uint64_t row_bytes = (uint64_t)p.kv_heads * D * 2;
     const uint64_t slabs = D / 64;
     const uint64_t rows_total =

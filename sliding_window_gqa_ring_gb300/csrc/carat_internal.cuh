@@ -61,12 +61,13 @@ struct AttnParams {
     int max_pages;
     int page_rows;
     int num_pages;
-    float scale_log2;           // softmax scale * log2(e)
+    float scale_log2;           // softmax scale * log2(e) (FP8: times the K scale)
+    float out_scale = 1.f;      // FP8: the V scale, applied to the output
     KeySource source;
 };
 
 struct AppendParams {
-    uint16_t *k_ring, *v_ring;
+    uint16_t *k_ring, *v_ring;        // bf16 rows, or (elem_bytes 1) e4m3 bytes
     const int32_t *ids;
     const uint16_t *k_new, *v_new;
     const int32_t *context_lengths;
@@ -76,6 +77,10 @@ struct AppendParams {
     // Paged caches: rows go through the page table instead of a ring.
     const int32_t *page_table;
     int max_pages, page_rows, num_pages;
+    // FP8 rings: 1-byte elements; new rows are quantised as
+    // e4m3_rn(fp32(x * k_inv)) (k_inv = fp32(1 / k_scale)), likewise for V.
+    int elem_bytes = 2;               // 2 (bf16) or 1 (e4m3)
+    float k_inv = 1.f, v_inv = 1.f;
 };
 
 // ---------------------------------------------------------------------------
@@ -193,6 +198,7 @@ void count_launches(int n);
 // Host-side launchers (defined in the .cu files)
 // ---------------------------------------------------------------------------
 cudaError_t launch_ring_append(const AppendParams &p, cudaStream_t stream);
+cudaError_t launch_ring_append_fp8(const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_ring_rollback(const AppendParams &p, const int32_t *accepted,
                                  cudaStream_t stream);
 cudaError_t launch_attention_simt(const AttnParams &p, cudaStream_t stream);
@@ -205,10 +211,11 @@ cudaError_t launch_combine(const AttnParams &p, cudaStream_t stream);
 // units) or the persistent stream-K schedule (grid = resident slots).
 constexpr int kTcTileKeys = 128;
 int tc_rows_per_tile(int group, int k);
-int tc_ctas_per_sm(int head_dim, int rows_per_tile);
+int tc_ctas_per_sm(int head_dim, int rows_per_tile, bool fp8);
 bool tc_supported(int head_dim, int group, int k);
+bool tc_fp8_supported(int head_dim, int group, int k);   // FP8 e4m3 rings
 int tc_units_per_request(int group, int k, int kv_heads);
-cudaError_t launch_attention_tc(const AttnParams &p, int grid, bool unit_mode,
+cudaError_t launch_attention_tc(const AttnParams &p, int grid, bool unit_mode, bool fp8,
                                 cudaStream_t stream);
 
 }  // namespace carat

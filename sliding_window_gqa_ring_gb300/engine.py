@@ -105,6 +105,69 @@ class SlidingLayer:
         return out
 
 
+class Fp8SlidingLayer:
+    """K/V rings of one sliding-window layer stored as FP8 e4m3 ("Announcing
+    Carat ...", section "Server": the KV cache is FP8 e4m3 and lossy), one
+    dequantisation scale per tensor.  New rows arrive in bf16 and are
+    quantised by carat_ring_append_fp8; attention reads the e4m3 rings and
+    widens them on chip.  step() is append then attention (two launches)."""
+
+    def __init__(self, num_rings: int, *, k_scale: float, v_scale: float, window: int = 1024,
+                 q_heads: int = 16, kv_heads: int = 8, head_dim: int = 256,
+                 max_batch: int | None = None, max_proposals: int = 1,
+                 scale: float | None = None, device="cuda", fill: int | None = 0):
+        self.window, self.q_heads, self.kv_heads, self.head_dim = window, q_heads, kv_heads, head_dim
+        self.k_scale, self.v_scale = float(k_scale), float(v_scale)
+        self.max_batch = max_batch or num_rings
+        self.max_proposals = max_proposals
+        self.scale = (1.0 / math.sqrt(head_dim)) if scale is None else scale
+        self.device = torch.device(device)
+        shape = (num_rings, window, kv_heads, head_dim)
+        self.k_ring = torch.empty(shape, dtype=torch.uint8, device=self.device)
+        self.v_ring = torch.empty(shape, dtype=torch.uint8, device=self.device)
+        if fill is not None:
+            self.k_ring.fill_(fill)
+            self.v_ring.fill_(fill)
+        self.displaced = torch.zeros((self.max_batch, max(max_proposals - 1, 1), 2, kv_heads,
+                                      head_dim), dtype=torch.uint8, device=self.device)
+        self.ring_ids = None
+        # the FP8 call needs no more than the bf16 call's workspace
+        self.workspace = carat.workspace_tensor(
+            max(carat.swa_workspace_bytes(self.max_batch, p, q_heads, kv_heads, head_dim, window)
+                for p in range(1, max_proposals + 1)), self.device)
+
+    def append(self, k_new, v_new, context_lengths, ring_ids=None, save_displaced=True,
+               stream=None):
+        ring_ids = self.ring_ids if ring_ids is None else ring_ids
+        disp = self.displaced if (save_displaced and k_new.shape[1] > 1) else None
+        carat.carat_ring_append_fp8(self.k_ring, self.v_ring, k_new, v_new, context_lengths,
+                                    k_scale=self.k_scale, v_scale=self.v_scale, ring_ids=ring_ids,
+                                    displaced=disp, window=self.window, stream=stream)
+
+    def attend(self, queries, context_lengths, ring_ids=None, out=None, stream=None):
+        ring_ids = self.ring_ids if ring_ids is None else ring_ids
+        if out is None:
+            out = torch.empty(queries.shape, dtype=torch.float32, device=self.device)
+        carat.carat_swa_attention_fp8(out, queries, self.k_ring, self.v_ring, context_lengths,
+                                      scale=self.scale, k_scale=self.k_scale,
+                                      v_scale=self.v_scale, workspace=self.workspace,
+                                      ring_ids=ring_ids, displaced=self.displaced, stream=stream)
+        return out
+
+    def rollback(self, context_lengths, accepted, proposal_count, ring_ids=None, stream=None):
+        ring_ids = self.ring_ids if ring_ids is None else ring_ids
+        carat.carat_ring_rollback_fp8(self.k_ring, self.v_ring, self.displaced, context_lengths,
+                                      accepted, proposal_count, ring_ids=ring_ids,
+                                      window=self.window, stream=stream)
+
+    def step(self, queries, k_new, v_new, context_lengths, ring_ids=None, out=None, stream=None,
+             fused=False):
+        if fused:
+            raise ValueError("FP8 rings: append and attention are separate launches")
+        self.append(k_new, v_new, context_lengths, ring_ids=ring_ids, stream=stream)
+        return self.attend(queries, context_lengths, ring_ids=ring_ids, out=out, stream=stream)
+
+
 class SharedPool:
     """One K pool and one V pool of `num_pages` pages of `page_bytes` each,
     shared by the rings of sliding layers and the pages of global layers
