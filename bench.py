@@ -69,6 +69,16 @@ def sliding_call_bytes(w, b):
     return attn, fused_writes, append
 
 
+def fp8_attention_bytes(w, b):
+    """Algorithmic bytes of FP8 sliding attention for request b: the window's
+    e4m3 K and V rows (1 byte per element), bf16 queries, fp32 outputs."""
+    k, hkv, d, hq = w.proposal_count, w.kv_heads, w.head_dim, w.q_heads
+    kc = int(w.key_counts[b])
+    ctx = kc - k
+    keys = kc - max(0, ctx - w.window + 1)
+    return keys * hkv * d * 2 + k * hq * d * 2 + k * hq * d * 4
+
+
 def global_call_bytes(w, b):
     k, hkv, d, hq = w.proposal_count, w.kv_heads, w.head_dim, w.q_heads
     kc = int(w.key_counts[b])
@@ -279,7 +289,8 @@ def run_carat(args, world, rank, local):
                                   kv_heads=sliding.kv_heads, head_dim=sliding.head_dim,
                                   max_proposals=k, scale=sliding.scale, device=dev)
         inp = engine.stage_sliding(sliding, li, lay)
-        inp.host["hist"] = {}
+        if li > 0 or not args.fp8:
+            inp.host["hist"] = {}          # layer 0's history sizes the FP8 scales
         layers.append((lay, inp))
     glay = engine.GlobalLayer(B, capacity=glob.capacity, q_heads=glob.q_heads,
                               kv_heads=glob.kv_heads, head_dim=glob.head_dim, max_proposals=k,
@@ -460,6 +471,48 @@ def run_carat(args, world, rank, local):
                   "layout": "5 x 64 rings of 8 pages + paged global caches, one K and one V pool"}
         del pstep, p_layers, p_inputs, spool
 
+    # --- FP8 (e4m3) rings for one sliding layer of the same step ("Announcing
+    # Carat ...", section "Server": the KV cache is FP8 e4m3): append + attention
+    # and attention alone, per call; per-tensor scales max|x| / 448 of the layer
+    fp8 = None
+    if args.fp8:
+        hist = layers[0][1].host["hist"]
+        kmax = max(float(np.abs(synth.bf16_to_float(hist[b][1])).max()) for b in range(B))
+        vmax = max(float(np.abs(synth.bf16_to_float(hist[b][2])).max()) for b in range(B))
+        layers[0][1].host["hist"] = {}
+        f8 = engine.Fp8SlidingLayer(B, k_scale=kmax / 448.0, v_scale=vmax / 448.0,
+                                    window=sliding.window, q_heads=sliding.q_heads,
+                                    kv_heads=sliding.kv_heads, head_dim=sliding.head_dim,
+                                    max_proposals=k, scale=sliding.scale, device=dev)
+        f8in = engine.stage_sliding(sliding, 0, f8)
+        f8out = torch.empty(f8in.queries.shape, dtype=torch.float32, device=dev)
+
+        def f8_time(fn, reps):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) * 1e3 / reps
+
+        reps = max(3, min(nrep, 300))
+        f8.append(f8in.k_new, f8in.v_new, f8in.context_lengths)
+        att_us = f8_time(lambda: f8.attend(f8in.queries, f8in.context_lengths, out=f8out), reps)
+        both_us = f8_time(lambda: (f8.append(f8in.k_new, f8in.v_new, f8in.context_lengths),
+                                   f8.attend(f8in.queries, f8in.context_lengths, out=f8out)), reps)
+        att_bytes = sum(fp8_attention_bytes(sliding, b) for b in range(B))
+        fp8 = {"attention_us": round(att_us, 3),
+               "attention_gb_s": round(att_bytes / (att_us * 1e3), 1),
+               "attention_bytes": att_bytes,
+               "append_plus_attention_us": round(both_us, 3),
+               "bf16_fused_call_us": per_call["swa_call"]["us"],
+               "scales": {"k": kmax / 448.0, "v": vmax / 448.0},
+               "layer": "sliding layer 0 of the step: e4m3 rings, bf16 queries, fp32 out"}
+        del f8, f8in, f8out
+
     # --- the step replayed from a CUDA graph (one host launch per step)
     dstep.capture()
     for _ in range(3):
@@ -524,6 +577,7 @@ def run_carat(args, world, rank, local):
         "separate_calls": separate,
         "cuda_graph": graph,
         "shared_pool": pooled,
+        "fp8_sliding": fp8,
         "cpu_baseline": cpu_baseline,
         "parity_sample": parity,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -595,6 +649,8 @@ def main():
     ap.add_argument("--sample-requests", type=int, default=16,
                     help="requests the oracle recomputes for the CPU baseline / parity sample")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-fp8", dest="fp8", action="store_false",
+                    help="skip the FP8 (e4m3) sliding-layer measurement")
     ap.add_argument("--no-shared-pool", dest="shared_pool", action="store_false",
                     help="skip timing the step with all caches in one shared pool")
     args = ap.parse_args()

@@ -379,7 +379,8 @@ __device__ __forceinline__ void cp_async_wait() {
 
 // Two e4m3 values (low 16 bits of `two`, first value in the low byte) -> two
 // bf16 values (first in the low half).  Exact: e4m3 -> f16 -> f32 -> bf16
-// never rounds, as every e4m3 value is an f16 and a bf16 value.
+// never rounds, as every e4m3 value is an f16 and a bf16 value.  (An integer
+// rebias of the f16 bits measured slower than the two conversions it saves.)
 __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
     uint32_t h2;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two));
