@@ -4,11 +4,9 @@
 // sizes the caller's workspace, and the launches.  The kernels live in
 // ring_append.cu and attention_*.cu.
 #include <atomic>
-#include <chrono>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
-#include <random>
 
 #include "carat_internal.cuh"
 
@@ -52,7 +50,7 @@ struct SplitPlan {
     int nchunks = 0;           // CUDA-core path: splits per (request, KV head)
     size_t ml_bytes = 0;
     size_t o_bytes = 0;
-    size_t ticket_bytes = 0;
+    size_t unit_bytes = 0;
     size_t total = 0;
 };
 
@@ -107,7 +105,8 @@ SplitPlan simt_plan(long long pairs, long long keys, int rows, int head_dim) {
 // resident CTA slot and are all short (at most 16 tiles of 128 keys) run one
 // CTA each.  Otherwise one CTA per resident slot runs the stream-K schedule;
 // each keeps two partial slots (the first and last segment of its range), and
-// each unit a ticket.  The workspace is sized for stream-K either way.
+// each unit a 16-byte entry for the merge launch.  The workspace is sized for
+// stream-K either way.
 SplitPlan tc_plan(int batch, int group, int k, int kv_heads, int head_dim, long long max_tiles,
                   bool fp8 = false) {
     SplitPlan p;
@@ -121,21 +120,9 @@ SplitPlan tc_plan(int batch, int group, int k, int kv_heads, int head_dim, long 
     const size_t slots = (size_t)slots_total * 2 * n;
     p.ml_bytes = align256(slots * sizeof(float2));
     p.o_bytes = align256(slots * (size_t)head_dim * sizeof(float));
-    p.ticket_bytes =
-        align256((size_t)batch * tc_units_per_request(group, k, kv_heads) * sizeof(uint64_t));
-    p.total = p.ml_bytes + p.o_bytes + p.ticket_bytes;
+    p.unit_bytes = align256((size_t)batch * tc_units_per_request(group, k, kv_heads) * 16);
+    p.total = p.ml_bytes + p.o_bytes + p.unit_bytes;
     return p;
-}
-
-// Ticket tags: a random 48-bit start, one more per launch, so a ticket left by
-// another call (an aborted one, or another workspace's user) never matches.
-uint64_t next_epoch() {
-    static std::atomic<uint64_t> epoch{[] {
-        std::random_device rd;
-        const uint64_t t = (uint64_t)std::chrono::steady_clock::now().time_since_epoch().count();
-        return ((uint64_t)rd() << 20) ^ t;
-    }()};
-    return epoch.fetch_add(1, std::memory_order_relaxed) & ((1ull << 48) - 1);
 }
 
 // Point the call's parameters at its workspace.
@@ -143,10 +130,8 @@ void set_split_fields(AttnParams &p, const SplitPlan &plan, void *workspace) {
     char *w = static_cast<char *>(workspace);
     p.part_ml = reinterpret_cast<float2 *>(w);
     p.part_o = w ? reinterpret_cast<float *>(w + plan.ml_bytes) : nullptr;
-    p.tickets = (plan.tc && w)
-                    ? reinterpret_cast<unsigned long long *>(w + plan.ml_bytes + plan.o_bytes)
-                    : nullptr;
-    p.epoch = plan.tc ? next_epoch() : 0;
+    p.units = (plan.tc && w) ? reinterpret_cast<int4 *>(w + plan.ml_bytes + plan.o_bytes)
+                             : nullptr;
     p.chunk = plan.chunk;
     p.nchunks = plan.nchunks;
 }

@@ -36,8 +36,10 @@
 // one stage ring without a break between segments.  A segment that covers a
 // whole unit writes the normalised output; the at most two others (the
 // range's first and last) write a partial (row max, row sum, unnormalised O)
-// to the workspace and take a ticket on their unit, and the CTA that brings
-// the unit's last piece merges them all after its own range is done.  The
+// to the workspace, and the CTA holding a unit's first tile records in a unit
+// table whether the unit was split.  A second launch (attn_fixup_kernel, one
+// CTA per (unit, 4 rows), started early by programmatic dependent launch and
+// waiting for this grid) merges the split units' pieces in parallel.  The
 // range is never shorter than 1/(kMaxPieces - 1) of the longest unit, so no
 // unit is cut into more than kMaxPieces pieces.  The CTAs never wait for one
 // another.
@@ -55,8 +57,7 @@
 //               with a warp transpose-reduction and shared memory, updates the
 //               running max / sum (log2 domain), writes P, rescales O^T in
 //               TMEM when a row's maximum moved; per segment they write the
-//               output or the partial, and at the end merge the units whose
-//               last piece this CTA brought.
+//               output or the partial.
 //
 // Every wait is bounded (mbar_wait): on a timeout the CTA records
 // CARAT_DEV_TIMEOUT, stops issuing work, waits (bounded) for its own copies
@@ -77,7 +78,7 @@ constexpr int kTileKeys = 128;
 constexpr int kBoxBytes = 128 * 128;        // [128 keys][64 bf16]
 constexpr int kStageBytes = 2 * kBoxBytes;  // 128 keys x 128 d
 constexpr int kDispRows = 16;               // displaced rows loaded per tile (>= k - 1)
-constexpr int kMaxPieces = 16;              // CTAs one unit may be split across
+constexpr int kMaxPieces = 64;              // CTAs one unit may be split across
 constexpr int kDispBoxBytes = kDispRows * 128;
 constexpr int kThreads = 192;
 constexpr uint32_t kFull = 0xffffffffu;
@@ -116,10 +117,6 @@ struct Layout {
                       kPBlock % 1024 == 0 &&
                       kQBlock % 1024 == 0,
                   "operand blocks must be 1024-byte aligned for the 128-byte swizzle");
-    // The merge at the end stages (max, sum) pairs, weights and at least one
-    // row of every piece in the idle stage ring.
-    static_assert(kMaxPieces * N * 12 + 2 * kMaxPieces * D * 4 <= NS * kStageBytes,
-                  "merge buffers must fit the stages");
 };
 
 // K/V tensors are mapped with the head dimension cut into 64-element slabs
@@ -142,18 +139,14 @@ struct TcPlan {
 };
 
 // Per-CTA schedule, written by warp 0 before the block-wide barrier and read
-// by every role; plus the merges this CTA owes.
+// by every role.
 struct SkShared {
     uint32_t tmem_slot;
     int abort_flag;
-    int nduty;                 // units this CTA merges at the end (<= 2)
-    int b0, ur0, off0;         // first segment: request, unit within it, order offset
-    int duty_unit[2];
-    int duty_tiles[2];
+    int b0, ur0, off0;            // first segment: request, unit within it, order offset
     int id0, ntiles0, special0;   // first request's id, tiles and special tile
     long long ctx0;               // first request's context length
-    long long s, e, len;       // tile range [s, e) of the flattened order; range length
-    long long duty_start[2];   // flattened index of each owed unit's first tile
+    long long s, e, len;          // tile range [s, e) of the flattened order; range length
 };
 static_assert(sizeof(SkShared) <= 128, "SkShared must fit the misc area");
 
@@ -327,7 +320,6 @@ __device__ __noinline__ void locate_range(const AttnParams &p, int upr, int lane
         sk->b0 = b0;
         sk->ur0 = ur0;
         sk->off0 = off0;
-        sk->nduty = 0;
         sk->ntiles0 = nt0;
         sk->special0 = sp0;
         sk->id0 = id0;
@@ -350,31 +342,12 @@ __device__ void locate_unit(const AttnParams &p, int upr, int lane, SkShared *sk
         sk->b0 = b;
         sk->ur0 = blockIdx.x % upr;
         sk->off0 = 0;
-        sk->nduty = 0;
         sk->ntiles0 = nt;
         sk->special0 = sp;
         sk->id0 = id;
         sk->ctx0 = ctx;
     }
     __syncwarp();
-}
-
-// 16-byte copy global -> shared through L2 only (cp.async.cg), and the wait
-// for all of this thread's copies.
-__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(smem_dst)),
-                 "l"(gsrc)
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-
-// Wait until at most `pending` of this thread's committed groups are in flight.
-template <int pending>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(pending) : "memory");
 }
 
 // Two e4m3 values (low 16 bits of `two`, first value in the low byte) -> two
@@ -719,6 +692,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
     };
 
     // ------------------------------------------------------------ prologue
+    // The merge launch that follows a stream-K launch may start as soon as
+    // every CTA of this grid is running; it waits for this grid to finish.
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (warp == 0) {
         if (lane == 0) {
             // descriptors first: their fetch overlaps the range computation
@@ -966,8 +942,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
         struct PendingEpi {
             bool on;
             bool whole;
-            int si, b, c, pos0, row0, rows_here, unit, ntiles;
-            long long start, unit_start;
+            int si, b, c, pos0, row0, rows_here;
+            long long start;
         } pend{};
         constexpr int kLdPair = N >= 32 ? 2 : 1;   // TMEM loads issued per wait
         auto write_segment = [&](const PendingEpi &pe) {
@@ -1040,36 +1016,19 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     }
                 }
             }
-            // Publish the partial, then count it: the ticket's low 16 bits
-            // count the unit's pieces that are in, its upper bits carry this
-            // call's epoch (a value from another call counts as none).
-            __threadfence();
-            named_bar_softmax_any(false);
-            if (t == 0) {
-                const long long len = sk->len;
-                const int pieces =
-                    (int)((pe.unit_start + pe.ntiles - 1) / len - pe.unit_start / len + 1);
-                unsigned long long *ticket = p.tickets + pe.unit;
-                const unsigned long long tag = p.epoch << 16;
-                unsigned long long old = *reinterpret_cast<volatile unsigned long long *>(ticket);
-                unsigned long long now;
-                while (true) {
-                    now = ((old & ~0xffffull) == tag) ? old + 1 : tag + 1;
-                    const unsigned long long seen = atomicCAS(ticket, old, now);
-                    if (seen == old) break;
-                    old = seen;
-                }
-                if ((int)(now & 0xffffull) == pieces) {
-                    const int d = sk->nduty++;
-                    sk->duty_unit[d] = pe.unit;
-                    sk->duty_tiles[d] = pe.ntiles;
-                    sk->duty_start[d] = pe.unit_start;
-                }
-            }
         };
         while (alive && it.next(p, upr, plan.row_groups, sg)) {
             const uint32_t tmem_o = tmem_o_of(si);
             const int n = sg.x1 - sg.x0;
+            if (t == 0 && sg.x0 == 0 && !plan.unit_mode) {
+                // The unit's entry for the merge launch: where it starts in
+                // the flattened order and its tiles when it is split across
+                // CTAs, 0 tiles when this segment covers it whole.
+                const bool whole = sg.x1 == sg.ntiles;
+                p.units[sg.unit] = make_int4((int)(sg.unit_start & 0xffffffffll),
+                                             (int)(sg.unit_start >> 32), whole ? 0 : sg.ntiles,
+                                             (int)sk->len);
+            }
             const int b = sg.b, c = sg.c;
             const long long ctx = sg.ctx;
             const int disp_tile = p.fused ? -1 : sg.special;   // displaced rows (append done before)
@@ -1470,10 +1429,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
             pend.pos0 = pos0;
             pend.row0 = row0;
             pend.rows_here = rows_here;
-            pend.unit = sg.unit;
-            pend.ntiles = sg.ntiles;
             pend.start = sg.start;
-            pend.unit_start = sg.unit_start;
             gt += n;
             cnt_base += stages_before(2 * n);
             ++si;
@@ -1500,121 +1456,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
             pend.on = false;
         }
 
-        // ------------------------------------------------ merges this CTA owes
-        // Every piece of such a unit is in: weight each piece's partial by
-        // 2^(m_piece - M) / L (M the row's maximum over pieces, L the weighted
-        // sum of the pieces' row sums) and add them up.  The stage ring is
-        // idle now: it takes the pieces' (max, sum) pairs, the weights, and
-        // blocks of the pieces' partial rows, all copied in with cp.async so
-        // that many copies are in flight at once.
-        alive = !named_bar_softmax_any(!alive || *abort_flag);
-        if (alive && sk->nduty > 0) {
-            __threadfence();
-            float2 *s_ml = reinterpret_cast<float2 *>(smem);                 // [piece][row]
-            float *s_w = reinterpret_cast<float *>(smem + kMaxPieces * N * 8); // [row][piece]
-            float4 *s_buf = reinterpret_cast<float4 *>(smem + kMaxPieces * N * 12);
-            constexpr int kBufBytes = NS * kStageBytes - kMaxPieces * N * 12;
-            constexpr int D4 = D / 4;
-            const long long len = sk->len;
-            for (int d = 0; d < sk->nduty; ++d) {
-                const int u = sk->duty_unit[d];
-                const long long u0 = sk->duty_start[d];
-                const int nt = sk->duty_tiles[d];
-                const int b = u / upr, ur = u % upr;
-                const int c = ur / plan.row_groups, rg = ur % plan.row_groups;
-                const int pos0 = rg * plan.pos_per_group;
-                const int npos = min(plan.pos_per_group, p.k - pos0);
-                const int rows_here = npos * p.group;
-                const long long g_first = u0 / len;
-                const int np = (int)((u0 + nt - 1) / len - g_first + 1);
-                // first partial row of piece q: the slot of CTA g_first + q
-                // (1 when the piece starts inside that CTA's range)
-                auto piece_base = [&](int q) -> size_t {
-                    const long long gq = g_first + q;
-                    return ((size_t)gq * 2 + (u0 > gq * len ? 1 : 0)) * N;
-                };
-                // Blocks of rb rows, two buffers: block i + 1 streams in while
-                // block i is summed.
-                int rb = kBufBytes / (2 * np * D * 4);
-                if (rb < 1) rb = 1;
-                if (rb > rows_here) rb = rows_here;
-                const int nblk = (rows_here + rb - 1) / rb;
-                auto load_block = [&](int blk) {
-                    const int r0 = blk * rb, nr = min(rb, rows_here - r0);
-                    const int chunk = nr * D4;
-                    float4 *dst = s_buf + (size_t)(blk & 1) * np * rb * D4;
-                    for (int e = t; e < np * chunk; e += 128) {
-                        const int q = e / chunk, off = e % chunk;
-                        cp_async16(&dst[e], reinterpret_cast<const float4 *>(
-                                                p.part_o + (piece_base(q) + r0) * D) + off);
-                    }
-                    cp_async_commit();
-                };
-                // the pieces' (max, sum) pairs and the first block together
-                for (int e = t; e < np * rows_here; e += 128) {
-                    const int q = e / rows_here, r = e % rows_here;
-                    if ((r & 1) == 0) {
-                        if (r + 1 < rows_here)
-                            cp_async16(&s_ml[q * N + r], &p.part_ml[piece_base(q) + r]);
-                        else
-                            s_ml[q * N + r] = __ldcg(&p.part_ml[piece_base(q) + r]);
-                    }
-                }
-                cp_async_commit();
-                load_block(0);
-                cp_async_wait<1>();
-                named_bar_softmax_any(false);
-                for (int r = t; r < rows_here; r += 128) {
-                    float M = -INFINITY;
-                    for (int q = 0; q < np; ++q)
-                        if (s_ml[q * N + r].y > 0.f) M = fmaxf(M, s_ml[q * N + r].x);
-                    float lsum = 0.f;
-                    for (int q = 0; q < np; ++q) {
-                        const float2 v = s_ml[q * N + r];
-                        const float w = v.y > 0.f ? fast_exp2(v.x - M) : 0.f;
-                        s_w[r * kMaxPieces + q] = w;
-                        lsum += v.y * w;
-                    }
-                    const float inv = 1.f / lsum;
-                    for (int q = 0; q < np; ++q) s_w[r * kMaxPieces + q] *= inv;
-                }
-                for (int blk = 0; blk < nblk; ++blk) {
-                    if (blk + 1 < nblk) {
-                        load_block(blk + 1);
-                        cp_async_wait<1>();
-                    } else {
-                        cp_async_wait<0>();
-                    }
-                    named_bar_softmax_any(false);
-                    const int r0 = blk * rb, nr = min(rb, rows_here - r0);
-                    const int chunk = nr * D4;
-                    const float4 *src = s_buf + (size_t)(blk & 1) * np * rb * D4;
-                    // out row of block row rr: r = r0 + rr = j' * group + h'
-                    for (int e = t; e < chunk; e += 128) {
-                        const int rr = e / D4, d4 = e % D4, r = r0 + rr;
-                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                        for (int q = 0; q < np; ++q) {
-                            const float w = s_w[r * kMaxPieces + q];
-                            const float4 v = src[q * chunk + e];
-                            if (w != 0.f) {
-                                acc.x += v.x * w;
-                                acc.y += v.y * w;
-                                acc.z += v.z * w;
-                                acc.w += v.w * w;
-                            }
-                        }
-                        const int row = pos0 * p.group + r, j = row / p.group, hp = row - j * p.group;
-                        reinterpret_cast<float4 *>(
-                            p.out + (((size_t)b * p.k + j) * p.q_heads + (size_t)c * p.group + hp) *
-                                        D)[d4] = acc;
-                    }
-                    named_bar_softmax_any(false);
-                }
-                // The ticket is ready for the next call (a graph replay keeps
-                // its epoch, so a leftover count would be wrong).
-                if (t == 0) p.tickets[u] = 0ull;
-            }
-        }
     }
 
     tc::tc_fence_before();
@@ -1623,6 +1464,98 @@ __global__ void __launch_bounds__(kThreads, MINB)
     if (warp == 1) {
         __syncwarp();
         tc::tmem_dealloc(tmem, L::kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Merge of split units (stream-K launches)
+// ---------------------------------------------------------------------------
+//
+// Each piece of a split unit left, per row, its running maximum m_s (log2
+// units), its sum l_s and its unnormalised output O_s (already times the V
+// scale); the softmax over the union of the pieces is
+//     out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,   M = max_s m_s,
+// the rescaling an online softmax applies between key blocks; pieces with
+// l_s = 0 saw no visible key.  One CTA per (unit, 4 rows): the unit table
+// says whether the unit was split and where it starts; piece q sits in slot
+// (g, 0/1) of CTA g = first CTA + q.  It starts before the attention grid
+// ends (programmatic dependent launch) and waits for it with
+// griddepcontrol.wait, which also makes the grid's writes visible.
+constexpr int kFixRows = 4;
+constexpr int kFixThreads = 256;
+
+template <int D>
+__global__ void __launch_bounds__(kFixThreads) attn_fixup_kernel(const AttnParams p, int upr,
+                                                                 int row_groups,
+                                                                 int pos_per_group,
+                                                                 int slot_rows) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int u = blockIdx.x;
+    const int b = u / upr, ur = u % upr;
+    const int c = ur / row_groups, rg = ur % row_groups;
+    int id;
+    long long ctx;
+    if (b >= p.batch || !request_ok(p, b, &id, &ctx)) return;   // NaN already written
+    const int4 e = p.units[u];
+    const int nt = e.z;
+    if (nt == 0) return;                                          // whole: already written
+    const long long u0 = (long long)(unsigned)e.x | ((long long)e.y << 32);
+    const long long len = e.w;
+    const int pos0 = rg * pos_per_group;
+    const int npos = min(pos_per_group, p.k - pos0);
+    const int rows_here = npos * p.group;
+    const int r_first = blockIdx.y * kFixRows;
+    if (r_first >= rows_here) return;
+    const int nr = min(kFixRows, rows_here - r_first);
+    const long long g_first = u0 / len;
+    const int np = (int)((u0 + nt - 1) / len - g_first + 1);
+    auto piece_base = [&](int q) -> size_t {
+        const long long gq = g_first + q;
+        return ((size_t)gq * 2 + (u0 > gq * len ? 1 : 0)) * slot_rows;
+    };
+    __shared__ float s_w[kFixRows][kMaxPieces];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (warp < nr) {
+        const int r = r_first + warp;
+        float M = -INFINITY;
+        for (int q = lane; q < np; q += 32) {
+            const float2 v = p.part_ml[piece_base(q) + r];
+            if (v.y > 0.f) M = fmaxf(M, v.x);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+        float lsum = 0.f;
+        for (int q = lane; q < np; q += 32) {
+            const float2 v = p.part_ml[piece_base(q) + r];
+            const float w = v.y > 0.f ? fast_exp2(v.x - M) : 0.f;
+            s_w[warp][q] = w;
+            lsum += v.y * w;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(kFull, lsum, o);
+        const float inv = 1.f / lsum;
+        for (int q = lane; q < np; q += 32) s_w[warp][q] *= inv;
+    }
+    __syncthreads();
+    constexpr int D4 = D / 4;
+    for (int x = threadIdx.x; x < nr * D4; x += kFixThreads) {
+        const int rr = x / D4, d4 = x % D4, r = r_first + rr;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int q = 0; q < np; ++q) {
+            const float w = s_w[rr][q];
+            const float4 v =
+                reinterpret_cast<const float4 *>(p.part_o + (piece_base(q) + r) * D)[d4];
+            if (w != 0.f) {
+                acc.x += v.x * w;
+                acc.y += v.y * w;
+                acc.z += v.z * w;
+                acc.w += v.w * w;
+            }
+        }
+        const int row = pos0 * p.group + r, j = row / p.group, hp = row - j * p.group;
+        reinterpret_cast<float4 *>(
+            p.out + (((size_t)b * p.k + j) * p.q_heads + (size_t)c * p.group + hp) * D)[d4] = acc;
     }
 }
 
@@ -1649,7 +1582,25 @@ cudaError_t launch_tc(const AttnParams &p, const TcPlan &plan, const TcMaps &map
     }
     kernel<<<grid, kThreads, L::kAlloc, stream>>>(p, plan, maps);
     count_launches(1);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess || plan.unit_mode) return e;
+    // stream-K: merge the split units in a second launch that may start while
+    // this one drains (it waits for this grid inside the kernel)
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(p.batch * p.kv_heads * plan.row_groups, (N + kFixRows - 1) / kFixRows);
+    cfg.blockDim = dim3(kFixThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int upr = p.kv_heads * plan.row_groups;
+    e = cudaLaunchKernelEx(&cfg, attn_fixup_kernel<D>, p, upr, plan.row_groups,
+                           plan.pos_per_group, N);
+    count_launches(1);
+    return e;
 }
 
 }  // namespace

@@ -33,11 +33,14 @@ struct AttnParams {
     float *out;                 // [B][k][Hq][D]
     // Split partials (running max and sum in log2 units, unnormalised O).
     // CUDA-core path: [B][Hkv][nchunks][rows].  Tensor-core path: two slots
-    // per CTA, [grid][2][rows per tile], with one ticket per unit.
+    // per CTA, [grid][2][rows per tile].
     float2 *part_ml;
     float *part_o;
-    unsigned long long *tickets;   // tensor-core path: [B * units per request]
-    unsigned long long epoch;      // tensor-core path: tag of this call's tickets
+    // Tensor-core stream-K path: per (request, KV head, row group) unit, its
+    // first tile's flattened index (x: low, y: high 32 bits), its tile count
+    // when split across CTAs (z; 0 when one CTA covered it) and the range
+    // length (w), for the merge launch.
+    int4 *units;
     int *dev_status;
     int num_ids;                // rings / caches available
     int batch, k, q_heads, kv_heads, head_dim, group, rows;

@@ -73,10 +73,9 @@ carat_status carat_swa_attention_noalloc(float *out, const void *queries, const 
     }
     void *scratch = nullptr;
     if (carat::scratch_address(&scratch) != cudaSuccess) return CARAT_ERR_CUDA;
-    // The split-K partials are fully written before they are read, and the
-    // tensor-core path's tickets start at zero (a static device array is
-    // zero-initialised), are reset by the CTA that merges their unit, and
-    // carry each call's epoch, so the array needs no clearing between calls.
+    // Everything in the scratch (partials, the tensor-core path's unit table)
+    // is written before it is read within a call, so the array needs no
+    // clearing between calls.
     return carat_swa_attention(out, queries, k_ring, v_ring, num_rings, ring_ids, displaced,
                                context_lengths, proposal_count, batch, q_heads, kv_heads,
                                head_dim, window, scale, scratch, carat::kNoAllocScratchBytes,

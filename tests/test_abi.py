@@ -56,13 +56,13 @@ def test_workspace_queries(lib):
     # Tensor-core path: two partial slots (rows per tile x head_dim floats, and
     # a (max, sum) pair per row) for each CTA of the persistent grid -- two
     # CTAs per SM for 16-row tiles at head_dim 256, 152 SMs when no GPU is
-    # present -- plus one 8-byte ticket per (request, KV head, row group).
+    # present -- plus one 16-byte merge entry per (request, KV head, row group).
     def a256(x):
         return (x + 255) // 256 * 256
 
     def expected(batch, rows_per_tile, head_dim, ctas_per_sm, units_per_request):
         slots = ctas_per_sm * 152 * 2 * rows_per_tile
-        return a256(slots * 8) + a256(slots * head_dim * 4) + a256(batch * units_per_request * 8)
+        return a256(slots * 8) + a256(slots * head_dim * 4) + a256(batch * units_per_request * 16)
 
     if lib.carat_swa_workspace_bytes(56, 1, 16, 8, 256, 1024) == expected(56, 16, 256, 2, 8):
         assert lib.carat_swa_workspace_bytes(1, 1, 16, 8, 256, 1024) == expected(1, 16, 256, 2, 8)
