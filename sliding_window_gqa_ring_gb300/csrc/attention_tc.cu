@@ -38,7 +38,7 @@
 // range's first and last) write a partial (row max, row sum, unnormalised O)
 // to the workspace, and the CTA holding a unit's first tile records in a unit
 // table whether the unit was split.  A second launch (attn_fixup_kernel, one
-// CTA per (unit, 4 rows), started early by programmatic dependent launch and
+// CTA per (unit, row), started early by programmatic dependent launch and
 // waiting for this grid) merges the split units' pieces in parallel.  The
 // range is never shorter than 1/(kMaxPieces - 1) of the longest unit, so no
 // unit is cut into more than kMaxPieces pieces.  The CTAs never wait for one
@@ -1476,87 +1476,85 @@ __global__ void __launch_bounds__(kThreads, MINB)
 // scale); the softmax over the union of the pieces is
 //     out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,   M = max_s m_s,
 // the rescaling an online softmax applies between key blocks; pieces with
-// l_s = 0 saw no visible key.  One CTA per (unit, 4 rows): the unit table
-// says whether the unit was split and where it starts; piece q sits in slot
-// (g, 0/1) of CTA g = first CTA + q.  It starts before the attention grid
+// l_s = 0 saw no visible key.  One CTA per (unit, row), one thread per 16
+// bytes of the row: the unit table says whether the unit was split and
+// where it starts; piece q sits in slot (g, 0/1) of CTA g = first CTA + q.  It starts before the attention grid
 // ends (programmatic dependent launch) and waits for it with
 // griddepcontrol.wait, which also makes the grid's writes visible.
-constexpr int kFixRows = 4;
-constexpr int kFixThreads = 256;
-
 template <int D>
-__global__ void __launch_bounds__(kFixThreads) attn_fixup_kernel(const AttnParams p, int upr,
-                                                                 int row_groups,
-                                                                 int pos_per_group,
-                                                                 int slot_rows) {
+__global__ void __launch_bounds__(D / 4) attn_fixup_kernel(const AttnParams p, int upr,
+                                                            int row_groups, int pos_per_group,
+                                                            int slot_rows) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int u = blockIdx.x;
+    const int u = blockIdx.x, r = blockIdx.y;   // unit, row within its row group
     const int b = u / upr, ur = u % upr;
     const int c = ur / row_groups, rg = ur % row_groups;
-    int id;
-    long long ctx;
-    if (b >= p.batch || !request_ok(p, b, &id, &ctx)) return;   // NaN already written
+    if (b >= p.batch) return;
+    // the request's validity and the unit's entry, in one round trip
+    const long long ctx = p.context_lengths[b];
+    const int id = p.ids ? p.ids[b] : b;
     const int4 e = p.units[u];
-    const int nt = e.z;
-    if (nt == 0) return;                                          // whole: already written
-    const long long u0 = (long long)(unsigned)e.x | ((long long)e.y << 32);
-    const long long len = e.w;
+    if (!request_valid(p, id, ctx)) return;     // NaN already written
     const int pos0 = rg * pos_per_group;
     const int npos = min(pos_per_group, p.k - pos0);
-    const int rows_here = npos * p.group;
-    const int r_first = blockIdx.y * kFixRows;
-    if (r_first >= rows_here) return;
-    const int nr = min(kFixRows, rows_here - r_first);
+    if (r >= npos * p.group) return;
+    const int nt = e.z;
+    if (nt == 0) return;                          // whole: already written
+    const long long u0 = (long long)(unsigned)e.x | ((long long)e.y << 32);
+    const long long len = e.w;
     const long long g_first = u0 / len;
     const int np = (int)((u0 + nt - 1) / len - g_first + 1);
     auto piece_base = [&](int q) -> size_t {
         const long long gq = g_first + q;
         return ((size_t)gq * 2 + (u0 > gq * len ? 1 : 0)) * slot_rows;
     };
-    __shared__ float s_w[kFixRows][kMaxPieces];
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    if (warp < nr) {
-        const int r = r_first + warp;
-        float M = -INFINITY;
-        for (int q = lane; q < np; q += 32) {
-            const float2 v = p.part_ml[piece_base(q) + r];
-            if (v.y > 0.f) M = fmaxf(M, v.x);
-        }
+    // weights 2^(m_q - M) / L of the pieces, by warp 0 (each lane reads the
+    // (max, sum) pairs of pieces lane and lane + 32 once)
+    __shared__ float s_w[kMaxPieces];
+    static_assert(kMaxPieces <= 64, "two pieces per lane");
+    const int lane = threadIdx.x % 32;
+    if (threadIdx.x < 32) {
+        float2 v0 = make_float2(-INFINITY, 0.f), v1 = v0;
+        if (lane < np) v0 = p.part_ml[piece_base(lane) + r];
+        if (lane + 32 < np) v1 = p.part_ml[piece_base(lane + 32) + r];
+        float M = fmaxf(v0.y > 0.f ? v0.x : -INFINITY, v1.y > 0.f ? v1.x : -INFINITY);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-        float lsum = 0.f;
-        for (int q = lane; q < np; q += 32) {
-            const float2 v = p.part_ml[piece_base(q) + r];
-            const float w = v.y > 0.f ? fast_exp2(v.x - M) : 0.f;
-            s_w[warp][q] = w;
-            lsum += v.y * w;
-        }
+        const float w0 = v0.y > 0.f ? fast_exp2(v0.x - M) : 0.f;
+        const float w1 = v1.y > 0.f ? fast_exp2(v1.x - M) : 0.f;
+        float lsum = v0.y * w0 + v1.y * w1;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(kFull, lsum, o);
         const float inv = 1.f / lsum;
-        for (int q = lane; q < np; q += 32) s_w[warp][q] *= inv;
+        if (lane < np) s_w[lane] = w0 * inv;
+        if (lane + 32 < np) s_w[lane + 32] = w1 * inv;
     }
     __syncthreads();
-    constexpr int D4 = D / 4;
-    for (int x = threadIdx.x; x < nr * D4; x += kFixThreads) {
-        const int rr = x / D4, d4 = x % D4, r = r_first + rr;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-        for (int q = 0; q < np; ++q) {
-            const float w = s_w[rr][q];
-            const float4 v =
-                reinterpret_cast<const float4 *>(p.part_o + (piece_base(q) + r) * D)[d4];
-            if (w != 0.f) {
-                acc.x += v.x * w;
-                acc.y += v.y * w;
-                acc.z += v.z * w;
-                acc.w += v.w * w;
+    // one 16-byte column per thread, eight pieces' loads in flight at a time
+    const int d4 = threadIdx.x;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q0 = 0; q0 < np; q0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (q0 + i < np)
+                v[i] = reinterpret_cast<const float4 *>(p.part_o + (piece_base(q0 + i) + r) * D)[d4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (q0 + i < np) {
+                const float w = s_w[q0 + i];
+                if (w != 0.f) {
+                    acc.x += v[i].x * w;
+                    acc.y += v[i].y * w;
+                    acc.z += v[i].z * w;
+                    acc.w += v[i].w * w;
+                }
             }
         }
-        const int row = pos0 * p.group + r, j = row / p.group, hp = row - j * p.group;
-        reinterpret_cast<float4 *>(
-            p.out + (((size_t)b * p.k + j) * p.q_heads + (size_t)c * p.group + hp) * D)[d4] = acc;
     }
+    const int row = pos0 * p.group + r, j = row / p.group, hp = row - j * p.group;
+    reinterpret_cast<float4 *>(
+        p.out + (((size_t)b * p.k + j) * p.q_heads + (size_t)c * p.group + hp) * D)[d4] = acc;
 }
 
 // ---------------------------------------------------------------------------
@@ -1587,8 +1585,8 @@ cudaError_t launch_tc(const AttnParams &p, const TcPlan &plan, const TcMaps &map
     // stream-K: merge the split units in a second launch that may start while
     // this one drains (it waits for this grid inside the kernel)
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(p.batch * p.kv_heads * plan.row_groups, (N + kFixRows - 1) / kFixRows);
-    cfg.blockDim = dim3(kFixThreads);
+    cfg.gridDim = dim3(p.batch * p.kv_heads * plan.row_groups, N);
+    cfg.blockDim = dim3(D / 4);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
