@@ -65,6 +65,7 @@
 #include <cfloat>
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "carat_internal.cuh"
 #include "tc_common.cuh"
@@ -88,18 +89,19 @@ struct Layout {
     static constexpr int KS = D / 128;                 // stages per K (or V) tile
     static constexpr int kQBlock = N * 128;            // one 64-d block of Q rows
     // FP8 caches (NR > 0): NR raw stages of e4m3 bytes (128 keys x 128 d) in
-    // front of the bf16 stages the tensor core reads.
+    // front of the 16-bit stages the tensor core reads.
     static constexpr int kRawBytes = 128 * 128;
     static constexpr int kOffRaw = NS * kStageBytes;
     static constexpr int kOffQ = kOffRaw + NR * kRawBytes;
     static constexpr int kOffP = kOffQ + (D / 64) * kQBlock;
     static constexpr int kPBlock = N * 128;            // 64 keys of P rows
     static constexpr int kOffRed = kOffP + 2 * kPBlock;
-    // 2 x max buffers + sum buffer (4 warps x N each), then one segment's
-    // row maxima and sums kept for its deferred epilogue
-    static constexpr int kRedFloats = 3 * 4 * N + 2 * N;
+    // 2 x max buffers + sum buffer (4 warps x N each), one segment's row
+    // maxima and sums kept for its deferred epilogue, then (FP8) the row
+    // score scales of the segment being computed
+    static constexpr int kRedFloats = 3 * 4 * N + 3 * N;
     static constexpr int kOffBar = kOffRed + kRedFloats * 4;
-    static constexpr int kNumBars = 2 * NS + 7 + 2 * NR;
+    static constexpr int kNumBars = 2 * NS + 7 + 2 * NR + (NR > 0 ? 1 : 0);
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;   // SkShared
     static constexpr int kBytes = kOffMisc + 128;
     static constexpr int kAlloc = kBytes + 1024;       // base alignment slack
@@ -350,46 +352,92 @@ __device__ void locate_unit(const AttnParams &p, int upr, int lane, SkShared *sk
     __syncwarp();
 }
 
-// Two e4m3 values (low 16 bits of `two`, first value in the low byte) -> two
-// bf16 values (first in the low half).  Exact: e4m3 -> f16 -> f32 -> bf16
-// never rounds, as every e4m3 value is an f16 and a bf16 value.  (An integer
-// rebias of the f16 bits measured slower than the two conversions it saves.)
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two));
-    float lo, hi;
-    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\t"
-        "cvt.f32.f16 %1, b;\n\t}"
-        : "=f"(lo), "=f"(hi)
-        : "r"(h2));
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-// 16 e4m3 bytes -> 16 bf16 values (two 16-byte chunks, in order).
-__device__ __forceinline__ void e4m3x16_to_bf16(uint4 v, uint4 &o0, uint4 &o1) {
-    o0 = make_uint4(e4m3x2_to_bf16x2(v.x), e4m3x2_to_bf16x2(v.x >> 16), e4m3x2_to_bf16x2(v.y),
-                    e4m3x2_to_bf16x2(v.y >> 16));
-    o1 = make_uint4(e4m3x2_to_bf16x2(v.z), e4m3x2_to_bf16x2(v.z >> 16), e4m3x2_to_bf16x2(v.w),
-                    e4m3x2_to_bf16x2(v.w >> 16));
+// Four e4m3 values (first in the low byte) -> four f16 values, two per word
+// (first in the low half).  Exact: every e4m3 value, subnormals included, is
+// an f16 value.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
 }
 
 // One 128-byte row of e4m3 (a 128-d block, 128-byte swizzle at row `row`)
-// -> its bf16 image: 16-byte chunk c' of 64-d slab (c / 4) of the
-// destination, each slab a 128-byte swizzled row; zero: write zeros.
+// -> its f16 image: 16-byte chunk c' of 64-d slab (c / 4) of the
+// destination, each slab a 128-byte swizzled row; zero: write zeros.  All
+// eight loads are issued before the first conversion (source and
+// destination are both shared memory, so the compiler would not hoist a load
+// above an earlier store by itself).
 __device__ __forceinline__ void convert_row(const uint8_t *src, uint8_t *dst0, uint8_t *dst1,
                                             int row, bool zero) {
     const int sw = row & 7;
+    uint4 v[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        v[c] = zero ? make_uint4(0, 0, 0, 0)
+                    : *reinterpret_cast<const uint4 *>(src + ((c ^ sw) << 4));
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-        uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
-        if (!zero) e4m3x16_to_bf16(*reinterpret_cast<const uint4 *>(src + ((c ^ sw) << 4)), o0, o1);
+        uint4 o0, o1;
+        e4m3x4_to_f16x4(v[c].x, o0.x, o0.y);
+        e4m3x4_to_f16x4(v[c].y, o0.z, o0.w);
+        e4m3x4_to_f16x4(v[c].z, o1.x, o1.y);
+        e4m3x4_to_f16x4(v[c].w, o1.z, o1.w);
         uint8_t *d = (c < 4) ? dst0 : dst1;
         const int cc = 2 * (c & 3);
         *reinterpret_cast<uint4 *>(d + ((cc ^ sw) << 4)) = o0;
         *reinterpret_cast<uint4 *>(d + (((cc + 1) ^ sw) << 4)) = o1;
     }
+}
+
+// Two fp32 values -> an f16 pair (first in the low half), round to nearest.
+__device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// FP8 caches: the N query rows of a segment, loaded as bf16 (D/64 swizzled
+// blocks of N rows x 128 bytes), rewritten in place as f16 for the f16
+// tensor-core products.  Row r is multiplied by 2^s_r, s_r chosen so its
+// largest |q| lands in [2^14, 2^15): every element down to 2^-28 of that
+// maximum keeps its bf16 value exactly, and the row's scores come out
+// multiplied by 2^s_r, which qscale[r] = scale_log2 * 2^-s_r takes back out
+// (both factors powers of two, so nothing rounds).  128 threads, 128 / N per
+// row, each over every (128 / N)-th 16-byte chunk of its row.
+template <int D, int N, int QBlock>
+__device__ __forceinline__ void convert_q_f16(uint8_t *s_q, float *qscale, float scale_log2,
+                                              int t) {
+    constexpr int kTpr = 128 / N;
+    const int r = t / kTpr, j = t % kTpr;
+    uint8_t *row = s_q + r * 128;
+    const int sw = r & 7;
+    uint32_t amax = 0;   // |q| bits; ordered like the values for non-NaN inputs
+#pragma unroll
+    for (int ch = j; ch < D / 8; ch += kTpr) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(row + (ch / 8) * QBlock +
+                                                         (((ch % 8) ^ sw) << 4));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            amax = max(amax, max((w[e] << 16) & 0x7fffffffu, w[e] & 0x7fff0000u));
+    }
+#pragma unroll
+    for (int o = 1; o < kTpr; o <<= 1) amax = max(amax, __shfl_xor_sync(kFull, amax, o));
+    // floor(log2 amax) for a normal amax; zero or subnormal rows take s = 100
+    int s = 14 - ((int)(amax >> 23) - 127);
+    s = s < -100 ? -100 : (s > 100 ? 100 : s);
+    const float up = __int_as_float((127 + s) << 23);
+#pragma unroll
+    for (int ch = j; ch < D / 8; ch += kTpr) {
+        uint4 *a = reinterpret_cast<uint4 *>(row + (ch / 8) * QBlock + (((ch % 8) ^ sw) << 4));
+        const uint4 v = *a;
+        *a = make_uint4(f16x2_rn(bf16lo(v.x) * up, bf16hi(v.x) * up),
+                        f16x2_rn(bf16lo(v.y) * up, bf16hi(v.y) * up),
+                        f16x2_rn(bf16lo(v.z) * up, bf16hi(v.z) * up),
+                        f16x2_rn(bf16lo(v.w) * up, bf16hi(v.w) * up));
+    }
+    if (j == 0) qscale[r] = scale_log2 * __int_as_float((127 - s) << 23);
 }
 
 // Barrier over the 128 softmax threads that also ORs a predicate across them,
@@ -476,8 +524,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
     using L = Layout<D, N, NS, NR>;
     constexpr int KS = L::KS;
     // FP8 caches: the producer fills raw e4m3 stages, the softmax warps
-    // convert each into a bf16 stage (exactly: every e4m3 value is a bf16
-    // value), and the tensor core reads the bf16 stages as for a bf16 cache.
+    // convert each into an f16 stage (exactly: every e4m3 value is an f16
+    // value, and one conversion instruction widens two of them), rewrite each
+    // segment's Q as f16 with a power-of-two scale per row, and write P as
+    // f16; the tensor core then runs the same products with f16 operands.
     constexpr bool F8 = NR > 0;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int upr = p.kv_heads * plan.row_groups;   // units per request
@@ -498,6 +548,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     uint64_t *fin = s_full + 6;
     uint64_t *raw_full = s_full + 7;     // [NR] FP8: e4m3 stage landed
     uint64_t *raw_empty = raw_full + NR; // [NR] FP8: e4m3 stage converted
+    uint64_t *q_conv = raw_empty + NR;   // FP8: Q rewritten as f16
     uint8_t *s_raw = smem + L::kOffRaw;
     SkShared *sk = reinterpret_cast<SkShared *>(smem + L::kOffMisc);
     volatile int *abort_flag = &sk->abort_flag;
@@ -718,6 +769,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
             tc::mbar_init(p_full, 128);
             tc::mbar_init(o_done, 1);
             tc::mbar_init(q_full, 1);
+            if (F8) tc::mbar_init(q_conv, 128);
             tc::mbar_init(q_empty, 1);
             tc::mbar_init(fin, 1);
             sk->abort_flag = 0;
@@ -779,8 +831,11 @@ __global__ void __launch_bounds__(kThreads, MINB)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(128, N, false, false);
-            constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(128, N, true, false);
+            // FP8 caches compute with f16 operands (K, V, Q and P), else bf16.
+            constexpr uint32_t idesc_qk = F8 ? tc::idesc_f16_f32(128, N, false, false)
+                                             : tc::idesc_bf16_f32(128, N, false, false);
+            constexpr uint32_t idesc_pv = F8 ? tc::idesc_f16_f32(128, N, true, false)
+                                             : tc::idesc_bf16_f32(128, N, true, false);
             const uint32_t q_base = tc::smem_u32(s_q);
             const uint32_t p_base = tc::smem_u32(s_p);
             SegIter it;
@@ -791,7 +846,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
             int si = 0;
             while (alive && it.next(p, upr, plan.row_groups, sg)) {
                 const int n = sg.x1 - sg.x0;
-                if (!wait_or_abort(q_full, si & 1, abort_flag, p.dev_status)) {
+                if (!wait_or_abort(F8 ? q_conv : q_full, si & 1, abort_flag, p.dev_status)) {
                     alive = false;
                     break;
                 }
@@ -937,6 +992,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         uint32_t ccnt = 0;                   // FP8: stages converted so far
         float *s_mrow = red + 12 * N;        // a finished segment's row maxima
         float *s_lrow = red + 13 * N;        // and row sums
+        float *s_qscale = red + 14 * N;      // FP8: this segment's row score scales
         // The epilogue of a finished segment, run once the next segment's first
         // tile is under way (or at once with a single O^T buffer).
         struct PendingEpi {
@@ -1124,6 +1180,19 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 }
                 return true;
             };
+            if constexpr (F8) {
+                // This segment's Q as f16 once its copy has landed; then the
+                // MMA warp may start the segment's products.
+                const bool q_ok =
+                    __all_sync(kFull, wait_or_abort(q_full, si & 1, abort_flag, p.dev_status));
+                if (q_ok) convert_q_f16<D, N, L::kQBlock>(s_q, s_qscale, p.scale_log2, t);
+                tc::fence_proxy_async_smem();
+                if (named_bar_softmax_any(!q_ok || *abort_flag)) {
+                    alive = false;
+                    break;
+                }
+                tc::mbar_arrive(q_conv);
+            }
             float m_run[N], l_part[N];
 #pragma unroll
             for (int r = 0; r < N; ++r) {
@@ -1136,7 +1205,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 const int i = order_tile(sg, sg.x0 + idx);
                 if constexpr (F8) {
                     // K of this tile and the next, before their QK products
-                    const int xk = idx + 1 < n ? idx + 1 : idx;
+                    // (When the stage ring holds one K tile only, the stage of a
+                    // special tile is free again only after its PV product, which
+                    // waits for this tile's P: no look-ahead past it.)
+                    const int xk = (idx + 1 < n && !(NS == KS && idx == xs)) ? idx + 1 : idx;
                     if (!convert_through(cnt_base + stages_before((xk == 0 ? 0 : 2 * xk - 1) + 1),
                                          false))
                         alive = false;
@@ -1197,7 +1269,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 float tmax[N];
 #pragma unroll
                 for (int r = 0; r < N; ++r) {
-                    x[r] = ((rowmask >> r) & 1ull) ? x[r] * p.scale_log2 : -INFINITY;
+                    x[r] = ((rowmask >> r) & 1ull) ? x[r] * (F8 ? s_qscale[r] : p.scale_log2)
+                                                   : -INFINITY;
                     tmax[r] = x[r];
                 }
                 const int rb = warp_transpose_reduce<N, true>(tmax, lane);
@@ -1250,8 +1323,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     const uint32_t col = t % 64;
 #pragma unroll
                     for (int r = 0; r < N; ++r) {
-                        const __nv_bfloat16 h = __float2bfloat16_rn(x[r]);
-                        *reinterpret_cast<__nv_bfloat16 *>(pblk + tc::sw128_offset(r, col)) = h;
+                        uint16_t h;
+                        if constexpr (F8)
+                            h = __half_as_ushort(__float2half_rn(x[r]));
+                        else
+                            h = __bfloat16_as_ushort(__float2bfloat16_rn(x[r]));
+                        *reinterpret_cast<uint16_t *>(pblk + tc::sw128_offset(r, col)) = h;
                     }
                     if (idx > 0 && rescale) {
 #pragma unroll
@@ -1290,8 +1367,11 @@ __global__ void __launch_bounds__(kThreads, MINB)
                         }
                     }
                     if constexpr (F8) {
-                        // V of this tile, its no-token rows as zeros
-                        if (!convert_through(cnt_base + stages_before(v_part(idx, n) + 1),
+                        // V of this tile, its no-token rows as zeros (a special
+                        // tile's V rows were converted with its K rows; going on
+                        // to the parts after it here could wait on its own PV)
+                        if (idx != xs &&
+                            !convert_through(cnt_base + stages_before(v_part(idx, n) + 1),
                                              tile_partial && !ki.data))
                             alive = false;
                     } else if (idx == xs) {
@@ -1611,7 +1691,7 @@ int tc_rows_per_tile(int group, int k) {
 }
 
 int tc_ctas_per_sm(int head_dim, int rows_per_tile, bool fp8) {
-    return (!fp8 && head_dim == 256 && rows_per_tile == 16) ? 2 : 1;
+    return (head_dim == 256 && rows_per_tile == 16) ? 2 : 1;
 }
 
 bool tc_fp8_supported(int head_dim, int group, int k) {
@@ -1673,8 +1753,9 @@ cudaError_t launch_attention_tc(const AttnParams &p, int grid, bool unit_mode, b
         const uint32_t boxq[4] = {64, (uint32_t)p.group, (uint32_t)plan.pos_per_group, 1};
         if (!make_bf16_tensor_map(&maps.q, p.q, 4, dimsq, stridesq, boxq, true))
             return cudaErrorInvalidValue;
-        // one CTA per SM: 3 bf16 stages and 6 (or 4) raw stages in flight
-        if (n == 16) return launch_tc<256, 16, 3, 1, 6>(p, plan, maps, grid, stream);
+        // 16 rows: two CTAs per SM, each with 2 f16 stages and 2 raw stages;
+        // else one CTA per SM with 3 f16 stages and 6 (or 4) raw stages
+        if (n == 16) return launch_tc<256, 16, 2, 2, 2>(p, plan, maps, grid, stream);
         if (n == 32) return launch_tc<256, 32, 3, 1, 6>(p, plan, maps, grid, stream);
         return launch_tc<256, 64, 3, 1, 4>(p, plan, maps, grid, stream);
     }

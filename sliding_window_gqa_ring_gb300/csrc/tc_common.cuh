@@ -242,6 +242,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
            ((uint32_t)(M >> 4) << 24);
 }
 
+// The same for f16 A and B (type fields 0).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn_major,
+                                                     bool b_mn_major) {
+    return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // Byte offset of element (row, col) of a K-major bf16 tile stored as 128-byte
 // swizzled rows of 64 elements: 16-byte chunk index XORed with row % 8.
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col) {
