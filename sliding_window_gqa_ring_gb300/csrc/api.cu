@@ -115,10 +115,8 @@ SplitPlan tc_plan(int batch, int group, int k, int kv_heads, int head_dim, long 
     const int n = tc_rows_per_tile(group, k);
     const int slots_total = tc_ctas_per_sm(head_dim, n, fp8) * device_sm_count();
     const long long units = (long long)batch * tc_units_per_request(group, k, kv_heads);
-    // One CTA per unit when there are enough units and each is short; FP8
-    // caches run one CTA per SM, so they keep the persistent schedule, where a
-    // CTA's next segment streams in while it finishes the current one.
-    p.unit_mode = !fp8 && units >= slots_total && max_tiles <= 16;
+    // One CTA per unit when there are enough units and each is short.
+    p.unit_mode = units >= slots_total && max_tiles <= 16;
     p.grid = p.unit_mode ? (int)units : slots_total;
     const size_t slots = (size_t)slots_total * 2 * n;
     p.ml_bytes = align256(slots * sizeof(float2));

@@ -59,17 +59,6 @@
 //               TMEM when a row's maximum moved; per segment they write the
 //               output or the partial.
 //
-// FP8 (e4m3) rings, sliding layers.  The producer lands raw e4m3 stages (128
-// keys x 128 d bytes, 128-byte swizzle) in an NR-deep raw ring.  K stages feed
-// the QK product as they are: kind::f8f6f4 with Q rewritten per segment as
-// e4m3 high and low parts (2N columns of S^T, added by the softmax threads;
-// exact for every element within 2^-9 of its row's largest).  V stages are
-// widened (exactly) to f16 by the softmax threads after they publish P, into
-// the f16 stage ring that the f16 PV product reads; P is written as f16.  The
-// MMA thread frees each raw stage: a K stage by the commit of its QK product,
-// a V stage once its f16 copy is complete, a special stage (16 displaced K
-// and V rows) by the commit of its PV product.
-//
 // Every wait is bounded (mbar_wait): on a timeout the CTA records
 // CARAT_DEV_TIMEOUT, stops issuing work, waits (bounded) for its own copies
 // and MMAs in flight, frees its TMEM and returns.
@@ -116,24 +105,16 @@ struct Layout {
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;   // SkShared
     static constexpr int kBytes = kOffMisc + 128;
     static constexpr int kAlloc = kBytes + 1024;       // base alignment slack
-    // Columns of one S^T buffer: N, or with FP8 caches 2N (the products with
-    // the high and the low e4m3 parts of Q side by side).
-    static constexpr int kSCols = (NR > 0 ? 2 : 1) * N;
     // Two S^T buffers and two O^T buffers when they fit the 512 columns, so one
     // segment's output is written while the next accumulates; else one O^T.
-    static constexpr bool kDoubleO = 2 * kSCols + 2 * KS * N <= 512;
-    static constexpr int kTmemUsed = 2 * kSCols + (kDoubleO ? 2 : 1) * KS * N;
+    static constexpr bool kDoubleO = N * (2 + 2 * KS) <= 512;
+    static constexpr int kTmemUsed = N * (2 + (kDoubleO ? 2 : 1) * KS);
     static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64
                                    : kTmemUsed <= 128 ? 128 : kTmemUsed <= 256 ? 256 : 512;
     static_assert(kAlloc <= 232448, "more dynamic shared memory than one CTA may use");
     // The softmax warps zero masked V rows while all KS stages of a V tile are
     // resident, before the tile's PV product releases any of them.
-    static_assert(NR > 0 || NS >= KS, "the stage ring must hold a whole V tile");
-    // FP8: the raw ring holds a whole K tile, and one more stage when a
-    // special tile's raw stage stays until its PV product comes after the
-    // next tile's QK product (NS > KS).
-    static_assert(NR == 0 || (NR >= KS && (NS == KS || NR >= KS + 1)),
-                  "FP8 raw ring too small for the stage order");
+    static_assert(NS >= KS, "the stage ring must hold a whole V tile");
     static_assert(kOffRaw % 1024 == 0 && kOffQ % 1024 == 0 && kOffP % 1024 == 0 &&
                       kPBlock % 1024 == 0 &&
                       kQBlock % 1024 == 0,
@@ -188,19 +169,6 @@ struct Segment {
     long long start;           // flattened index of the segment's first tile
     long long unit_start;      // flattened index of the unit's first tile
 };
-
-// Stages a segment loads before its part P.  Parts in load order: K(0),
-// then K(x+1) before V(x), then V(n-1); a K or V part takes KS stages,
-// except that a special tile leading the segment (xs == 0) takes one stage
-// for its K part (its K and V rows together) and none for its V part.
-__device__ __forceinline__ uint32_t seg_stages_before(int P, int n, int xs, int KS) {
-    uint32_t st = (uint32_t)P * KS;
-    if (xs >= 0) {
-        if ((xs == 0 ? 0 : 2 * xs - 1) < P) st -= KS - 1;
-        if ((xs == n - 1 ? 2 * n - 1 : 2 * xs + 2) < P) st -= KS;
-    }
-    return st;
-}
 
 // Tile index of order index x: the special tile (this step's rows of a fused
 // append, or the displaced rows of a sliding verify; always the last tile
@@ -422,63 +390,32 @@ __device__ __forceinline__ void convert_row(const uint8_t *src, uint8_t *dst0, u
     }
 }
 
-// e4m3 of two fp32 values (round to nearest even, saturating), first in
-// the low byte.
-__device__ __forceinline__ uint32_t e4m3x2_rn(float lo, float hi) {
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+// Two fp32 values -> an f16 pair (first in the low half), round to nearest.
+__device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
 
-// Eight values (x, already scaled) -> e4m3 high parts hi = e4m3(x) and low
-// parts lo = e4m3(x - hi), eight bytes each in element order.
-__device__ __forceinline__ void e4m3_split8(const float (&x)[8], uint2 &hi, uint2 &lo) {
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        h[e] = e4m3x2_rn(x[2 * e], x[2 * e + 1]);
-        uint32_t h2;
-        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)h[e]));
-        const float d0 = __half2float(__ushort_as_half((uint16_t)(h2 & 0xffffu)));
-        const float d1 = __half2float(__ushort_as_half((uint16_t)(h2 >> 16)));
-        l[e] = e4m3x2_rn(x[2 * e] - d0, x[2 * e + 1] - d1);
-    }
-    hi = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
-    lo = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
-}
-
-// Barrier over the 128 softmax threads (named barrier 1, in the same form
-// as named_bar_softmax_any below, so every use of the barrier is alike).
-__device__ __forceinline__ void named_bar_softmax() {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.u32 p, %0, 0;\n\t"
-        "bar.red.or.pred p, 1, 128, p;\n\t}" ::"r"(0u)
-        : "memory");
-}
-
 // FP8 caches: the N query rows of a segment, loaded as bf16 (D/64 swizzled
-// blocks of N rows x 128 bytes), rewritten in place for the e4m3 QK product
-// as D/128 swizzled blocks of 2N rows x 128 bytes (a 128-d block takes the
-// bytes of the two 64-d bf16 blocks it replaces).  Row r, multiplied by
-// 2^s_r so that its largest |q| lies in [2^7, 2^8), is held as hi = e4m3(q)
-// in row r and lo = e4m3(q - hi) in row N + r.  hi + lo is q exactly for
-// every element of at least 2^-2 after scaling (within 2^-9 of the row's
-// largest), and within 2^-10 of it for smaller ones: q has 8 significant bits,
-// hi keeps 4 and the remainder needs at most 4 more.  The two products give
-// 2^s_r S_r, which qscale[r] = scale_log2 * 2^-s_r takes back out (powers of
-// two: nothing rounds).  128 threads, 128 / N per row.
+// blocks of N rows x 128 bytes), rewritten in place as f16 for the f16
+// tensor-core products.  Row r is multiplied by 2^s_r, s_r chosen so its
+// largest |q| lands in [2^14, 2^15): every element down to 2^-28 of that
+// maximum keeps its bf16 value exactly, and the row's scores come out
+// multiplied by 2^s_r, which qscale[r] = scale_log2 * 2^-s_r takes back out
+// (both factors powers of two, so nothing rounds).  128 threads, 128 / N per
+// row, each over every (128 / N)-th 16-byte chunk of its row.
 template <int D, int N, int QBlock>
-__device__ __forceinline__ void convert_q_e4m3(uint8_t *s_q, float *qscale, float scale_log2,
-                                               int t) {
+__device__ __forceinline__ void convert_q_f16(uint8_t *s_q, float *qscale, float scale_log2,
+                                              int t) {
     constexpr int kTpr = 128 / N;
-    constexpr int kCh = 16 / kTpr;   // 16-byte bf16 chunks per thread per 128-d block
     const int r = t / kTpr, j = t % kTpr;
+    uint8_t *row = s_q + r * 128;
     const int sw = r & 7;
     uint32_t amax = 0;   // |q| bits; ordered like the values for non-NaN inputs
 #pragma unroll
     for (int ch = j; ch < D / 8; ch += kTpr) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(s_q + (ch / 8) * QBlock + r * 128 +
+        const uint4 v = *reinterpret_cast<const uint4 *>(row + (ch / 8) * QBlock +
                                                          (((ch % 8) ^ sw) << 4));
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -488,32 +425,17 @@ __device__ __forceinline__ void convert_q_e4m3(uint8_t *s_q, float *qscale, floa
 #pragma unroll
     for (int o = 1; o < kTpr; o <<= 1) amax = max(amax, __shfl_xor_sync(kFull, amax, o));
     // floor(log2 amax) for a normal amax; zero or subnormal rows take s = 100
-    int s = 7 - ((int)(amax >> 23) - 127);
+    int s = 14 - ((int)(amax >> 23) - 127);
     s = s < -100 ? -100 : (s > 100 ? 100 : s);
     const float up = __int_as_float((127 + s) << 23);
 #pragma unroll
-    for (int b8 = 0; b8 < D / 128; ++b8) {
-        uint4 v[kCh];
-#pragma unroll
-        for (int i = 0; i < kCh; ++i) {
-            const int ch = j + i * kTpr;   // 8 values at d = 128 b8 + 8 ch
-            v[i] = *reinterpret_cast<const uint4 *>(s_q + (2 * b8 + ch / 8) * QBlock + r * 128 +
-                                                    (((ch % 8) ^ sw) << 4));
-        }
-        named_bar_softmax();   // the block is read before any thread rewrites it
-        uint8_t *blk = s_q + b8 * 2 * QBlock;
-#pragma unroll
-        for (int i = 0; i < kCh; ++i) {
-            const int ch = j + i * kTpr;
-            const float x[8] = {bf16lo(v[i].x) * up, bf16hi(v[i].x) * up, bf16lo(v[i].y) * up,
-                                bf16hi(v[i].y) * up, bf16lo(v[i].z) * up, bf16hi(v[i].z) * up,
-                                bf16lo(v[i].w) * up, bf16hi(v[i].w) * up};
-            uint2 hi, lo;
-            e4m3_split8(x, hi, lo);
-            const int off = (((ch >> 1) ^ sw) << 4) + 8 * (ch & 1);
-            *reinterpret_cast<uint2 *>(blk + r * 128 + off) = hi;
-            *reinterpret_cast<uint2 *>(blk + (N + r) * 128 + off) = lo;
-        }
+    for (int ch = j; ch < D / 8; ch += kTpr) {
+        uint4 *a = reinterpret_cast<uint4 *>(row + (ch / 8) * QBlock + (((ch % 8) ^ sw) << 4));
+        const uint4 v = *a;
+        *a = make_uint4(f16x2_rn(bf16lo(v.x) * up, bf16hi(v.x) * up),
+                        f16x2_rn(bf16lo(v.y) * up, bf16hi(v.y) * up),
+                        f16x2_rn(bf16lo(v.z) * up, bf16hi(v.z) * up),
+                        f16x2_rn(bf16lo(v.w) * up, bf16hi(v.w) * up));
     }
     if (j == 0) qscale[r] = scale_log2 * __int_as_float((127 - s) << 23);
 }
@@ -538,12 +460,12 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity,
                                               volatile int *abort_flag, int *dev_status) {
     if (tc::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = tc::globaltimer_ns();
-    while (true) {
+    for (uint32_t round = 1;; ++round) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (tc::mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (tc::globaltimer_ns() - t0 > 2000000000ull) {
+        if (tc::wait_expired(t0, round, 2000000000ull)) {
             *abort_flag = 1;
             set_status(dev_status, CARAT_DEV_TIMEOUT);
             return false;
@@ -626,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     uint64_t *fin = s_full + 6;
     uint64_t *raw_full = s_full + 7;     // [NR] FP8: e4m3 stage landed
     uint64_t *raw_empty = raw_full + NR; // [NR] FP8: e4m3 stage converted
-    uint64_t *q_conv = raw_empty + NR;   // FP8: Q rewritten as e4m3 high and low parts
+    uint64_t *q_conv = raw_empty + NR;   // FP8: Q rewritten as f16
     uint8_t *s_raw = smem + L::kOffRaw;
     SkShared *sk = reinterpret_cast<SkShared *>(smem + L::kOffMisc);
     volatile int *abort_flag = &sk->abort_flag;
@@ -646,6 +568,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     Segment ps{};
     bool p_have = false, p_qdone = false, alive_p = true;
     int ppart = 0, pks = 0, psi = 0;
+    uint32_t qcnt = 0;   // Q copies issued
     uint32_t cnt = 0;
     uint64_t pol = 0;
     // Paged caches: the page-table entries of the two pages last used and one
@@ -696,6 +619,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     tc::tma_load_4d(s_q + db * L::kQBlock, &maps.q, db * 64, ps.c * p.group,
                                     ps.rg * plan.pos_per_group, ps.b, q_full, pol);
                 p_qdone = true;
+                ++qcnt;
             }
             const int n = ps.x1 - ps.x0;
             int x;
@@ -834,16 +758,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
             if (p.fused) tc::tma_prefetch_map(&maps.vnew);
             for (int i = 0; i < NS; ++i) {
                 // bf16 stage filled by TMA (one arrival with its bytes), or
-                // with FP8 caches (V rows only) by the 128 converting threads
+                // with FP8 caches by the 128 converting threads
                 tc::mbar_init(&full[i], F8 ? 128 : 1);
                 tc::mbar_init(&empty[i], 1);
             }
             for (int i = 0; i < NR; ++i) {
                 tc::mbar_init(&raw_full[i], 1);
-                // released once by the MMA thread: a K stage by the commit of
-                // its QK product, a V stage once its f16 copy is complete, a
-                // special stage by the commit of its PV product
-                tc::mbar_init(&raw_empty[i], 1);
+                tc::mbar_init(&raw_empty[i], 128);
             }
             tc::mbar_init(&s_full[0], 1);
             tc::mbar_init(&s_full[1], 1);
@@ -889,32 +810,33 @@ __global__ void __launch_bounds__(kThreads, MINB)
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = sk->tmem_slot;
-    // O^T buffer of segment si: KS blocks of N columns (S^T buffers: 0, kSCols)
+    // O^T buffer of segment si: KS blocks of N columns (S^T buffers: 0, N)
     auto tmem_o_of = [&](int si) -> uint32_t {
-        return tmem + 2 * L::kSCols + (L::kDoubleO ? (uint32_t)(si & 1) : 0u) * KS * N;
+        return tmem + 2 * N + (L::kDoubleO ? (uint32_t)(si & 1) : 0u) * KS * N;
     };
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             produce(0xffffffffu, false);
-            if (!alive_p) {
-                // Wait (bounded) for the copies already issued before leaving.
-                if constexpr (F8) {
-                    for (uint32_t x = cnt > (uint32_t)NR ? cnt - NR : 0; x < cnt; ++x)
-                        tc::mbar_wait(&raw_full[x % NR], (x / NR) & 1, 100000000ull);
-                } else {
-                    for (uint32_t x = cnt > (uint32_t)NS ? cnt - NS : 0; x < cnt; ++x)
-                        tc::mbar_wait(&full[x % NS], (x / NS) & 1, 100000000ull);
-                }
+            // Wait (bounded) for the last copies issued (the stage ring holds
+            // every copy still in flight): none may land in shared memory after
+            // this CTA is gone, also when a consumer stopped early.  After a
+            // normal run they have all landed and the waits return at once.
+            if (qcnt > 0) tc::mbar_wait(q_full, (qcnt - 1) & 1, 100000000ull);
+            if constexpr (F8) {
+                for (uint32_t x = cnt > (uint32_t)NR ? cnt - NR : 0; x < cnt; ++x)
+                    tc::mbar_wait(&raw_full[x % NR], (x / NR) & 1, 100000000ull);
+            } else {
+                for (uint32_t x = cnt > (uint32_t)NS ? cnt - NS : 0; x < cnt; ++x)
+                    tc::mbar_wait(&full[x % NS], (x / NS) & 1, 100000000ull);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            // FP8 caches: QK in e4m3 (K straight from the raw stages, Q as high
-            // and low parts: 2N columns), PV in f16; else both in bf16.
-            constexpr uint32_t idesc_qk = F8 ? tc::idesc_e4m3_f32(128, 2 * N)
+            // FP8 caches compute with f16 operands (K, V, Q and P), else bf16.
+            constexpr uint32_t idesc_qk = F8 ? tc::idesc_f16_f32(128, N, false, false)
                                              : tc::idesc_bf16_f32(128, N, false, false);
             constexpr uint32_t idesc_pv = F8 ? tc::idesc_f16_f32(128, N, true, false)
                                              : tc::idesc_bf16_f32(128, N, true, false);
@@ -924,8 +846,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
             it.init(p, sk);
             Segment sg;
             bool alive = true;
-            uint32_t mcnt = 0, gt = 0;   // 16-bit stages consumed, tiles before this segment
-            uint32_t rbase = 0;          // FP8: raw stages of the segments before this one
+            uint32_t mcnt = 0, gt = 0;   // stages consumed, tiles before this segment
             int si = 0;
             while (alive && it.next(p, upr, plan.row_groups, sg)) {
                 const int n = sg.x1 - sg.x0;
@@ -935,47 +856,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 }
                 tc::tc_fence_after();
                 const uint32_t tmem_o = tmem_o_of(si);
-                int spec_stage = 0;   // stage holding the special tile's (K and) V rows
-                uint32_t spec_raw = 0;   // FP8: raw stage of the special tile
+                int spec_stage = 0;   // stage holding the special tile's K and V rows
                 const bool sp0 = order_tile(sg, sg.x0) == sg.special;   // segment leads with it
-                const int xs = sp0 ? 0 : -1;
                 for (int step = 0; step <= n && alive; ++step) {
                     if (step < n) {
                         // S^T[tile & 1] = K_tile . Q^T over D in steps of 16
-                        const uint32_t tmem_s = tmem + ((gt + step) & 1) * L::kSCols;
-                        if constexpr (F8) {
-                            // S^T = [K . Qhi^T | K . Qlo^T] from the raw e4m3 stages
-                            // (K-major, 128 d each, 32 d per product).  A special
-                            // stage holds 16 K rows per 128-d block, 2 KB apart;
-                            // key rows past 16 read other bytes and are masked.
-                            const bool spx = order_tile(sg, sg.x0 + step) == sg.special;
-                            const uint32_t r0 =
-                                rbase + seg_stages_before(step == 0 ? 0 : 2 * step - 1, n, xs, KS);
-#pragma unroll 1
-                            for (int ks = 0; ks < KS; ++ks) {
-                                const uint32_t rc = spx ? r0 : r0 + ks;
-                                const int r = rc % NR;
-                                if (ks == 0 || !spx) {
-                                    if (!wait_or_abort(&raw_full[r], (rc / NR) & 1, abort_flag,
-                                                       p.dev_status)) {
-                                        alive = false;
-                                        break;
-                                    }
-                                    tc::tc_fence_after();
-                                }
-                                const uint32_t abase = tc::smem_u32(s_raw + r * L::kRawBytes) +
-                                                       (spx ? ks * kDispRows * 128 : 0);
-#pragma unroll
-                                for (int kk = 0; kk < 4; ++kk) {
-                                    const uint64_t a = tc::sdesc_sw128(abase + kk * 32, 16, 1024);
-                                    const uint64_t q = tc::sdesc_sw128(
-                                        q_base + ks * 2 * L::kQBlock + kk * 32, 16, 1024);
-                                    tc::mma_e4m3_ss(tmem_s, a, q, idesc_qk, (ks | kk) != 0);
-                                }
-                                if (!spx) tc::mma_commit(&raw_empty[r]);
-                            }
-                            if (spx) spec_raw = r0;   // released after the tile's PV product
-                        } else if (order_tile(sg, sg.x0 + step) == sg.special) {
+                        const uint32_t tmem_s = tmem + ((gt + step) & 1) * N;
+                        if (order_tile(sg, sg.x0 + step) == sg.special) {
                             // 16 K rows per 64-d box, 2 KB apart; key rows past
                             // 16 read other rows of the stage and are masked.
                             const int s = mcnt % NS;
@@ -1000,7 +887,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                             spec_stage = s;   // released after the tile's PV product
                             ++mcnt;
                         }
-                        for (int ks = 0; ks < KS && alive && !F8 &&
+                        for (int ks = 0; ks < KS && alive &&
                                          order_tile(sg, sg.x0 + step) != sg.special;
                              ++ks) {
                             const int s = mcnt % NS;
@@ -1047,18 +934,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
                         }
                         tc::tc_fence_after();
                         const bool special = order_tile(sg, sg.x0 + x) == sg.special;
-                        if (F8 && special) {
-                            // FP8: the special tile's V rows have their own f16 stage.
-                            const int s = mcnt % NS;
-                            if (!wait_or_abort(&full[s], (mcnt / NS) & 1, abort_flag,
-                                               p.dev_status)) {
-                                alive = false;
-                                break;
-                            }
-                            tc::tc_fence_after();
-                            spec_stage = s;
-                            ++mcnt;
-                        }
                         if (special) {
                             // The 16 keys of the special tile: one K=16 product per
                             // 128-d block; V boxes of 16 rows follow the K boxes.
@@ -1072,7 +947,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
                                 tc::mma_bf16_ss(tmem_o + vs * N, a, pp, idesc_pv, x > 0);
                             }
                             tc::mma_commit(&empty[spec_stage]);
-                            if constexpr (F8) tc::mma_commit(&raw_empty[spec_raw % NR]);
                         }
                         for (int vs = 0; vs < KS && alive && !special; ++vs) {
                             const int s = mcnt % NS;
@@ -1082,13 +956,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
                                 break;
                             }
                             tc::tc_fence_after();
-                            if constexpr (F8) {
-                                // every converting thread has read this stage's raw
-                                // copy: its raw slot is free
-                                const uint32_t rv =
-                                    rbase + seg_stages_before(v_part(x, n), n, xs, KS) + vs;
-                                tc::mbar_arrive(&raw_empty[rv % NR]);
-                            }
                             const uint32_t base = tc::smem_u32(smem + s * kStageBytes);
 #pragma unroll
                             for (int kk = 0; kk < 8; ++kk) {
@@ -1107,7 +974,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     }
                 }
                 gt += n;
-                if constexpr (F8) rbase += seg_stages_before(2 * n, n, xs, KS);
                 ++si;
             }
             if (!alive) {
@@ -1127,8 +993,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         bool alive = true;
         uint32_t gt = 0, cnt_base = 0;       // tiles and stages before this segment
         int si = 0;                          // segments before this one
-        uint32_t ccnt = 0;                   // FP8: raw stages passed so far (load order)
-        uint32_t fcnt = 0;                   // FP8: f16 stages written so far
+        uint32_t ccnt = 0;                   // FP8: stages converted so far
         float *s_mrow = red + 12 * N;        // a finished segment's row maxima
         float *s_lrow = red + 13 * N;        // and row sums
         float *s_qscale = red + 14 * N;      // FP8: this segment's row score scales
@@ -1244,13 +1109,18 @@ __global__ void __launch_bounds__(kThreads, MINB)
             // segment): its K part takes one stage and its V part none.
             const int xs = (sg.special >= 0 && sg.x0 == 0) ? 0 : -1;
             // Stages the producer issued for the segment's parts before part P.
-            auto stages_before = [&](int P) -> uint32_t { return seg_stages_before(P, n, xs, KS); };
-            // FP8: walk the segment's raw stages in load order until `target`
-            // of them are passed, widening the V ones into f16 stages (K
-            // stages feed the tensor core as they are).  Thread t converts key
-            // row t (rows t < 16 of a special stage, whose V rows follow its
-            // K rows); rows of keys that hold no token (zero_v) are written as
-            // zeros.  Returns false on a timeout.
+            auto stages_before = [&](int P) -> uint32_t {
+                uint32_t st = (uint32_t)P * KS;
+                if (xs >= 0) {
+                    if ((xs == 0 ? 0 : 2 * xs - 1) < P) st -= KS - 1;
+                    if (v_part(xs, n) < P) st -= KS;
+                }
+                return st;
+            };
+            // FP8: convert the segment's raw stages, in load order, until
+            // `target` stages are done.  Thread t converts key row t (rows
+            // t < 16 of a special tile); V rows of keys that hold no token
+            // (zero_v) are written as zeros.  Returns false on a timeout.
             int cv_part = 0, cv_pks = 0;
             auto convert_through = [&](uint32_t target, bool zero_v) -> bool {
                 if constexpr (F8) {
@@ -1272,16 +1142,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
                             ++cv_part;
                             continue;
                         }
-                        if (!special && !is_v) {
-                            ++ccnt;
-                            if (++cv_pks == KS) {
-                                cv_pks = 0;
-                                ++cv_part;
-                            }
-                            continue;
-                        }
-                        const int sidx = fcnt % NS, r = ccnt % NR;
-                        if (fcnt >= NS && !wait_or_abort(&empty[sidx], ((fcnt / NS) & 1) ^ 1,
+                        const int sidx = ccnt % NS, r = ccnt % NR;
+                        if (ccnt >= NS && !wait_or_abort(&empty[sidx], ((ccnt / NS) & 1) ^ 1,
                                                          abort_flag, p.dev_status))
                             return false;
                         if (!wait_or_abort(&raw_full[r], (ccnt / NR) & 1, abort_flag, p.dev_status))
@@ -1289,48 +1151,50 @@ __global__ void __launch_bounds__(kThreads, MINB)
                         const uint8_t *raw = s_raw + r * L::kRawBytes;
                         uint8_t *stg = smem + sidx * kStageBytes;
                         if (special) {
-                            // 16 displaced V rows (after the K rows, 2 KB per 128-d
-                            // block) into the stage's V boxes of 16 rows
+                            // 16 displaced rows: K slabs then V slabs (2 KB each)
                             if (t < kDispRows) {
                                 const long long pos = ctx - p.window + 1 + t;
                                 const bool valid = t < p.k - 1 && pos >= 0;
 #pragma unroll
-                                for (int sl = 0; sl < D / 128; ++sl)
+                                for (int sl = 0; sl < D / 128; ++sl) {
+                                    convert_row(raw + sl * 2048 + t * 128,
+                                                stg + (2 * sl) * kDispBoxBytes + t * 128,
+                                                stg + (2 * sl + 1) * kDispBoxBytes + t * 128, t,
+                                                false);
                                     convert_row(raw + (D / 128 + sl) * 2048 + t * 128,
                                                 stg + (D / 64 + 2 * sl) * kDispBoxBytes + t * 128,
                                                 stg + (D / 64 + 2 * sl + 1) * kDispBoxBytes + t * 128,
                                                 t, !valid);
+                                }
                             }
                             ++cv_part;
                         } else {
                             convert_row(raw + t * 128, stg + t * 128, stg + kBoxBytes + t * 128, t,
-                                        zero_v);
+                                        is_v && zero_v);
                             if (++cv_pks == KS) {
                                 cv_pks = 0;
                                 ++cv_part;
                             }
                         }
                         tc::fence_proxy_async_smem();
+                        tc::mbar_arrive(&raw_empty[r]);
                         tc::mbar_arrive(&full[sidx]);
-                        ++fcnt;
                         ++ccnt;
                     }
                 }
                 return true;
             };
             if constexpr (F8) {
-                // This segment's Q as e4m3 high and low parts once its copy has
-                // landed (the decision is taken by all 128 threads together:
-                // the conversion has barriers of its own); then the MMA warp
-                // may start the segment's products.
-                const bool q_ok = wait_or_abort(q_full, si & 1, abort_flag, p.dev_status);
+                // This segment's Q as f16 once its copy has landed; then the
+                // MMA warp may start the segment's products.
+                const bool q_ok =
+                    __all_sync(kFull, wait_or_abort(q_full, si & 1, abort_flag, p.dev_status));
+                if (q_ok) convert_q_f16<D, N, L::kQBlock>(s_q, s_qscale, p.scale_log2, t);
+                tc::fence_proxy_async_smem();
                 if (named_bar_softmax_any(!q_ok || *abort_flag)) {
                     alive = false;
                     break;
                 }
-                convert_q_e4m3<D, N, L::kQBlock>(s_q, s_qscale, p.scale_log2, t);
-                tc::fence_proxy_async_smem();
-                named_bar_softmax();   // the row scales are read by every thread
                 tc::mbar_arrive(q_conv);
             }
             float m_run[N], l_part[N];
@@ -1343,12 +1207,22 @@ __global__ void __launch_bounds__(kThreads, MINB)
             for (; idx < n; ++idx) {
                 const uint32_t tile = gt + idx;
                 const int i = order_tile(sg, sg.x0 + idx);
+                if constexpr (F8) {
+                    // K of this tile and the next, before their QK products
+                    // (When the stage ring holds one K tile only, the stage of a
+                    // special tile is free again only after its PV product, which
+                    // waits for this tile's P: no look-ahead past it.)
+                    const int xk = (idx + 1 < n && !(NS == KS && idx == xs)) ? idx + 1 : idx;
+                    if (!convert_through(cnt_base + stages_before((xk == 0 ? 0 : 2 * xk - 1) + 1),
+                                         false))
+                        alive = false;
+                }
                 // warp-uniform: the TMEM load below is warp-collective
                 const bool w_ok = __all_sync(kFull, alive && wait_or_abort(&s_full[tile & 1],
                                                                            (tile >> 1) & 1,
                                                                            abort_flag,
                                                                            p.dev_status));
-                const uint32_t tmem_s = tmem + (tile & 1) * L::kSCols;
+                const uint32_t tmem_s = tmem + (tile & 1) * N;
                 float x[N];
                 if (w_ok) {
                     tc::tc_fence_after();
@@ -1356,19 +1230,9 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     for (int cb = 0; cb < N / 16; ++cb) {
                         uint32_t r16[16];
                         tc::tmem_ld16(tmem_s + lane_off + cb * 16, r16);
-                        if constexpr (F8) {
-                            // the product with the low parts of Q, N columns on
-                            uint32_t l16[16];
-                            tc::tmem_ld16(tmem_s + lane_off + N + cb * 16, l16);
-                            tc::tmem_ld_wait();
+                        tc::tmem_ld_wait();
 #pragma unroll
-                            for (int e = 0; e < 16; ++e)
-                                x[cb * 16 + e] = __uint_as_float(r16[e]) + __uint_as_float(l16[e]);
-                        } else {
-                            tc::tmem_ld_wait();
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) x[cb * 16 + e] = __uint_as_float(r16[e]);
-                        }
+                        for (int e = 0; e < 16; ++e) x[cb * 16 + e] = __uint_as_float(r16[e]);
                     }
                 } else {
 #pragma unroll
@@ -1457,7 +1321,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
                                                             p.dev_status));
                     tc::tc_fence_after();
                 }
-                bool v_zero = false;   // FP8: key t's V row is widened as zeros
                 if (alive) {
                     // P^T as a K-major operand: row r, key t (two 64-key blocks).
                     uint8_t *pblk = s_p + (t / 64) * L::kPBlock;
@@ -1496,7 +1359,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
                         (ring && ((long long)(i + 1) * kTileKeys >
                                   min((long long)p.window, held_tokens))) ||
                         (!ring && (long long)(i + 1) * kTileKeys > held_tokens);
-                    v_zero = tile_partial && !ki.data;
                     // Fused append into a ring: the one CTA that loads tile i
                     // overwrites slots of the tile once its own copies of the
                     // tile have landed.
@@ -1509,7 +1371,13 @@ __global__ void __launch_bounds__(kThreads, MINB)
                         }
                     }
                     if constexpr (F8) {
-                        // (V is widened below, once P is published.)
+                        // V of this tile, its no-token rows as zeros (a special
+                        // tile's V rows were converted with its K rows; going on
+                        // to the parts after it here could wait on its own PV)
+                        if (idx != xs &&
+                            !convert_through(cnt_base + stages_before(v_part(idx, n) + 1),
+                                             tile_partial && !ki.data))
+                            alive = false;
                     } else if (idx == xs) {
                         // The special tile's stage: zero its V rows that hold no
                         // token (only the 16 rows its PV product reads).
@@ -1556,15 +1424,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
                     break;
                 }
                 tc::mbar_arrive(p_full);
-                if constexpr (F8) {
-                    // V of this tile, its no-token rows as zeros (a special tile:
-                    // the V rows of its one stage, and nothing after it, whose K
-                    // rows may wait on this tile's PV product).  After P: the PV
-                    // product of one f16 stage frees it for the next.
-                    const uint32_t vt = idx == xs ? cnt_base + 1
-                                                  : cnt_base + stages_before(v_part(idx, n) + 1);
-                    if (!convert_through(vt, v_zero)) alive = false;
-                }
                 if (p.fused_write && (ring || sg.rg == 0)) {
                     // Write this step's rows whose slot this tile covers (ring), or
                     // that no loaded tile covers, or every row (cache), from the new
@@ -1709,7 +1568,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
 template <int D>
 __global__ void __launch_bounds__(D / 4) attn_fixup_kernel(const AttnParams p, int upr,
                                                             int row_groups, int pos_per_group,
-                                                            int slot_rows) {
+                                                            int slot_rows, int slots) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int u = blockIdx.x, r = blockIdx.y;   // unit, row within its row group
     const int b = u / upr, ur = u % upr;
@@ -1727,8 +1586,16 @@ __global__ void __launch_bounds__(D / 4) attn_fixup_kernel(const AttnParams p, i
     if (nt == 0) return;                          // whole: already written
     const long long u0 = (long long)(unsigned)e.x | ((long long)e.y << 32);
     const long long len = e.w;
-    const long long g_first = u0 / len;
-    const int np = (int)((u0 + nt - 1) / len - g_first + 1);
+    // An entry the attention grid did not write this time (it stopped on a
+    // timeout before reaching the unit) is not used: its pieces could lie
+    // outside the workspace.
+    const long long g_first = len >= 1 && u0 >= 0 && nt > 0 ? u0 / len : -1;
+    const long long g_last = g_first >= 0 ? (u0 + nt - 1) / len : -1;
+    if (g_first < 0 || g_last >= slots || g_last - g_first + 1 > kMaxPieces) {
+        if (threadIdx.x == 0) set_status(p.dev_status, CARAT_DEV_TIMEOUT);
+        return;
+    }
+    const int np = (int)(g_last - g_first + 1);
     auto piece_base = [&](int q) -> size_t {
         const long long gq = g_first + q;
         return ((size_t)gq * 2 + (u0 > gq * len ? 1 : 0)) * slot_rows;
@@ -1821,7 +1688,7 @@ cudaError_t launch_tc(const AttnParams &p, const TcPlan &plan, const TcMaps &map
     cfg.numAttrs = 1;
     const int upr = p.kv_heads * plan.row_groups;
     e = cudaLaunchKernelEx(&cfg, attn_fixup_kernel<D>, p, upr, plan.row_groups,
-                           plan.pos_per_group, N);
+                           plan.pos_per_group, N, grid);
     count_launches(1);
     return e;
 }
@@ -1836,7 +1703,7 @@ int tc_rows_per_tile(int group, int k) {
 }
 
 int tc_ctas_per_sm(int head_dim, int rows_per_tile, bool fp8) {
-    return (head_dim == 256 && rows_per_tile == 16) ? 2 : 1;
+    return (!fp8 && head_dim == 256 && rows_per_tile == 16) ? 2 : 1;
 }
 
 bool tc_fp8_supported(int head_dim, int group, int k) {
@@ -1898,11 +1765,8 @@ cudaError_t launch_attention_tc(const AttnParams &p, int grid, bool unit_mode, b
         const uint32_t boxq[4] = {64, (uint32_t)p.group, (uint32_t)plan.pos_per_group, 1};
         if (!make_bf16_tensor_map(&maps.q, p.q, 4, dimsq, stridesq, boxq, true))
             return cudaErrorInvalidValue;
-        // 16 rows: two CTAs per SM, each with 2 f16 V stages and 2 raw stages
-        // (measured: 103 us on the mixed step's sliding layer, against 107 us
-        // with one f16 stage and 4 raw stages); else one CTA per SM with 3 f16
-        // stages and 6 (or 4) raw stages
-        if (n == 16) return launch_tc<256, 16, 2, 2, 2>(p, plan, maps, grid, stream);
+        // one CTA per SM: 3 f16 stages and 6 (or 4) raw stages in flight
+        if (n == 16) return launch_tc<256, 16, 3, 1, 6>(p, plan, maps, grid, stream);
         if (n == 32) return launch_tc<256, 32, 3, 1, 6>(p, plan, maps, grid, stream);
         return launch_tc<256, 64, 3, 1, 4>(p, plan, maps, grid, stream);
     }

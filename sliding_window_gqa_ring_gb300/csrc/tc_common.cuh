@@ -55,17 +55,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Whether a bounded wait that began at t0 and has made `rounds` rounds of
+// polls has run out.  The elapsed time is a signed difference, so a global
+// timer that steps backwards cannot end a wait early (an unsigned difference
+// would wrap to a huge value); a wait also needs kMinRounds rounds before the
+// timer is believed, and ends after kMaxRounds whatever the timer says.
+constexpr uint32_t kMinRounds = 1u << 12;
+constexpr uint32_t kMaxRounds = 1u << 24;
+__device__ __forceinline__ bool wait_expired(uint64_t t0, uint32_t rounds, uint64_t limit_ns) {
+    if (rounds >= kMaxRounds) return true;
+    const long long dt = (long long)(globaltimer_ns() - t0);
+    return rounds >= kMinRounds && dt > (long long)limit_ns;
+}
+
 // Wait until the barrier's phase with parity `parity` has completed.  Returns
 // false (and never hangs) if that takes longer than timeout_ns of wall time.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           uint64_t timeout_ns = 2000000000ull) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    while (true) {
+    for (uint32_t round = 1;; ++round) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > timeout_ns) return false;
+        if (wait_expired(t0, round, timeout_ns)) return false;
     }
 }
 
@@ -169,18 +182,6 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
-// D (+)= A . B with 8-bit operands: kind::f8f6f4 (the formats are in the
-// instruction descriptor; K = 32 elements, 32 bytes of each row, per product).
-__device__ __forceinline__ void mma_e4m3_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // Arrive (once) on `bar` when every tcgen05 operation this thread issued so
 // far has completed.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
@@ -259,12 +260,6 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn_maj
                                                      bool b_mn_major) {
     return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-// kind::f8f6f4 with e4m3 A and B (format fields 0), both K-major, fp32
-// accumulator.
-__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
-    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // Byte offset of element (row, col) of a K-major bf16 tile stored as 128-byte

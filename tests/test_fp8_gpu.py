@@ -7,10 +7,10 @@ calls it lossy, outside the bit-exact comparison.  Here:
     quantiser bit for bit (integer work: exact);
   * the attention output equals the oracle's attention of the DEQUANTISED
     history (e4m3 value x scale) within the same tolerance as the bf16 path
-    (gpu_harness): the kernel multiplies the e4m3 keys with the queries split
-    into e4m3 high and low parts (exact for every element within 2^-9 of its
-    row's largest), widens V to f16 exactly and rounds P to f16, so its
-    arithmetic error stays within the bf16 path's;
+    (gpu_harness): the kernel widens K and V to f16 exactly, converts each
+    query row to f16 after a power-of-two scale (exact for every element
+    within 2^-28 of the row's largest) and rounds P to f16, so its arithmetic
+    error stays within the bf16 path's;
   * the FP8 output differs from the oracle's attention of the UNQUANTISED
     bf16 history by about what the oracle itself computes for the
     quantisation (the test's own tolerance: the oracle's quantisation effect
