@@ -393,10 +393,15 @@ class DecodeStep:
     run()        -- every layer's fused append+attention on the current stream
                     (inputs already on the device).
     run_from_host(host_inputs, host_outputs)
-                 -- the same step from pinned host buffers: all layers' inputs
-                    are copied on a separate copy stream up front, each layer
-                    waits only for its own inputs, and each layer's output is
-                    copied back while the next layer computes.
+                 -- the same step from pinned host buffers: the inputs are
+                    copied in on one stream and the outputs out on another,
+                    into two sets of device buffers that alternate between
+                    calls, so one step's inputs stream in while the step before
+                    computes and its outputs stream out while the next one
+                    computes; each layer waits only for its own inputs.  The
+                    layers run in order on the current stream (they update the
+                    rings and caches).  finish() makes the current stream wait
+                    for the last call's outputs.
     capture() / replay()
                  -- record run() once into a CUDA graph and replay it (one
                     launch of the whole step from the host).
@@ -411,34 +416,64 @@ class DecodeStep:
         self.outputs = outputs or [torch.empty(q.shape, dtype=torch.float32, device=q.device)
                                    for (q, _, _, _) in self.inputs]
         self.device = self.inputs[0][0].device
-        self.copy_stream = torch.cuda.Stream(device=self.device)
+        self.copy_stream = torch.cuda.Stream(device=self.device)      # host -> device
+        self.copy_out_stream = torch.cuda.Stream(device=self.device)  # device -> host
         self.graph = None
-        self._in_ready = [torch.cuda.Event() for _ in self.layers]
-        self._out_ready = [torch.cuda.Event() for _ in self.layers]
+        # run_from_host: two sets of device buffers (set 0 is inputs/outputs);
+        # per set, when compute is done with its inputs and the copy-out stream
+        # with its outputs
+        self._sets = [(self.inputs, self.outputs), None]
+        self._calls = 0
+        self._in_ready = [[torch.cuda.Event() for _ in self.layers] for _ in range(2)]
+        self._out_ready = [[torch.cuda.Event() for _ in self.layers] for _ in range(2)]
+        self._in_free = [None, None]
+        self._out_free = [None, None]
 
     def run(self, stream=None):
+        if self._calls and not torch.cuda.is_current_stream_capturing():
+            # outputs[] is also a run_from_host staging set: its copy out first
+            s = stream if stream is not None else torch.cuda.current_stream(self.device)
+            s.wait_stream(self.copy_out_stream)
         for layer, (q, kn, vn, ctx), out in zip(self.layers, self.inputs, self.outputs):
             layer.step(q, kn, vn, ctx, out=out, stream=stream)
         return self.outputs
 
     def run_from_host(self, host_inputs, host_outputs):
         compute = torch.cuda.current_stream(self.device)
-        self.copy_stream.wait_stream(compute)
+        k = self._calls & 1
+        self._calls += 1
+        if self._sets[k] is None:
+            self._sets[k] = ([tuple(torch.empty_like(x) for x in din) for din in self.inputs],
+                             [torch.empty_like(o) for o in self.outputs])
+        dins, douts = self._sets[k]
+        # inputs in, once compute is done with this set's previous inputs
+        if self._in_free[k] is not None:
+            self.copy_stream.wait_event(self._in_free[k])
         with torch.cuda.stream(self.copy_stream):
-            for i, (hin, din) in enumerate(zip(host_inputs, self.inputs)):
+            for i, (hin, din) in enumerate(zip(host_inputs, dins)):
                 for src, dst in zip(hin, din):
                     dst.copy_(src, non_blocking=True)
-                self._in_ready[i].record(self.copy_stream)
-        for i, (layer, (q, kn, vn, ctx), out) in enumerate(
-                zip(self.layers, self.inputs, self.outputs)):
-            compute.wait_event(self._in_ready[i])
+                self._in_ready[k][i].record(self.copy_stream)
+        # this set's previous outputs must be out before they are overwritten
+        if self._out_free[k] is not None:
+            compute.wait_event(self._out_free[k])
+        for i, (layer, (q, kn, vn, ctx), out) in enumerate(zip(self.layers, dins, douts)):
+            compute.wait_event(self._in_ready[k][i])
             layer.step(q, kn, vn, ctx, out=out)
-            self._out_ready[i].record(compute)
-            self.copy_stream.wait_event(self._out_ready[i])
-            with torch.cuda.stream(self.copy_stream):
+            self._out_ready[k][i].record(compute)
+            self.copy_out_stream.wait_event(self._out_ready[k][i])
+            with torch.cuda.stream(self.copy_out_stream):
                 host_outputs[i].copy_(out, non_blocking=True)
-        compute.wait_stream(self.copy_stream)
+        self._in_free[k] = torch.cuda.Event()
+        self._in_free[k].record(compute)
+        self._out_free[k] = torch.cuda.Event()
+        self._out_free[k].record(self.copy_out_stream)
         return host_outputs
+
+    def finish(self):
+        """Make the current stream wait until the host outputs of every
+        run_from_host call so far have been written."""
+        torch.cuda.current_stream(self.device).wait_stream(self.copy_out_stream)
 
     def capture(self):
         """Record run() into a CUDA graph (after at least one eager run, so

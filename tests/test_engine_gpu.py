@@ -56,10 +56,21 @@ def test_eager_graph_and_host_paths_agree(orc):
     step.capture()
     replayed = [o.clone() for o in step.replay()]
     h_in = [tuple(x.cpu().pin_memory() for x in din) for din in step.inputs]
-    h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in step.outputs]
-    step.run_from_host(h_in, h_out)
+    # three host-path steps back to back: both device staging sets, and the
+    # first set again once its previous outputs have been copied out
+    h_outs = [[torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in step.outputs]
+              for _ in range(3)]
+    for h_out in h_outs:
+        step.run_from_host(h_in, h_out)
+    step.finish()
     torch.cuda.synchronize()
-    for a, b_, c in zip(eager, replayed, h_out):
-        assert torch.equal(a, b_)
-        assert torch.equal(a.cpu(), c)
+    for h_out in h_outs:
+        for a, b_, c in zip(eager, replayed, h_out):
+            assert torch.equal(a, b_)
+            assert torch.equal(a.cpu(), c)
+    # and the device path after the host path
+    again = [o.clone() for o in step.run()]
+    torch.cuda.synchronize()
+    for a, d in zip(eager, again):
+        assert torch.equal(a, d)
     assert carat.carat_get_device_status(clear=True) == 0
