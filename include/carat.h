@@ -432,6 +432,17 @@ size_t carat_global_workspace_bytes(int batch, int proposal_count, int q_heads,
  */
 carat_status carat_get_device_status(int32_t *host_out, int clear, void *stream);
 
+/*
+ * Self-check of the bounded waits every kernel of this library uses: a
+ * one-thread kernel waits on a barrier phase that nothing completes, gives up
+ * after `limit_ns` nanoseconds (and a minimum number of polls), sets
+ * CARAT_DEV_TIMEOUT in the current device's status word and returns; the
+ * context stays usable.  limit_ns must lie in [1e6, 1e10] (1 ms .. 10 s), else
+ * CARAT_ERR_INVALID_ARG.  Enqueued on `stream` (read the result with
+ * carat_get_device_status); CARAT_ERR_CUDA if the launch fails.
+ */
+carat_status carat_check_bounded_wait(uint64_t limit_ns, void *stream);
+
 /* Static English text for a status code. */
 const char *carat_status_string(carat_status status);
 

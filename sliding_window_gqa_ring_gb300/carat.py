@@ -31,6 +31,7 @@ CARAT_ERR_WORKSPACE = 3
 CARAT_ERR_CUDA = 4
 CARAT_DEV_BAD_CONTEXT = 0x1
 CARAT_DEV_BAD_CACHE_ID = 0x2
+CARAT_DEV_TIMEOUT = 0x4
 MAX_PROPOSALS = 16
 MAX_TILE_ROWS = 128
 
@@ -44,6 +45,7 @@ EXPORTED = (
     "carat_pool_create", "carat_pool_destroy", "carat_pool_alloc_ring", "carat_pool_free_ring",
     "carat_pool_alloc_pages", "carat_pool_free_pages", "carat_pool_stats",
     "carat_ring_append_fp8", "carat_ring_rollback_fp8", "carat_swa_attention_fp8",
+    "carat_check_bounded_wait",
 )
 
 
@@ -71,6 +73,8 @@ def _declare(lib):
     lib.carat_swa_workspace_bytes.argtypes = [i32] * 6
     lib.carat_global_workspace_bytes.restype = sz
     lib.carat_global_workspace_bytes.argtypes = [i32] * 6
+    lib.carat_check_bounded_wait.restype = i32
+    lib.carat_check_bounded_wait.argtypes = [ctypes.c_uint64, vp]
     lib.carat_get_device_status.restype = i32
     lib.carat_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32), i32, vp]
     lib.carat_status_string.restype = ctypes.c_char_p
@@ -391,6 +395,15 @@ def carat_get_device_status(clear: bool = True, stream=None) -> int:
     _check(library().carat_get_device_status(ctypes.byref(v), 1 if clear else 0, _stream(stream)),
            "carat_get_device_status")
     return int(v.value)
+
+
+def carat_check_bounded_wait(limit_ns: int, stream=None) -> None:
+    """Run the self-check of the library's bounded waits: a kernel waits on a
+    barrier phase nothing completes, gives up after limit_ns and sets
+    CARAT_DEV_TIMEOUT in the device status word (read it with
+    carat_get_device_status)."""
+    _check(library().carat_check_bounded_wait(ctypes.c_uint64(int(limit_ns)), _stream(stream)),
+           "carat_check_bounded_wait")
 
 
 def kernel_launches() -> int:

@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "carat_internal.cuh"
+#include "tc_common.cuh"
 
 namespace carat {
 
@@ -712,6 +713,30 @@ carat_status carat_swa_attention_fp8(float *out, const void *queries, const void
     p.out_scale = v_scale;
     p.source = KeySource::kRing;
     return launch_status(launch_attention(p, plan, static_cast<cudaStream_t>(stream)));
+}
+
+namespace carat {
+namespace {
+// One bounded wait on a barrier phase that nothing completes: the wait the
+// attention kernels use, given up after limit_ns.
+__global__ void bounded_wait_check_kernel(int *dev_status, unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    tc::mbar_init(&bar, 1);
+    tc::fence_mbar_init();
+    if (!tc::mbar_wait(&bar, 0, limit_ns)) set_status(dev_status, CARAT_DEV_TIMEOUT);
+}
+}  // namespace
+}  // namespace carat
+
+carat_status carat_check_bounded_wait(uint64_t limit_ns, void *stream) {
+    if (limit_ns < 1000000ull || limit_ns > 10000000000ull) return CARAT_ERR_INVALID_ARG;
+    int *status = carat::device_status_ptr();
+    if (!status) return CARAT_ERR_CUDA;
+    carat::bounded_wait_check_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        status, (unsigned long long)limit_ns);
+    carat::count_launches(1);
+    return cudaGetLastError() == cudaSuccess ? CARAT_OK : CARAT_ERR_CUDA;
 }
 
 carat_status carat_get_device_status(int32_t *host_out, int clear, void *stream) {

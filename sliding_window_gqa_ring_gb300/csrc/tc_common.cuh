@@ -59,8 +59,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // polls has run out.  The elapsed time is a signed difference, so a global
 // timer that steps backwards cannot end a wait early (an unsigned difference
 // would wrap to a huge value); a wait also needs kMinRounds rounds before the
-// timer is believed, and ends after kMaxRounds whatever the timer says.
-constexpr uint32_t kMinRounds = 1u << 12;
+// timer is believed (a poll of a phase that never completes may itself suspend
+// the thread for a while, so this stays small), and ends after kMaxRounds
+// whatever the timer says.
+constexpr uint32_t kMinRounds = 2;
 constexpr uint32_t kMaxRounds = 1u << 24;
 __device__ __forceinline__ bool wait_expired(uint64_t t0, uint32_t rounds, uint64_t limit_ns) {
     if (rounds >= kMaxRounds) return true;
