@@ -1012,6 +1012,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
             long long start;
         } pend{};
         constexpr int kLdPair = N >= 32 ? 2 : 1;   // TMEM loads issued per wait
+        constexpr bool kSkipMax = N <= 16;         // skip the row-max reduction when idle
         auto write_segment = [&](const PendingEpi &pe) {
             const uint32_t tmo = tmem_o_of(pe.si);
             if (pe.whole) {
@@ -1277,48 +1278,70 @@ __global__ void __launch_bounds__(kThreads, MINB)
                         rowmask = low_bits((int)jhi * p.group) & ~low_bits((int)jlo * p.group);
                 }
                 float tmax[N];
+                bool need = false;   // a score past its row's running maximum + slack
 #pragma unroll
                 for (int r = 0; r < N; ++r) {
                     x[r] = ((rowmask >> r) & 1ull) ? x[r] * (F8 ? s_qscale[r] : p.scale_log2)
                                                    : -INFINITY;
-                    tmax[r] = x[r];
+                    if constexpr (kSkipMax) need |= x[r] > m_run[r] + kRescaleSlack;
                 }
-                const int rb = warp_transpose_reduce<N, true>(tmax, lane);
-                float *red_max = red + (idx & 1) * 4 * N;
-                constexpr int kHeld = N >= 32 ? N / 32 : 1;
-#pragma unroll
-                for (int e = 0; e < kHeld; ++e) red_max[q4 * N + rb + e] = tmax[e];
-                if (named_bar_softmax_any(!w_ok || *abort_flag)) {
-                    alive = false;
-                    break;
-                }
-#pragma unroll
-                for (int r = 0; r < N; r += 4) {
-                    float4 a0 = *reinterpret_cast<const float4 *>(red_max + 0 * N + r);
-                    float4 a1 = *reinterpret_cast<const float4 *>(red_max + 1 * N + r);
-                    float4 a2 = *reinterpret_cast<const float4 *>(red_max + 2 * N + r);
-                    float4 a3 = *reinterpret_cast<const float4 *>(red_max + 3 * N + r);
-                    tmax[r + 0] = fmaxf(fmaxf(a0.x, a1.x), fmaxf(a2.x, a3.x));
-                    tmax[r + 1] = fmaxf(fmaxf(a0.y, a1.y), fmaxf(a2.y, a3.y));
-                    tmax[r + 2] = fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z));
-                    tmax[r + 3] = fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w));
-                }
+                // The running maximum of a row moves only when the tile's maximum
+                // exceeds it by more than kRescaleSlack (log2 units; P stays below
+                // 2^kRescaleSlack and O^T is rescaled only when a maximum really
+                // moves).  With 16 rows, one predicated barrier tells all 128
+                // threads whether any row of this tile does; only then are the
+                // tile's row maxima reduced (a warp transpose-reduction, then
+                // across the 4 warps in shared memory).  Either way the result is
+                // the same.  (With more rows the extra registers cost more than the
+                // skipped reduction saves: always reduce.)
+                const bool reduce =
+                    !kSkipMax || named_bar_softmax_any(need || !w_ok || *abort_flag);
                 float alpha[N];
                 bool rescale = false;
+                if (reduce) {
 #pragma unroll
-                for (int r = 0; r < N; ++r) {
-                    // Keep a stale running maximum unless the tile's maximum exceeds
-                    // it by more than kRescaleSlack (log2 units): P stays below
-                    // 2^kRescaleSlack and O^T is rescaled only when a row's maximum
-                    // really moves.
-                    const float mn = tmax[r] > m_run[r] + kRescaleSlack ? tmax[r] : m_run[r];
-                    const float ms = mn == -INFINITY ? 0.f : mn;
-                    alpha[r] = fast_exp2(m_run[r] - ms);
-                    const float pr = fast_exp2(x[r] - ms);
-                    l_part[r] = l_part[r] * alpha[r] + pr;
-                    x[r] = pr;
-                    rescale |= (mn != m_run[r]) && (m_run[r] != -INFINITY);
-                    m_run[r] = mn;
+                    for (int r = 0; r < N; ++r) tmax[r] = x[r];
+                    const int rb = warp_transpose_reduce<N, true>(tmax, lane);
+                    float *red_max = red + (idx & 1) * 4 * N;
+                    constexpr int kHeld = N >= 32 ? N / 32 : 1;
+#pragma unroll
+                    for (int e = 0; e < kHeld; ++e) red_max[q4 * N + rb + e] = tmax[e];
+                    if (named_bar_softmax_any(!w_ok || *abort_flag)) {
+                        alive = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int r = 0; r < N; r += 4) {
+                        float4 a0 = *reinterpret_cast<const float4 *>(red_max + 0 * N + r);
+                        float4 a1 = *reinterpret_cast<const float4 *>(red_max + 1 * N + r);
+                        float4 a2 = *reinterpret_cast<const float4 *>(red_max + 2 * N + r);
+                        float4 a3 = *reinterpret_cast<const float4 *>(red_max + 3 * N + r);
+                        tmax[r + 0] = fmaxf(fmaxf(a0.x, a1.x), fmaxf(a2.x, a3.x));
+                        tmax[r + 1] = fmaxf(fmaxf(a0.y, a1.y), fmaxf(a2.y, a3.y));
+                        tmax[r + 2] = fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z));
+                        tmax[r + 3] = fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w));
+                    }
+#pragma unroll
+                    for (int r = 0; r < N; ++r) {
+                        const float mn = tmax[r] > m_run[r] + kRescaleSlack ? tmax[r] : m_run[r];
+                        const float ms = mn == -INFINITY ? 0.f : mn;
+                        alpha[r] = fast_exp2(m_run[r] - ms);
+                        const float pr = fast_exp2(x[r] - ms);
+                        l_part[r] = l_part[r] * alpha[r] + pr;
+                        x[r] = pr;
+                        rescale |= (mn != m_run[r]) && (m_run[r] != -INFINITY);
+                        m_run[r] = mn;
+                    }
+                } else {
+                    // every maximum stays: alpha = 1
+#pragma unroll
+                    for (int r = 0; r < N; ++r) {
+                        const float ms = m_run[r] == -INFINITY ? 0.f : m_run[r];
+                        const float pr = fast_exp2(x[r] - ms);
+                        l_part[r] += pr;
+                        x[r] = pr;
+                        alpha[r] = 1.f;
+                    }
                 }
                 // PV of the previous tile (of this segment or the one before)
                 // must be done before P and O are touched.
