@@ -1446,12 +1446,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
                         }
                     }
                 }
+                // Each thread publishes its own P column (and zeroed V rows): the
+                // MMA thread waits for all 128 arrivals.  A thread that gave up
+                // a wait above goes on to the next barrier, where all 128 leave
+                // together.
                 tc::fence_proxy_async_smem();
                 tc::tc_fence_before();
-                if (named_bar_softmax_any(!alive || *abort_flag)) {
-                    alive = false;
-                    break;
-                }
                 tc::mbar_arrive(p_full);
                 if (p.fused_write && (ring || sg.rg == 0)) {
                     // Write this step's rows whose slot this tile covers (ring), or
