@@ -58,6 +58,9 @@
 //               running max / sum (log2 domain), writes P, rescales O^T in
 //               TMEM when a row's maximum moved; per segment they write the
 //               output or the partial.
+//   warps 6-9   (FP8 e4m3 caches only, 320 threads) widen each raw e4m3 stage
+//               the producer lands into an f16 stage, in load order, and each
+//               segment's Q into f16 with a power-of-two scale per row.
 //
 // Every wait is bounded (mbar_wait): on a timeout the CTA records
 // CARAT_DEV_TIMEOUT, stops issuing work, waits (bounded) for its own copies
@@ -82,6 +85,7 @@ constexpr int kDispRows = 16;               // displaced rows loaded per tile (>
 constexpr int kMaxPieces = 64;              // CTAs one unit may be split across
 constexpr int kDispBoxBytes = kDispRows * 128;
 constexpr int kThreads = 192;
+constexpr int kConvThreads = 128;           // FP8 caches: four more warps widen the stages
 constexpr uint32_t kFull = 0xffffffffu;
 
 template <int D, int N, int NS, int NR = 0>
@@ -98,10 +102,10 @@ struct Layout {
     static constexpr int kOffRed = kOffP + 2 * kPBlock;
     // 2 x max buffers + sum buffer (4 warps x N each), one segment's row
     // maxima and sums kept for its deferred epilogue, then (FP8) the row
-    // score scales of the segment being computed
-    static constexpr int kRedFloats = 3 * 4 * N + (NR > 0 ? 3 : 2) * N;
+    // score scales of two segments (even, odd)
+    static constexpr int kRedFloats = 3 * 4 * N + (NR > 0 ? 4 : 2) * N;
     static constexpr int kOffBar = kOffRed + kRedFloats * 4;
-    static constexpr int kNumBars = 2 * NS + 7 + 2 * NR + (NR > 0 ? 1 : 0);
+    static constexpr int kNumBars = 2 * NS + 7 + 2 * NR + (NR > 0 ? 2 : 0);
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;   // SkShared
     static constexpr int kBytes = kOffMisc + 128;
     static constexpr int kAlloc = kBytes + 1024;       // base alignment slack
@@ -440,6 +444,19 @@ __device__ __forceinline__ void convert_q_f16(uint8_t *s_q, float *qscale, float
     if (j == 0) qscale[r] = scale_log2 * __int_as_float((127 - s) << 23);
 }
 
+// FP8 (ring, append done before the call): whether key t of ring tile i
+// holds no token, so its V row is widened as zeros (its contents, zero or
+// not, must not reach O through P = 0).  held: tokens the ring holds.
+__device__ __forceinline__ bool ring_key_empty(int i, int t, int window, long long held) {
+    if ((long long)(i + 1) * kTileKeys <= (held < window ? held : (long long)window)) return false;
+    const long long newest = held - 1;
+    const int slot = i * kTileKeys + t;
+    if (newest < 0 || slot >= window) return true;
+    long long delta = newest % window - slot;
+    if (delta < 0) delta += window;
+    return newest - delta < 0;
+}
+
 // Barrier over the 128 softmax threads that also ORs a predicate across them,
 // so every thread takes the same abort decision.
 __device__ __forceinline__ bool named_bar_softmax_any(bool pred) {
@@ -521,7 +538,7 @@ struct KeyInfo {
 }  // namespace
 
 template <int D, int N, int NS, int MINB, int NR = 0>
-__global__ void __launch_bounds__(kThreads, MINB)
+__global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, MINB)
     attn_tc_kernel(const AttnParams p, const TcPlan plan, const __grid_constant__ TcMaps maps) {
     using L = Layout<D, N, NS, NR>;
     constexpr int KS = L::KS;
@@ -550,11 +567,12 @@ __global__ void __launch_bounds__(kThreads, MINB)
     uint64_t *fin = s_full + 6;
     uint64_t *raw_full = s_full + 7;     // [NR] FP8: e4m3 stage landed
     uint64_t *raw_empty = raw_full + NR; // [NR] FP8: e4m3 stage converted
-    uint64_t *q_conv = raw_empty + NR;   // FP8: Q rewritten as f16
+    uint64_t *qs_ready = raw_empty + NR; // [2] FP8: a segment's Q rewritten (segments alternate)
     uint8_t *s_raw = smem + L::kOffRaw;
     SkShared *sk = reinterpret_cast<SkShared *>(smem + L::kOffMisc);
     volatile int *abort_flag = &sk->abort_flag;
     float *red = reinterpret_cast<float *>(smem + L::kOffRed);
+    float *s_qscale = red + 14 * N;   // FP8: row score scales of two segments (even, odd)
     uint8_t *s_q = smem + L::kOffQ;
     uint8_t *s_p = smem + L::kOffP;
 
@@ -761,19 +779,22 @@ __global__ void __launch_bounds__(kThreads, MINB)
             for (int i = 0; i < NS; ++i) {
                 // bf16 stage filled by TMA (one arrival with its bytes), or
                 // with FP8 caches by the 128 converting threads
-                tc::mbar_init(&full[i], F8 ? 128 : 1);
+                tc::mbar_init(&full[i], F8 ? kConvThreads : 1);
                 tc::mbar_init(&empty[i], 1);
             }
             for (int i = 0; i < NR; ++i) {
                 tc::mbar_init(&raw_full[i], 1);
-                tc::mbar_init(&raw_empty[i], 128);
+                tc::mbar_init(&raw_empty[i], kConvThreads);
             }
             tc::mbar_init(&s_full[0], 1);
             tc::mbar_init(&s_full[1], 1);
             tc::mbar_init(p_full, 128);
             tc::mbar_init(o_done, 1);
             tc::mbar_init(q_full, 1);
-            if (F8) tc::mbar_init(q_conv, 128);
+            if (F8) {
+                tc::mbar_init(&qs_ready[0], kConvThreads);
+                tc::mbar_init(&qs_ready[1], kConvThreads);
+            }
             tc::mbar_init(q_empty, 1);
             tc::mbar_init(fin, 1);
             sk->abort_flag = 0;
@@ -793,7 +814,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     } else if (warp == 1) {
         tc::tmem_alloc(&sk->tmem_slot, L::kTmemCols);
         tc::tmem_relinquish();
-    } else {
+    } else if (warp < 6) {
         // Requests rejected on the device get NaN outputs and a status bit
         // (requests b = blockIdx.x, blockIdx.x + grid, ...); their units have
         // no tiles in the flattened order.
@@ -856,7 +877,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
             int si = 0;
             while (alive && it.next(p, upr, plan.row_groups, sg)) {
                 const int n = sg.x1 - sg.x0;
-                if (!wait_or_abort(F8 ? q_conv : q_full, si & 1, abort_flag, p.dev_status)) {
+                if (!wait_or_abort(F8 ? &qs_ready[si & 1] : q_full, F8 ? (si >> 1) & 1 : si & 1,
+                                   abort_flag, p.dev_status)) {
                     alive = false;
                     break;
                 }
@@ -988,7 +1010,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 tc::mbar_wait(fin, 0, 100000000ull);
             }
         }
-    } else {
+    } else if (warp < 6) {
         // ------------------------------------------------------------ softmax
         const int q4 = warp & 3;              // TMEM lane quadrant this warp may access
         const int t = q4 * 32 + lane;         // key of the tile / d within an O block
@@ -999,10 +1021,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
         bool alive = true;
         uint32_t gt = 0, cnt_base = 0;       // tiles and stages before this segment
         int si = 0;                          // segments before this one
-        uint32_t ccnt = 0;                   // FP8: stages converted so far
         float *s_mrow = red + 12 * N;        // a finished segment's row maxima
         float *s_lrow = red + 13 * N;        // and row sums
-        float *s_qscale = red + 14 * N;      // FP8: this segment's row score scales
         // The epilogue of a finished segment, run once the next segment's first
         // tile is under way (or at once with a single O^T buffer).
         struct PendingEpi {
@@ -1124,85 +1144,17 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 }
                 return st;
             };
-            // FP8: convert the segment's raw stages, in load order, until
-            // `target` stages are done.  Thread t converts key row t (rows
-            // t < 16 of a special tile); V rows of keys that hold no token
-            // (zero_v) are written as zeros.  Returns false on a timeout.
-            int cv_part = 0, cv_pks = 0;
-            auto convert_through = [&](uint32_t target, bool zero_v) -> bool {
-                if constexpr (F8) {
-                    while (ccnt < target) {
-                        int x;
-                        bool is_v;
-                        if (cv_part == 0) {
-                            x = 0;
-                            is_v = false;
-                        } else if (cv_part == 2 * n - 1) {
-                            x = n - 1;
-                            is_v = true;
-                        } else {
-                            x = (cv_part - 1) / 2 + ((cv_part - 1) % 2 == 0 ? 1 : 0);
-                            is_v = (cv_part - 1) % 2 == 1;
-                        }
-                        const bool special = order_tile(sg, sg.x0 + x) == sg.special;
-                        if (special && is_v) {
-                            ++cv_part;
-                            continue;
-                        }
-                        const int sidx = ccnt % NS, r = ccnt % NR;
-                        if (ccnt >= NS && !wait_or_abort(&empty[sidx], ((ccnt / NS) & 1) ^ 1,
-                                                         abort_flag, p.dev_status))
-                            return false;
-                        if (!wait_or_abort(&raw_full[r], (ccnt / NR) & 1, abort_flag, p.dev_status))
-                            return false;
-                        const uint8_t *raw = s_raw + r * L::kRawBytes;
-                        uint8_t *stg = smem + sidx * kStageBytes;
-                        if (special) {
-                            // 16 displaced rows: K slabs then V slabs (2 KB each)
-                            if (t < kDispRows) {
-                                const long long pos = ctx - p.window + 1 + t;
-                                const bool valid = t < p.k - 1 && pos >= 0;
-#pragma unroll
-                                for (int sl = 0; sl < D / 128; ++sl) {
-                                    convert_row(raw + sl * 2048 + t * 128,
-                                                stg + (2 * sl) * kDispBoxBytes + t * 128,
-                                                stg + (2 * sl + 1) * kDispBoxBytes + t * 128, t,
-                                                false);
-                                    convert_row(raw + (D / 128 + sl) * 2048 + t * 128,
-                                                stg + (D / 64 + 2 * sl) * kDispBoxBytes + t * 128,
-                                                stg + (D / 64 + 2 * sl + 1) * kDispBoxBytes + t * 128,
-                                                t, !valid);
-                                }
-                            }
-                            ++cv_part;
-                        } else {
-                            convert_row(raw + t * 128, stg + t * 128, stg + kBoxBytes + t * 128, t,
-                                        is_v && zero_v);
-                            if (++cv_pks == KS) {
-                                cv_pks = 0;
-                                ++cv_part;
-                            }
-                        }
-                        tc::fence_proxy_async_smem();
-                        tc::mbar_arrive(&raw_empty[r]);
-                        tc::mbar_arrive(&full[sidx]);
-                        ++ccnt;
-                    }
-                }
-                return true;
-            };
+            // FP8: this segment's row score scales, written by the widening
+            // warps with its f16 Q (segments alternate between two barriers
+            // and two scale buffers: those warps run at most one segment ahead)
+            const float *qsc = s_qscale + (si & 1) * N;
             if constexpr (F8) {
-                // This segment's Q as f16 once its copy has landed; then the
-                // MMA warp may start the segment's products.
-                const bool q_ok =
-                    __all_sync(kFull, wait_or_abort(q_full, si & 1, abort_flag, p.dev_status));
-                if (q_ok) convert_q_f16<D, N, L::kQBlock>(s_q, s_qscale, p.scale_log2, t);
-                tc::fence_proxy_async_smem();
+                const bool q_ok = wait_or_abort(&qs_ready[si & 1], (si >> 1) & 1, abort_flag,
+                                                p.dev_status);
                 if (named_bar_softmax_any(!q_ok || *abort_flag)) {
                     alive = false;
                     break;
                 }
-                tc::mbar_arrive(q_conv);
             }
             float m_run[N], l_part[N];
 #pragma unroll
@@ -1214,16 +1166,6 @@ __global__ void __launch_bounds__(kThreads, MINB)
             for (; idx < n; ++idx) {
                 const uint32_t tile = gt + idx;
                 const int i = order_tile(sg, sg.x0 + idx);
-                if constexpr (F8) {
-                    // K of this tile and the next, before their QK products
-                    // (When the stage ring holds one K tile only, the stage of a
-                    // special tile is free again only after its PV product, which
-                    // waits for this tile's P: no look-ahead past it.)
-                    const int xk = (idx + 1 < n && !(NS == KS && idx == xs)) ? idx + 1 : idx;
-                    if (!convert_through(cnt_base + stages_before((xk == 0 ? 0 : 2 * xk - 1) + 1),
-                                         false))
-                        alive = false;
-                }
                 // warp-uniform: the TMEM load below is warp-collective
                 const bool w_ok = __all_sync(kFull, alive && wait_or_abort(&s_full[tile & 1],
                                                                            (tile >> 1) & 1,
@@ -1281,7 +1223,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
                 bool need = false;   // a score past its row's running maximum + slack
 #pragma unroll
                 for (int r = 0; r < N; ++r) {
-                    x[r] = ((rowmask >> r) & 1ull) ? x[r] * (F8 ? s_qscale[r] : p.scale_log2)
+                    x[r] = ((rowmask >> r) & 1ull) ? x[r] * (F8 ? qsc[r] : p.scale_log2)
                                                    : -INFINITY;
                     if constexpr (kSkipMax) need |= x[r] > m_run[r] + kRescaleSlack;
                 }
@@ -1400,13 +1342,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
                         }
                     }
                     if constexpr (F8) {
-                        // V of this tile, its no-token rows as zeros (a special
-                        // tile's V rows were converted with its K rows; going on
-                        // to the parts after it here could wait on its own PV)
-                        if (idx != xs &&
-                            !convert_through(cnt_base + stages_before(v_part(idx, n) + 1),
-                                             tile_partial && !ki.data))
-                            alive = false;
+                        // (the widening warps write the V rows, zeros for keys
+                        // that hold no token)
                     } else if (idx == xs) {
                         // The special tile's stage: zero its V rows that hold no
                         // token (only the 16 rows its PV product reads).
@@ -1569,6 +1506,87 @@ __global__ void __launch_bounds__(kThreads, MINB)
             pend.on = false;
         }
 
+    } else {
+        // ------------------------------------------------------------ widening
+        // (warps 6-9, FP8 caches only) Thread t widens key row t of every raw
+        // e4m3 stage, in load order, into the f16 stage ring the MMA thread
+        // reads -- the part a TMA producer plays for a bf16 cache -- writing
+        // zeros for V rows of keys that hold no token, and at the start of
+        // each segment rewrites its Q as f16 with a power-of-two scale per row.
+        if constexpr (F8) {
+            const int t = threadIdx.x - kThreads;
+            SegIter it;
+            it.init(p, sk);
+            Segment sg;
+            bool alive = true;
+            uint32_t ccnt = 0;   // raw stages widened so far
+            int si = 0;
+            while (alive && it.next(p, upr, plan.row_groups, sg)) {
+                const int n = sg.x1 - sg.x0;
+                alive = __all_sync(kFull, wait_or_abort(q_full, si & 1, abort_flag, p.dev_status));
+                if (!alive) break;
+                convert_q_f16<D, N, L::kQBlock>(s_q, s_qscale + (si & 1) * N, p.scale_log2, t);
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(&qs_ready[si & 1]);
+                const long long held = sg.ctx + p.k;   // tokens the ring holds (append done)
+                for (int part = 0; part < 2 * n && alive; ++part) {
+                    int x;
+                    bool is_v;
+                    if (part == 0) {
+                        x = 0;
+                        is_v = false;
+                    } else if (part == 2 * n - 1) {
+                        x = n - 1;
+                        is_v = true;
+                    } else {
+                        x = (part - 1) / 2 + ((part - 1) % 2 == 0 ? 1 : 0);
+                        is_v = (part - 1) % 2 == 1;
+                    }
+                    const int i = order_tile(sg, sg.x0 + x);
+                    const bool special = i == sg.special;
+                    if (special && is_v) continue;   // its V rows came with its K rows
+                    const bool zero_v = is_v && ring_key_empty(i, t, p.window, held);
+                    for (int ks = 0; ks < (special ? 1 : KS); ++ks) {
+                        const int sidx = ccnt % NS, r = ccnt % NR;
+                        alive = __all_sync(
+                            kFull, (ccnt < (uint32_t)NS ||
+                                    wait_or_abort(&empty[sidx], ((ccnt / NS) & 1) ^ 1, abort_flag,
+                                                  p.dev_status)) &&
+                                       wait_or_abort(&raw_full[r], (ccnt / NR) & 1, abort_flag,
+                                                     p.dev_status));
+                        if (!alive) break;
+                        const uint8_t *raw = s_raw + r * L::kRawBytes;
+                        uint8_t *stg = smem + sidx * kStageBytes;
+                        if (special) {
+                            // 16 displaced rows: K slabs then V slabs (2 KB each)
+                            if (t < kDispRows) {
+                                const long long pos = sg.ctx - p.window + 1 + t;
+                                const bool valid = t < p.k - 1 && pos >= 0;
+#pragma unroll
+                                for (int sl = 0; sl < D / 128; ++sl) {
+                                    convert_row(raw + sl * 2048 + t * 128,
+                                                stg + (2 * sl) * kDispBoxBytes + t * 128,
+                                                stg + (2 * sl + 1) * kDispBoxBytes + t * 128, t,
+                                                false);
+                                    convert_row(raw + (D / 128 + sl) * 2048 + t * 128,
+                                                stg + (D / 64 + 2 * sl) * kDispBoxBytes + t * 128,
+                                                stg + (D / 64 + 2 * sl + 1) * kDispBoxBytes + t * 128,
+                                                t, !valid);
+                                }
+                            }
+                        } else {
+                            convert_row(raw + t * 128, stg + t * 128, stg + kBoxBytes + t * 128, t,
+                                        zero_v);
+                        }
+                        tc::fence_proxy_async_smem();
+                        tc::mbar_arrive(&raw_empty[r]);
+                        tc::mbar_arrive(&full[sidx]);
+                        ++ccnt;
+                    }
+                }
+                ++si;
+            }
+        }
     }
 
     tc::tc_fence_before();
@@ -1702,7 +1720,7 @@ cudaError_t launch_tc(const AttnParams &p, const TcPlan &plan, const TcMaps &map
         if (e != cudaSuccess) return e;
         configured_devices[dev] = 1;
     }
-    kernel<<<grid, kThreads, L::kAlloc, stream>>>(p, plan, maps);
+    kernel<<<grid, NR > 0 ? kThreads + kConvThreads : kThreads, L::kAlloc, stream>>>(p, plan, maps);
     count_launches(1);
     e = cudaGetLastError();
     if (e != cudaSuccess || plan.unit_mode) return e;
