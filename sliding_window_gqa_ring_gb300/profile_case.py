@@ -26,6 +26,9 @@ CASES = {
     "global_sweep15": lambda: synth.global_sweep(15),
     # the mixed step's global layer: about 9 GB of caches, for one-pass captures only
     "global_mixed": lambda: synth.mixed_step()[1],
+    # the mixed step's sliding layer with FP8 e4m3 rings (append once, then the
+    # attention call repeats)
+    "swa_mixed_fp8": lambda: synth.mixed_step()[0],
 }
 
 
@@ -37,6 +40,30 @@ def main():
                     help="time carat_ring_append + the attention call instead of the fused call")
     args = ap.parse_args()
     w = CASES[args.case]()
+    if args.case.endswith("_fp8"):
+        # scales as a caller would calibrate them: max |x| / 448 over the layer
+        probe = engine.SlidingLayer(w.batch, window=w.window, q_heads=w.q_heads,
+                                    kv_heads=w.kv_heads, head_dim=w.head_dim,
+                                    max_proposals=w.proposal_count, scale=w.scale)
+        hist = engine.stage_sliding(w, 0, probe).host["hist"]
+        kmax = max(float(abs(synth.bf16_to_float(h[1])).max()) for h in hist.values())
+        vmax = max(float(abs(synth.bf16_to_float(h[2])).max()) for h in hist.values())
+        del probe
+        layer = engine.Fp8SlidingLayer(w.batch, k_scale=kmax / 448.0, v_scale=vmax / 448.0,
+                                       window=w.window, q_heads=w.q_heads, kv_heads=w.kv_heads,
+                                       head_dim=w.head_dim, max_proposals=w.proposal_count,
+                                       scale=w.scale)
+        inp = engine.stage_sliding(w, 0, layer)
+        out = torch.empty(inp.queries.shape, dtype=torch.float32, device=layer.device)
+        layer.append(inp.k_new, inp.v_new, inp.context_lengths)
+        for _ in range(args.calls):
+            layer.attend(inp.queries, inp.context_lengths, out=out)
+        torch.cuda.synchronize()
+        status = carat.carat_get_device_status(clear=True)
+        print(f"{args.case}: {args.calls} calls, device status {status:#x}")
+        if status:
+            raise SystemExit(1)
+        return
     if w.window:
         layer = engine.SlidingLayer(w.batch, window=w.window, q_heads=w.q_heads,
                                     kv_heads=w.kv_heads, head_dim=w.head_dim,
