@@ -34,7 +34,10 @@
  *    row-major in the order written next to each argument.
  *  - The caller owns every buffer, including the workspace; the library
  *    allocates no device memory and keeps no state across calls except one
- *    device status word per GPU (carat_get_device_status).
+ *    device status word per GPU (carat_get_device_status), whose device
+ *    address is looked up on a device's first call and kept: after
+ *    cudaDeviceReset on a device, do not call the library on it again in the
+ *    same process.
  *  - Positions.  For request b, context_lengths[b] tokens are in the cache
  *    BEFORE this step; the step's proposal_count new tokens sit at positions
  *    context_lengths[b] + j, j = 0 .. proposal_count-1, and
@@ -174,7 +177,8 @@ carat_status carat_ring_rollback(void *k_ring, void *v_ring, int num_rings,
  *                    the GPU need separate workspaces.
  *
  * Supported: head_dim 256 or 512; (q_heads/kv_heads)*proposal_count <= 128;
- * proposal_count <= 16 and <= window.
+ * q_heads/kv_heads <= 64; proposal_count <= 16 and <= window (other shapes:
+ * CARAT_ERR_UNSUPPORTED, nothing launched).
  */
 carat_status carat_swa_attention(float *out, const void *queries,
                                  const void *k_ring, const void *v_ring, int num_rings,
@@ -209,7 +213,8 @@ carat_status carat_swa_attention(float *out, const void *queries,
  *   workspace        >= carat_global_workspace_bytes(...) bytes, as above.
  *
  * Supported: head_dim 256 or 512; (q_heads/kv_heads)*proposal_count <= 128;
- * proposal_count <= 16.
+ * q_heads/kv_heads <= 64; proposal_count <= 16 (other shapes:
+ * CARAT_ERR_UNSUPPORTED, nothing launched).
  */
 carat_status carat_global_verify_attention(float *out, const void *queries,
                                            const void *key_cache, const void *value_cache,
@@ -240,7 +245,10 @@ carat_status carat_global_verify_attention(float *out, const void *queries,
  *
  * The first call on each device looks up the array's device address (with
  * that device current) and caches it; make that first call before any
- * stream capture begins.  Every call uses the same array and nothing in it
+ * stream capture begins.  The cached address belongs to that device's
+ * context as it was then: after cudaDeviceReset on a device, do not call this
+ * library on that device again in the same process (the status word that
+ * every entry point writes is cached the same way).  Every call uses the same array and nothing in it
  * needs to start at zero, but calls that can run at the same time on the GPU
  * (other streams or host threads without ordering between them) race on it:
  * order them on one stream.  No device memory is allocated or freed.
@@ -276,8 +284,7 @@ size_t carat_noalloc_scratch_bytes(void);
  * attention.  displaced: NULL, or a buffer as in carat_ring_append that
  * receives the rows the new ones overwrite (for carat_ring_rollback).
  * workspace: carat_swa_workspace_bytes(...) bytes.
- * Supported: as carat_swa_attention, for (q_heads/kv_heads) <= 64 (otherwise
- * CARAT_ERR_UNSUPPORTED).
+ * Supported: as carat_swa_attention.
  */
 carat_status carat_swa_append_attention(float *out, const void *queries,
                                         void *k_ring, void *v_ring, int num_rings,
@@ -370,9 +377,9 @@ int carat_pool_free_pages(carat_pool *pool, int n, const int32_t *pages);
 int carat_pool_stats(carat_pool *pool, int32_t *out4);
 
 /*
- * FP8 (e4m3) sliding-window rings -- "Announcing Carat: An inference engine
- * designed for Gemma 4", section "Server": the KV cache is stored as FP8
- * e4m3, which is lossy (outside the bit-exact comparison).  The pages give
+ * FP8 (e4m3) sliding-window rings -- "gemma-cuda-hybrid", "Features" /
+ * "Server": the KV cache is stored as FP8 e4m3; "Limitations": FP8 KV is
+ * lossy (outside the bit-exact comparison).  The pages give
  * no scaling scheme; here each ring tensor has one dequantisation scale:
  * the value of a stored byte is e4m3(byte) * k_scale (K) or * v_scale (V).
  *
@@ -390,7 +397,7 @@ int carat_pool_stats(carat_pool *pool, int32_t *out4);
  *
  * carat_swa_attention_fp8 -- carat_swa_attention over e4m3 rings: the
  *   attention of the dequantised K and V (bf16 queries, fp32 out).  Each e4m3
- *   value is widened exactly to bf16 on chip; k_scale scales the scores and
+ *   value is widened exactly to f16 on chip; k_scale scales the scores and
  *   v_scale the output.  head_dim 256 only (CARAT_ERR_UNSUPPORTED else).  The
  *   workspace it needs is at most carat_swa_workspace_bytes for the same
  *   sizes.  Other arguments, limits and device-side error handling as in
@@ -442,6 +449,16 @@ carat_status carat_get_device_status(int32_t *host_out, int clear, void *stream)
  * carat_get_device_status); CARAT_ERR_CUDA if the launch fails.
  */
 carat_status carat_check_bounded_wait(uint64_t limit_ns, void *stream);
+
+/*
+ * Launch floor, for measurement: one empty kernel, and with dependent != 0 a
+ * second empty kernel launched after it with programmatic dependent launch
+ * (it may start once the first has started and waits for it to finish) --
+ * the two-launch pattern of a stream-K attention call and its merge launch.
+ * Timing this call with CUDA events on `stream` gives the part of a call's
+ * time that no kernel work can remove.  The pages have no counterpart.
+ */
+carat_status carat_launch_floor(int dependent, void *stream);
 
 /* Static English text for a status code. */
 const char *carat_status_string(carat_status status);

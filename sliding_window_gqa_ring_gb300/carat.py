@@ -45,7 +45,7 @@ EXPORTED = (
     "carat_pool_create", "carat_pool_destroy", "carat_pool_alloc_ring", "carat_pool_free_ring",
     "carat_pool_alloc_pages", "carat_pool_free_pages", "carat_pool_stats",
     "carat_ring_append_fp8", "carat_ring_rollback_fp8", "carat_swa_attention_fp8",
-    "carat_check_bounded_wait",
+    "carat_check_bounded_wait", "carat_launch_floor",
 )
 
 
@@ -73,6 +73,8 @@ def _declare(lib):
     lib.carat_swa_workspace_bytes.argtypes = [i32] * 6
     lib.carat_global_workspace_bytes.restype = sz
     lib.carat_global_workspace_bytes.argtypes = [i32] * 6
+    lib.carat_launch_floor.restype = i32
+    lib.carat_launch_floor.argtypes = [i32, vp]
     lib.carat_check_bounded_wait.restype = i32
     lib.carat_check_bounded_wait.argtypes = [ctypes.c_uint64, vp]
     lib.carat_get_device_status.restype = i32
@@ -177,6 +179,43 @@ def _expect(t, dtype, name):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+def _attention_args(out, queries, k_cache, v_cache, context_lengths, cache_dtype, what,
+                    displaced=None, k_new=None, v_new=None):
+    """Shape and dtype checks the C ABI cannot make (it sees only pointers and
+    sizes): a cache of the wrong element type or head_dim would be read past
+    its end on the GPU.  Returns (batch, k, q_heads, head_dim, num, rows,
+    kv_heads) with num/rows the cache's first two dimensions."""
+    _expect(queries, torch.bfloat16, f"{what}: queries")
+    _expect(out, torch.float32, f"{what}: out")
+    _expect(k_cache, cache_dtype, f"{what}: key cache")
+    _expect(v_cache, cache_dtype, f"{what}: value cache")
+    _expect(context_lengths, torch.int32, f"{what}: context_lengths")
+    if queries.dim() != 4 or k_cache.dim() != 4:
+        raise ValueError(f"{what}: queries and caches must be 4-D")
+    batch, k, q_heads, head_dim = queries.shape
+    num, rows, kv_heads, cache_dim = k_cache.shape
+    if tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError(f"{what}: key and value caches differ in shape")
+    if cache_dim != head_dim:
+        raise ValueError(f"{what}: cache head_dim {cache_dim} != query head_dim {head_dim}")
+    if tuple(out.shape) != tuple(queries.shape):
+        raise ValueError(f"{what}: out must have the queries' shape")
+    if tuple(context_lengths.shape) != (batch,):
+        raise ValueError(f"{what}: context_lengths must be [batch]")
+    if displaced is not None:
+        _expect(displaced, cache_dtype, f"{what}: displaced")
+        if displaced.dim() != 5 or displaced.shape[0] < batch or \
+                tuple(displaced.shape[2:]) != (2, kv_heads, head_dim) or \
+                (k > 1 and displaced.shape[1] < k - 1):
+            raise ValueError(f"{what}: displaced must be [>=batch][>=k-1][2][kv_heads][head_dim]")
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        if t is not None:
+            _expect(t, torch.bfloat16, f"{what}: {name}")
+            if tuple(t.shape) != (batch, k, kv_heads, head_dim):
+                raise ValueError(f"{what}: {name} must be [batch][k][kv_heads][head_dim]")
+    return batch, k, q_heads, head_dim, num, rows, kv_heads
+
+
 def _check(status: int, what: str):
     if status != CARAT_OK:
         raise CaratError(status, what)
@@ -218,10 +257,9 @@ def carat_swa_attention(out, queries, k_ring, v_ring, context_lengths, *, scale,
     out fp32 [B][k][Hq][D]; queries bf16 [B][k][Hq][D]; workspace: a CUDA tensor
     of at least swa_workspace_bytes(...) bytes.
     """
-    _expect(queries, torch.bfloat16, "queries")
-    _expect(out, torch.float32, "out")
-    batch, k, q_heads, head_dim = queries.shape
-    num_rings, window, kv_heads, _ = k_ring.shape
+    batch, k, q_heads, head_dim, num_rings, window, kv_heads = _attention_args(
+        out, queries, k_ring, v_ring, context_lengths, torch.bfloat16, "carat_swa_attention",
+        displaced=displaced)
     _check(library().carat_swa_attention(
         _ptr(out), _ptr(queries), _ptr(k_ring), _ptr(v_ring), num_rings, _ptr(ring_ids),
         _ptr(displaced), _ptr(context_lengths), k, batch, q_heads, kv_heads, head_dim, window,
@@ -236,10 +274,9 @@ def carat_swa_attention_noalloc(out, queries, k_ring, v_ring, context_lengths, *
     CaratError (CARAT_ERR_WORKSPACE) for sizes that need more scratch than
     noalloc_scratch_bytes().  Calls that overlap on the GPU share the scratch
     and race; order them on one stream."""
-    _expect(queries, torch.bfloat16, "queries")
-    _expect(out, torch.float32, "out")
-    batch, k, q_heads, head_dim = queries.shape
-    num_rings, window, kv_heads, _ = k_ring.shape
+    batch, k, q_heads, head_dim, num_rings, window, kv_heads = _attention_args(
+        out, queries, k_ring, v_ring, context_lengths, torch.bfloat16,
+        "carat_swa_attention_noalloc", displaced=displaced)
     _check(library().carat_swa_attention_noalloc(
         _ptr(out), _ptr(queries), _ptr(k_ring), _ptr(v_ring), num_rings, _ptr(ring_ids),
         _ptr(displaced), _ptr(context_lengths), k, batch, q_heads, kv_heads, head_dim, window,
@@ -253,10 +290,9 @@ def noalloc_scratch_bytes() -> int:
 def carat_global_verify_attention(out, queries, key_cache, value_cache, context_lengths, *,
                                   scale, workspace, cache_ids=None, stream=None):
     """Grouped-head causal verify attention over a full cache (masked tail)."""
-    _expect(queries, torch.bfloat16, "queries")
-    _expect(out, torch.float32, "out")
-    batch, k, q_heads, head_dim = queries.shape
-    num_caches, capacity, kv_heads, _ = key_cache.shape
+    batch, k, q_heads, head_dim, num_caches, capacity, kv_heads = _attention_args(
+        out, queries, key_cache, value_cache, context_lengths, torch.bfloat16,
+        "carat_global_verify_attention")
     _check(library().carat_global_verify_attention(
         _ptr(out), _ptr(queries), _ptr(key_cache), _ptr(value_cache), num_caches,
         _ptr(cache_ids), _ptr(context_lengths), k, batch, q_heads, kv_heads, head_dim, capacity,
@@ -269,11 +305,9 @@ def carat_swa_append_attention(out, queries, k_ring, v_ring, k_new, v_new, conte
     """Append this step's rows to the rings and attend, in one launch.  Rings
     are passed as before the step; afterwards they hold the new rows (and
     `displaced`, if given, the rows they overwrote, for carat_ring_rollback)."""
-    _expect(queries, torch.bfloat16, "queries")
-    _expect(out, torch.float32, "out")
-    _expect(k_new, torch.bfloat16, "k_new")
-    batch, k, q_heads, head_dim = queries.shape
-    num_rings, window, kv_heads, _ = k_ring.shape
+    batch, k, q_heads, head_dim, num_rings, window, kv_heads = _attention_args(
+        out, queries, k_ring, v_ring, context_lengths, torch.bfloat16,
+        "carat_swa_append_attention", displaced=displaced, k_new=k_new, v_new=v_new)
     _check(library().carat_swa_append_attention(
         _ptr(out), _ptr(queries), _ptr(k_ring), _ptr(v_ring), num_rings, _ptr(ring_ids),
         _ptr(displaced), _ptr(k_new), _ptr(v_new), _ptr(context_lengths), k, batch, q_heads,
@@ -301,11 +335,9 @@ def carat_global_append_verify_attention(out, queries, key_cache, value_cache, k
                                          stream=None):
     """Append this step's rows to the global caches and run grouped verify
     attention, in one launch."""
-    _expect(queries, torch.bfloat16, "queries")
-    _expect(out, torch.float32, "out")
-    _expect(k_new, torch.bfloat16, "k_new")
-    batch, k, q_heads, head_dim = queries.shape
-    num_caches, capacity, kv_heads, _ = key_cache.shape
+    batch, k, q_heads, head_dim, num_caches, capacity, kv_heads = _attention_args(
+        out, queries, key_cache, value_cache, context_lengths, torch.bfloat16,
+        "carat_global_append_verify_attention", k_new=k_new, v_new=v_new)
     _check(library().carat_global_append_verify_attention(
         _ptr(out), _ptr(queries), _ptr(key_cache), _ptr(value_cache), num_caches,
         _ptr(cache_ids), _ptr(k_new), _ptr(v_new), _ptr(context_lengths), k, batch, q_heads,
@@ -321,11 +353,10 @@ def carat_global_append_verify_attention_paged(out, queries, key_pages, value_pa
 
     key_pages / value_pages bf16 [num_pages][page_rows][Hkv][D]; page_table
     int32 [B][max_pages] (device)."""
-    _expect(queries, torch.bfloat16, "queries")
-    _expect(out, torch.float32, "out")
     _expect(page_table, torch.int32, "page_table")
-    batch, k, q_heads, head_dim = queries.shape
-    num_pages, page_rows, kv_heads, _ = key_pages.shape
+    batch, k, q_heads, head_dim, num_pages, page_rows, kv_heads = _attention_args(
+        out, queries, key_pages, value_pages, context_lengths, torch.bfloat16,
+        "carat_global_append_verify_attention_paged", k_new=k_new, v_new=v_new)
     max_pages = page_table.shape[1]
     _check(library().carat_global_append_verify_attention_paged(
         _ptr(out), _ptr(queries), _ptr(key_pages), _ptr(value_pages), num_pages, _ptr(page_table),
@@ -406,6 +437,13 @@ def carat_check_bounded_wait(limit_ns: int, stream=None) -> None:
            "carat_check_bounded_wait")
 
 
+def carat_launch_floor(dependent: bool = False, stream=None) -> None:
+    """Launch one empty kernel (and, with dependent, an empty dependent launch
+    after it): the floor under a call's measured time."""
+    _check(library().carat_launch_floor(1 if dependent else 0, _stream(stream)),
+           "carat_launch_floor")
+
+
 def kernel_launches() -> int:
     """Kernels libcarat.so has launched in this process so far."""
     return int(library().carat_kernel_launches())
@@ -455,11 +493,9 @@ def carat_ring_rollback_fp8(k_ring, v_ring, displaced, context_lengths, accepted
 def carat_swa_attention_fp8(out, queries, k_ring, v_ring, context_lengths, *, scale, k_scale,
                             v_scale, workspace, ring_ids=None, displaced=None, stream=None):
     """Sliding-window attention over e4m3 rings (dequantised: byte value x scale)."""
-    _expect(queries, torch.bfloat16, "queries")
-    _expect(out, torch.float32, "out")
-    _expect(k_ring, torch.uint8, "k_ring")
-    batch, k, q_heads, head_dim = queries.shape
-    num_rings, window, kv_heads, _ = k_ring.shape
+    batch, k, q_heads, head_dim, num_rings, window, kv_heads = _attention_args(
+        out, queries, k_ring, v_ring, context_lengths, torch.uint8, "carat_swa_attention_fp8",
+        displaced=displaced)
     _check(library().carat_swa_attention_fp8(
         _ptr(out), _ptr(queries), _ptr(k_ring), _ptr(v_ring), num_rings, _ptr(ring_ids),
         _ptr(displaced), _ptr(context_lengths), k, batch, q_heads, kv_heads, head_dim, window,

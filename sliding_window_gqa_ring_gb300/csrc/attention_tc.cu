@@ -2,10 +2,10 @@
 // cores (tcgen05 + TMEM) with TMA-staged K/V tiles, scheduled stream-K over a
 // persistent grid.
 //
-// What it computes is what attention_simt.cu computes: for each request b and
-// KV head c, the rows r = j*g + h' (the g query heads sharing KV head c times
-// the proposal positions j; "Announcing Carat: An inference engine designed
-// for Gemma 4", "Doing it all in one kernel can be slower") attend to the keys
+// What it computes: for each request b and KV head c, the rows r = j*g + h'
+// (the g query heads sharing KV head c times the proposal positions j;
+// "Announcing Carat: An inference engine designed for Gemma 4", "Doing it all
+// in one kernel can be slower") attend to the keys
 // their position may see -- the last `window` positions for a sliding layer
 // read in place from the rotated ring ("Improving Decode Throughput on Intel
 // Gaudi 3", "Our approach"), every position up to their own for a global

@@ -31,12 +31,11 @@ struct AttnParams {
     const uint16_t *displaced;  // [B][k-1][2][Hkv][D] (ring source, k > 1)
     const int32_t *context_lengths;
     float *out;                 // [B][k][Hq][D]
-    // Split partials (running max and sum in log2 units, unnormalised O).
-    // CUDA-core path: [B][Hkv][nchunks][rows].  Tensor-core path: two slots
-    // per CTA, [grid][2][rows per tile].
+    // Split partials (running max and sum in log2 units, unnormalised O):
+    // two slots per CTA of a stream-K grid, [grid][2][rows per tile].
     float2 *part_ml;
     float *part_o;
-    // Tensor-core stream-K path: per (request, KV head, row group) unit, its
+    // Stream-K schedule: per (request, KV head, row group) unit, its
     // first tile's flattened index (x: low, y: high 32 bits), its tile count
     // when split across CTAs (z; 0 when one CTA covered it) and the range
     // length (w), for the merge launch.
@@ -46,9 +45,7 @@ struct AttnParams {
     int batch, k, q_heads, kv_heads, head_dim, group, rows;
     int window;                 // ring slots (kRing) -- positions older than p-window+1 hidden
     int capacity;               // cache rows (kLinear)
-    int chunk;                  // CUDA-core path: keys per split
-    int nchunks;                // CUDA-core path: splits per (request, KV head)
-    // Fused append (tensor-core path): the caches hold the tokens before this
+    // Fused append: the caches hold the tokens before this
     // step and this step's rows come from k_new / v_new [B][k][Hkv][D]; when
     // fused_write is set the kernel also writes them into k_dst / v_dst.
     int fused;
@@ -188,12 +185,6 @@ __device__ __forceinline__ long long paged_row(const int32_t *page_table, int ma
     return (long long)page * page_rows + t % page_rows;
 }
 
-// Number of key slots scanned per (request, KV head).
-__host__ __device__ __forceinline__ long long keys_scanned(KeySource src, int window, int k,
-                                                          long long key_count) {
-    return src == KeySource::kRing ? (long long)window + (k - 1) : key_count;
-}
-
 // Host-side count of kernel launches (carat_kernel_launches).
 void count_launches(int n);
 
@@ -204,8 +195,6 @@ cudaError_t launch_ring_append(const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_ring_append_fp8(const AppendParams &p, cudaStream_t stream);
 cudaError_t launch_ring_rollback(const AppendParams &p, const int32_t *accepted,
                                  cudaStream_t stream);
-cudaError_t launch_attention_simt(const AttnParams &p, cudaStream_t stream);
-cudaError_t launch_combine(const AttnParams &p, cudaStream_t stream);
 
 // Tensor-core path (attention_tc.cu): rows per tile (16, 32 or 64) for a
 // group size and proposal count, CTAs resident per SM, whether the shape is

@@ -75,6 +75,7 @@ def test_workspace_queries(lib):
     assert lib.carat_swa_workspace_bytes(1, 1, 16, 8, 128, 1024) == 0       # unsupported D
     assert lib.carat_global_workspace_bytes(1, 17, 16, 2, 512, 1024) == 0   # too many proposals
     assert lib.carat_global_workspace_bytes(1, 16, 16, 1, 512, 1024) == 0   # 256 rows > 128
+    assert lib.carat_swa_workspace_bytes(1, 1, 128, 1, 256, 1024) == 0      # 128 heads per KV head
     # monotone in batch
     a = lib.carat_global_workspace_bytes(4, 4, 16, 2, 512, 8192)
     b = lib.carat_global_workspace_bytes(8, 4, 16, 2, 512, 8192)
@@ -124,6 +125,7 @@ def test_swa_argument_checks(lib):
     assert _swa(lib, nr=2) == c.CARAT_ERR_INVALID_ARG                 # fewer rings than requests
     assert _swa(lib, scale=float("nan")) == c.CARAT_ERR_INVALID_ARG
     assert _swa(lib, hq=64, hkv=1, k=4) == c.CARAT_ERR_UNSUPPORTED    # 256 rows per tile
+    assert _swa(lib, hq=128, hkv=1, k=1) == c.CARAT_ERR_UNSUPPORTED   # > 64 heads per KV head
     assert _swa(lib, wsb=16) == c.CARAT_ERR_WORKSPACE
     assert _swa(lib, ws=None, wsb=1 << 30) == c.CARAT_ERR_WORKSPACE
     assert _swa(lib, B=0) == c.CARAT_OK                               # empty batch: no launch
@@ -136,6 +138,7 @@ def test_global_argument_checks(lib):
     assert _glob(lib, vc=MISALIGNED) == c.CARAT_ERR_INVALID_ARG
     assert _glob(lib, d=64) == c.CARAT_ERR_UNSUPPORTED
     assert _glob(lib, k=15, hq=32, hkv=2) == c.CARAT_ERR_UNSUPPORTED  # 240 rows
+    assert _glob(lib, k=1, hq=128, hkv=1) == c.CARAT_ERR_UNSUPPORTED  # > 64 heads per KV head
     assert _glob(lib, wsb=1024) == c.CARAT_ERR_WORKSPACE
     assert _glob(lib, B=0) == c.CARAT_OK
 
@@ -186,3 +189,39 @@ def test_python_status_text_matches_library(lib):
     from sliding_window_gqa_ring_gb300 import carat
     for code in range(6):
         assert carat.status_string(code) == lib.carat_status_string(code).decode()
+
+
+def test_binding_checks_caches_against_queries(lib):
+    """The binding rejects caches whose element type, shape or head_dim does
+    not match the queries before calling the library (the C ABI sees only
+    pointers and sizes, so a kernel would read past such a buffer)."""
+    import torch
+
+    from sliding_window_gqa_ring_gb300 import carat
+    q = torch.zeros((2, 1, 16, 256), dtype=torch.bfloat16)
+    out = torch.zeros((2, 1, 16, 256), dtype=torch.float32)
+    ctx = torch.zeros((2,), dtype=torch.int32)
+    ring = torch.zeros((2, 1024, 8, 256), dtype=torch.bfloat16)
+    ring8 = torch.zeros((2, 1024, 8, 256), dtype=torch.uint8)
+    ring_d = torch.zeros((2, 1024, 8, 128), dtype=torch.bfloat16)
+    ws = torch.zeros(256, dtype=torch.uint8)
+    before = lib.carat_kernel_launches()
+    for fn, kw in ((carat.carat_swa_attention, {"workspace": ws}),
+                   (carat.carat_swa_attention_noalloc, {})):
+        with pytest.raises(TypeError):
+            fn(out, q, ring8, ring8, ctx, scale=0.0625, **kw)        # FP8 ring, bf16 kernel
+        with pytest.raises(TypeError):
+            fn(out, q, ring, ring8, ctx, scale=0.0625, **kw)         # K and V types differ
+        with pytest.raises(ValueError):
+            fn(out, q, ring_d, ring_d, ctx, scale=0.0625, **kw)      # head_dim 128 vs 256
+        with pytest.raises(ValueError):
+            fn(out[:1], q, ring, ring, ctx, scale=0.0625, **kw)      # out shape
+        with pytest.raises(ValueError):
+            fn(out, q, ring, ring, ctx[:1], scale=0.0625, **kw)      # context_lengths shape
+    with pytest.raises(TypeError):
+        carat.carat_swa_attention_fp8(out, q, ring, ring, ctx, scale=0.0625, k_scale=1.0,
+                                      v_scale=1.0, workspace=ws)     # bf16 ring, FP8 kernel
+    with pytest.raises(ValueError):
+        carat.carat_global_verify_attention(out, q, ring_d, ring_d, ctx, scale=0.0625,
+                                            workspace=ws)
+    assert lib.carat_kernel_launches() == before
