@@ -13,6 +13,13 @@ Every layer call streams > 400 MB, more than the 129 MB L2, so no L2 flush is
 needed between steps.  Timed steps repeat the same step at fixed positions (same
 work every step).
 
+The line's `configs` key times the single-layer workloads one call at a time
+(L2 flushed before each call): the single-request sliding decode (key count
+1500), the batched sliding decode (56 requests), the single-request global
+verify (6005 keys, 4 proposals) and the 8-request global verify sweeps (4 and
+15 proposals), with the launch floor and the pages' unfused design of the
+global verify as an ablation.
+
   python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 
 With --impl reference the fp64 CPU oracle is timed instead, on a bounded
@@ -266,6 +273,120 @@ def time_oracle(jobs, threads):
 
 
 # ---------------------------------------------------------------------------
+# Per-call timings of the single-layer workloads (configs 1-4)
+# ---------------------------------------------------------------------------
+
+def config_attention_bytes(w):
+    """Algorithmic bytes of one attention call of workload w: each K/V row of
+    every request's window (sliding) or key range (global) once, its queries
+    and its fp32 outputs."""
+    total = 0
+    row = w.kv_heads * w.head_dim * 2
+    for b in range(w.batch):
+        kc = int(w.key_counts[b])
+        keys = kc - max(0, kc - w.proposal_count - w.window + 1) if w.window else kc
+        total += keys * row * 2 + w.proposal_count * w.q_heads * w.head_dim * (2 + 4)
+    return total
+
+
+def median_call_us(fn, reps, flush, stream):
+    """Median over reps of one call timed with CUDA events on `stream`, with
+    the L2 flushed (a write larger than L2) before each timed call."""
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e3)
+    return statistics.median(times)
+
+
+def run_configs(dev, reps, peak, peak_kind, ablation_reps):
+    """Configs 1-4 (the single-layer workloads): append alone, attention
+    alone and the fused append+attention call, each the median of `reps`
+    L2-flushed calls; the launch floor; and the unfused design of the pages as
+    an ablation on the global workloads."""
+    import torch
+
+    from sliding_window_gqa_ring_gb300 import ablation, carat, engine, synth
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    floor1 = median_call_us(lambda: carat.carat_launch_floor(False), reps, flush, stream)
+    floor2 = median_call_us(lambda: carat.carat_launch_floor(True), reps, flush, stream)
+    rows = []
+    for w in (synth.sliding_single(), synth.sliding_batched(), synth.global_single(),
+              synth.global_sweep(4), synth.global_sweep(15)):
+        if w.window:
+            layer = engine.SlidingLayer(w.batch, window=w.window, q_heads=w.q_heads,
+                                        kv_heads=w.kv_heads, head_dim=w.head_dim,
+                                        max_proposals=w.proposal_count, scale=w.scale,
+                                        device=dev)
+            inp = engine.stage_sliding(w, 0, layer)
+        else:
+            layer = engine.GlobalLayer(w.batch, capacity=w.capacity, q_heads=w.q_heads,
+                                       kv_heads=w.kv_heads, head_dim=w.head_dim,
+                                       max_proposals=w.proposal_count, scale=w.scale,
+                                       device=dev)
+            inp = engine.stage_global(w, 0, layer, keep_history=False)
+        inp.host.clear()
+        out = torch.empty(inp.queries.shape, dtype=torch.float32, device=dev)
+
+        def append():
+            layer.append(inp.k_new, inp.v_new, inp.context_lengths)
+
+        def attend():
+            layer.attend(inp.queries, inp.context_lengths, out=out)
+
+        def fused():
+            layer.step(inp.queries, inp.k_new, inp.v_new, inp.context_lengths, out=out)
+
+        append()
+        n0 = carat.kernel_launches()
+        attend()
+        attn_launches = carat.kernel_launches() - n0
+        append_us = median_call_us(append, reps, flush, stream)
+        attn_us = median_call_us(attend, reps, flush, stream)
+        fused_us = median_call_us(fused, reps, flush, stream)
+        nbytes = config_attention_bytes(w)
+        floor = floor2 if attn_launches > 1 else floor1
+        gbs = nbytes / (attn_us * 1e3)
+        rows.append({"workload": w.name, "batch": w.batch, "proposal_count": w.proposal_count,
+                     "attention_bytes": nbytes, "append_us": round(append_us, 2),
+                     "attention_us": round(attn_us, 2), "fused_us": round(fused_us, 2),
+                     "attention_gb_s": round(gbs, 1), "attention_frac": round(gbs / peak, 4),
+                     "attention_launches": attn_launches,
+                     "attention_floor_us": round(floor, 2),
+                     "attention_excess_over_floor_us": round(attn_us - floor, 2),
+                     "attention_frac_excluding_floor": round(
+                         nbytes / max(attn_us - floor, 1e-3) / 1e3 / peak, 4)})
+        del layer, inp, out
+        torch.cuda.empty_cache()
+    abl = []
+    if ablation_reps > 0:
+        for w in (synth.global_single(), synth.global_sweep(4), synth.global_sweep(15)):
+            abl.append(ablation.measure(w, ablation_reps, flush))
+            torch.cuda.empty_cache()
+    return {"workloads": rows,
+            "launch_floor_us": {"one_empty_launch": round(floor1, 2),
+                                "empty_launch_then_dependent_launch": round(floor2, 2)},
+            "peak_gb_s": peak, "peak_source": f"{peak_kind} hbm_gbs",
+            "timing": (f"median of {reps} calls, CUDA events on the launching stream, L2 "
+                       "flushed (512 MB write) before every timed call; floor = the same "
+                       "timing of carat_launch_floor (one empty launch, or two with the "
+                       "second a programmatic dependent launch, matching the call's launch "
+                       "count)"),
+            "ablation_unfused_global_verify": abl}
+
+
+# ---------------------------------------------------------------------------
 # The GPU arm
 # ---------------------------------------------------------------------------
 
@@ -498,9 +619,10 @@ def run_carat(args, world, rank, local):
                   "layout": "5 x 64 rings of 8 pages + paged global caches, one K and one V pool"}
         del pstep, p_layers, p_inputs, spool
 
-    # --- FP8 (e4m3) rings for one sliding layer of the same step ("Announcing
-    # Carat ...", section "Server": the KV cache is FP8 e4m3): append + attention
-    # and attention alone, per call; per-tensor scales max|x| / 448 of the layer
+    # --- FP8 (e4m3) rings for one sliding layer of the same step
+    # ("gemma-cuda-hybrid", "Features" / "Server": the KV cache is FP8 e4m3):
+    # append + attention and attention alone, per call; per-tensor scales
+    # max|x| / 448 of the layer
     fp8 = None
     if args.fp8:
         hist = layers[0][1].host["hist"]
@@ -584,6 +706,17 @@ def run_carat(args, world, rank, local):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
     e2e_value = replica_throughput(nbytes["step"], e2e_steps, e2e_ms, world)
 
+    # --- configs 1-4 (rank 0): per-call timings of the single-layer workloads,
+    # under a clock record of their own
+    configs = None
+    if rank == 0 and args.configs:
+        del dstep, layers, glay, ginp, outs, gout, h_in, h_out
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        with ClockSampler(local) as cclk:
+            configs = run_configs(dev, args.config_reps, peak, peak_kind, args.ablation_reps)
+        configs["clocks"] = cclk.summary()
+
     status = carat.carat_get_device_status(clear=True)
     if rank != 0:
         return None
@@ -608,6 +741,7 @@ def run_carat(args, world, rank, local):
         "cuda_graph": graph,
         "shared_pool": pooled,
         "fp8_sliding": fp8,
+        "configs": configs,
         "cpu_baseline": cpu_baseline,
         "parity_sample": parity,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -686,6 +820,12 @@ def main():
                     help="skip the FP8 (e4m3) sliding-layer measurement")
     ap.add_argument("--no-shared-pool", dest="shared_pool", action="store_false",
                     help="skip timing the step with all caches in one shared pool")
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="skip the per-call timings of the single-layer workloads")
+    ap.add_argument("--config-reps", type=int, default=50,
+                    help="L2-flushed calls per median in the single-layer timings")
+    ap.add_argument("--ablation-reps", type=int, default=20,
+                    help="repetitions per median of the unfused-design ablation (0: skip)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

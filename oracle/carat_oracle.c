@@ -44,8 +44,8 @@
  *   history  [hist_len][kv_heads][head_dim], row i holds position hist_base+i
  *   out      [proposal_count][q_heads][head_dim], double
  *
- *  - FP8 KV cache: the cache holds e4m3 codes ("Announcing Carat ...",
- *    section "Server": lossy FP8 e4m3 KV), here with one dequantisation
+ *  - FP8 KV cache: the cache holds e4m3 codes ("gemma-cuda-hybrid",
+ *    "Features" / "Server": FP8 e4m3 KV; "Limitations": lossy), here with one dequantisation
  *    scale per tensor; the attention of such a cache is the attention of its
  *    dequantised values (oracle_attention_request_f64).
  *
@@ -281,9 +281,8 @@ int oracle_displaced_expected(uint16_t *displaced, uint8_t *row_valid,
 }
 
 /*
- * FP8 e4m3 (the KV-cache format of "Announcing Carat: An inference engine
- * designed for Gemma 4", section "Server": the cache is stored in e4m3 and
- * is lossy).  The format: 1 sign bit, 4 exponent bits with bias 7, 3
+ * FP8 e4m3 (the KV-cache format of "gemma-cuda-hybrid", "Features" /
+ * "Server": the cache is stored in e4m3; "Limitations": it is lossy).  The format: 1 sign bit, 4 exponent bits with bias 7, 3
  * mantissa bits; exponent field 0 holds subnormals m/8 * 2^-6; there is no
  * infinity; S.1111.111 is NaN, so the largest finite value is
  * S.1111.110 = 1.75 * 2^8 = 448.

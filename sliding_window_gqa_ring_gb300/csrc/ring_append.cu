@@ -118,7 +118,7 @@ cudaError_t launch_ring_rollback(const AppendParams &p, const int32_t *accepted,
     return cudaGetLastError();
 }
 
-// FP8 rings ("Announcing Carat ...", section "Server": the KV cache is FP8
+// FP8 rings ("gemma-cuda-hybrid", "Features" / "Server": the KV cache is FP8
 // e4m3): the same slot rule, with each new bf16 element stored as
 // e4m3_rn(fp32(x * inv)) -- one binary32 product, then a saturating
 // round-to-nearest-even conversion.  One CTA per (new token j, request b);

@@ -106,9 +106,9 @@ class SlidingLayer:
 
 
 class Fp8SlidingLayer:
-    """K/V rings of one sliding-window layer stored as FP8 e4m3 ("Announcing
-    Carat ...", section "Server": the KV cache is FP8 e4m3 and lossy), one
-    dequantisation scale per tensor.  New rows arrive in bf16 and are
+    """K/V rings of one sliding-window layer stored as FP8 e4m3
+    ("gemma-cuda-hybrid", "Features" / "Server": the KV cache is FP8 e4m3;
+    "Limitations": FP8 KV is lossy), one dequantisation scale per tensor.  New rows arrive in bf16 and are
     quantised by carat_ring_append_fp8; attention reads the e4m3 rings and
     widens them on chip.  step() is append then attention (two launches)."""
 

@@ -369,8 +369,8 @@ def pin_displaced_covers_windows(orc):
 
 
 # ---------------------------------------------------------------------------
-# FP8 (e4m3) KV cache ("Announcing Carat ...", section "Server": the KV cache
-# is stored as FP8 e4m3 and is lossy)
+# FP8 (e4m3) KV cache ("gemma-cuda-hybrid", "Features" / "Server": the KV
+# cache is stored as FP8 e4m3; "Limitations": it is lossy)
 # ---------------------------------------------------------------------------
 
 def _torch_e4m3_value(codes):

@@ -1,7 +1,7 @@
 """GPU parity of the FP8 (e4m3) ring variant against the fp64 oracle.
 
-"Announcing Carat ..." (section "Server") stores the KV cache as FP8 e4m3 and
-calls it lossy, outside the bit-exact comparison.  Here:
+"gemma-cuda-hybrid" ("Features" / "Server") stores the KV cache as FP8 e4m3;
+its "Limitations" call that lossy, outside the bit-exact comparison.  Here:
 
   * the appended e4m3 bytes (rings and displaced rows) equal the oracle's
     quantiser bit for bit (integer work: exact);
