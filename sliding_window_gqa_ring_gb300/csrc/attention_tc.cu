@@ -52,12 +52,15 @@
 //   warp 1      allocates TMEM; one thread issues every tcgen05.mma and the
 //               commits that free stages and signal the softmax warps.
 //   warps 2-5   write NaN outputs for rejected requests, then run the
-//               softmax: thread t owns key t of the tile (TMEM lane t): reads
-//               its N scores, masks by position, finds each row's tile maximum
-//               with a warp transpose-reduction and shared memory, updates the
-//               running max / sum (log2 domain), writes P, rescales O^T in
-//               TMEM when a row's maximum moved; per segment they write the
-//               output or the partial.
+//               softmax: thread t owns key t of the tile (TMEM lane t) and
+//               reads its N scores 16 rows at a time, masked by position; when
+//               some score passes its row's running maximum (log2 domain, kept
+//               in shared memory), the tile's row maxima are reduced (a warp
+//               transpose-reduction, then across the warps) and O^T and the
+//               row sums are rescaled in TMEM; then P is written.  Row sums
+//               are not accumulated by the threads: the MMA thread adds ONES .
+//               P^T into a TMEM buffer L^T with the same P as the PV product.
+//               Per segment they write the output or the partial.
 //   warps 6-9   (FP8 e4m3 caches only, 320 threads) widen each raw e4m3 stage
 //               the producer lands into an f16 stage, in load order, and each
 //               segment's Q into f16 with a power-of-two scale per row.
@@ -99,20 +102,26 @@ struct Layout {
     static constexpr int kOffQ = kOffRaw + NR * kRawBytes;
     static constexpr int kOffP = kOffQ + (D / 64) * kQBlock;
     static constexpr int kPBlock = N * 128;            // 64 keys of P rows
-    static constexpr int kOffRed = kOffP + 2 * kPBlock;
-    // 2 x max buffers + sum buffer (4 warps x N each), one segment's row
-    // maxima and sums kept for its deferred epilogue, then (FP8) the row
-    // score scales of two segments (even, odd)
-    static constexpr int kRedFloats = 3 * 4 * N + (NR > 0 ? 4 : 2) * N;
+    // 8 rows of 128 bytes of ones (bf16, or f16 with FP8 caches): the A operand
+    // of the row-sum product L^T += ONES . P^T, read for every 8-row group
+    static constexpr int kOffOnes = kOffP + 2 * kPBlock;
+    static constexpr int kOffRed = kOffOnes + 1024;
+    // floats of the reduction area: the 4 softmax warps' tile maxima (4 x N),
+    // the running row maxima, this tile's rescale factors, a finished
+    // segment's row maxima, then (FP8) the row score scales of two segments
+    static constexpr int kRedMax = 0, kRedM = 4 * N, kRedAlpha = 5 * N, kRedMrow = 6 * N;
+    static constexpr int kRedQscale = 7 * N;
+    static constexpr int kRedFloats = 7 * N + (NR > 0 ? 2 : 0) * N;
     static constexpr int kOffBar = kOffRed + kRedFloats * 4;
     static constexpr int kNumBars = 2 * NS + 7 + 2 * NR + (NR > 0 ? 2 : 0);
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;   // SkShared
     static constexpr int kBytes = kOffMisc + 128;
     static constexpr int kAlloc = kBytes + 1024;       // base alignment slack
-    // Two S^T buffers and two O^T buffers when they fit the 512 columns, so one
-    // segment's output is written while the next accumulates; else one O^T.
-    static constexpr bool kDoubleO = N * (2 + 2 * KS) <= 512;
-    static constexpr int kTmemUsed = N * (2 + (kDoubleO ? 2 : 1) * KS);
+    // Two S^T buffers, then per segment an O^T buffer (KS blocks of N columns)
+    // and a row-sum buffer L^T (N columns); two of each when they fit the 512
+    // columns, so one segment's output is written while the next accumulates.
+    static constexpr bool kDoubleO = N * (2 + 2 * (KS + 1)) <= 512;
+    static constexpr int kTmemUsed = N * (2 + (kDoubleO ? 2 : 1) * (KS + 1));
     static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64
                                    : kTmemUsed <= 128 ? 128 : kTmemUsed <= 256 ? 256 : 512;
     static_assert(kAlloc <= 232448, "more dynamic shared memory than one CTA may use");
@@ -120,7 +129,7 @@ struct Layout {
     // resident, before the tile's PV product releases any of them.
     static_assert(NS >= KS, "the stage ring must hold a whole V tile");
     static_assert(kOffRaw % 1024 == 0 && kOffQ % 1024 == 0 && kOffP % 1024 == 0 &&
-                      kPBlock % 1024 == 0 &&
+                      kPBlock % 1024 == 0 && kOffOnes % 1024 == 0 &&
                       kQBlock % 1024 == 0,
                   "operand blocks must be 1024-byte aligned for the 128-byte swizzle");
 };
@@ -142,6 +151,10 @@ struct TcPlan {
     int row_groups;
     int pos_per_group;    // proposal positions per row group
     int unit_mode;        // 1: CTA g takes unit g whole (grid = units); 0: stream-K
+    // stream-K with two row groups: CTAs 2r and 2r + 1 walk the same range r
+    // of the (request, KV head) order, one row group each, so each K/V tile is
+    // read by both at about the same time and the second read comes from L2
+    int paired;
 };
 
 // Per-CTA schedule, written by warp 0 before the block-wide barrier and read
@@ -189,8 +202,10 @@ struct SegIter {
     int b, ur, off;
     int id, ntiles, special;
     long long ctx;
+    int rg_fixed;   // paired schedule: this CTA's row group (else -1)
 
-    __device__ void init(const AttnParams &p, const SkShared *sk) {
+    __device__ void init(const AttnParams &p, const SkShared *sk, int rg = -1) {
+        rg_fixed = rg;
         pos = sk->s;
         end = sk->e;
         b = sk->b0;
@@ -202,6 +217,7 @@ struct SegIter {
         special = sk->special0;
     }
 
+    // upr: units per request in the flattened order (KV heads when paired).
     __device__ bool next(const AttnParams &p, int upr, int row_groups, Segment &sg) {
         if (pos >= end || ntiles <= off) return false;
         const long long left = end - pos;
@@ -211,9 +227,15 @@ struct SegIter {
         sg.ctx = ctx;
         sg.ntiles = ntiles;
         sg.special = special;
-        sg.c = ur / row_groups;
-        sg.rg = ur % row_groups;
-        sg.unit = b * upr + ur;
+        if (rg_fixed >= 0) {
+            sg.c = ur;
+            sg.rg = rg_fixed;
+            sg.unit = (b * upr + ur) * row_groups + rg_fixed;
+        } else {
+            sg.c = ur / row_groups;
+            sg.rg = ur % row_groups;
+            sg.unit = b * upr + ur;
+        }
         sg.x0 = off;
         sg.x1 = off + len;
         sg.start = pos;
@@ -251,7 +273,10 @@ __device__ __forceinline__ int warp_max_int(int v) {
 // Runs once per CTA from a cold instruction cache, so it is kept to two short
 // loops (32 requests per pass, the second pass re-reading through L2) rather
 // than unrolled code.
-__device__ __noinline__ void locate_range(const AttnParams &p, int upr, int lane, SkShared *sk) {
+// upr: units per request in the flattened order; the order is cut into
+// `ranges` ranges and this CTA takes range `rix`.
+__device__ __noinline__ void locate_range(const AttnParams &p, int upr, int lane, SkShared *sk,
+                                          int ranges, int rix) {
     long long total = 0;
     int nmax = 0;
 #pragma unroll 1
@@ -268,12 +293,12 @@ __device__ __noinline__ void locate_range(const AttnParams &p, int upr, int lane
     }
     total = warp_sum_ll(total) * upr;
     nmax = warp_max_int(nmax);
-    const long long grid = gridDim.x;
+    const long long grid = ranges;
     long long len = (total + grid - 1) / grid;
     const long long min_len = (nmax + kMaxPieces - 2) / (kMaxPieces - 1);
     if (len < min_len) len = min_len;
     if (len < 1) len = 1;
-    const long long s = (long long)blockIdx.x * len;
+    const long long s = (long long)rix * len;
     const long long e = s + len < total ? s + len : total;
     // First request whose tiles reach past s; its id, context length and
     // special tile come from the lane that read it.
@@ -550,6 +575,9 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
     constexpr bool F8 = NR > 0;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int upr = p.kv_heads * plan.row_groups;   // units per request
+    const bool paired = plan.paired != 0;
+    const int upo = paired ? p.kv_heads : upr;      // units per request in the flattened order
+    const int my_rg = paired ? (int)(blockIdx.x & 1) : -1;
     const bool ring = p.source == KeySource::kRing;
     const bool paged = p.source == KeySource::kPaged;
 
@@ -572,7 +600,7 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
     SkShared *sk = reinterpret_cast<SkShared *>(smem + L::kOffMisc);
     volatile int *abort_flag = &sk->abort_flag;
     float *red = reinterpret_cast<float *>(smem + L::kOffRed);
-    float *s_qscale = red + 14 * N;   // FP8: row score scales of two segments (even, odd)
+    float *s_qscale = red + L::kRedQscale;   // FP8: row score scales of two segments (even, odd)
     uint8_t *s_q = smem + L::kOffQ;
     uint8_t *s_p = smem + L::kOffP;
 
@@ -618,7 +646,7 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
         while (alive_p && cnt < limit) {
             if (!p_have) {
                 if (first_only && psi > 0) return;
-                if (!pit.next(p, upr, plan.row_groups, ps)) return;
+                if (!pit.next(p, upo, plan.row_groups, ps)) return;
                 p_have = true;
                 p_qdone = false;
                 ppart = 0;
@@ -799,26 +827,36 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
             tc::mbar_init(fin, 1);
             sk->abort_flag = 0;
             tc::fence_mbar_init();
-            pol = tc::l2_evict_first_policy();
+            // K/V rows are read once, except by a pair, where the second read
+            // should find them in L2
+            pol = paired ? tc::l2_evict_normal_policy() : tc::l2_evict_first_policy();
         }
         if (plan.unit_mode)
             locate_unit(p, upr, lane, sk);
         else
-            locate_range(p, upr, lane, sk);
+            locate_range(p, upo, lane, sk, paired ? gridDim.x / 2 : gridDim.x,
+                         paired ? blockIdx.x / 2 : blockIdx.x);
         if (lane == 0) {
             // Start streaming before the block-wide barrier: this thread made
             // the barriers, and the first NS stages need no release.
-            pit.init(p, sk);
+            pit.init(p, sk, my_rg);
             produce(F8 ? NR : NS, true);
         }
     } else if (warp == 1) {
         tc::tmem_alloc(&sk->tmem_slot, L::kTmemCols);
         tc::tmem_relinquish();
     } else if (warp < 6) {
+        // The ones block of the row-sum product (64 16-byte pieces), made
+        // visible to the tensor core before the block-wide barrier.
+        const int t = threadIdx.x - 64;
+        if (t < 64) {
+            const uint32_t one2 = F8 ? 0x3C003C00u : 0x3F803F80u;   // two f16 / bf16 ones
+            reinterpret_cast<uint4 *>(smem + L::kOffOnes)[t] = make_uint4(one2, one2, one2, one2);
+            tc::fence_proxy_async_smem();
+        }
         // Requests rejected on the device get NaN outputs and a status bit
         // (requests b = blockIdx.x, blockIdx.x + grid, ...); their units have
         // no tiles in the flattened order.
-        const int t = threadIdx.x - 64;
         for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
             int id;
             long long ctx;
@@ -833,9 +871,14 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = sk->tmem_slot;
-    // O^T buffer of segment si: KS blocks of N columns (S^T buffers: 0, N)
+    // O^T buffer of segment si: KS blocks of N columns (S^T buffers: 0, N);
+    // its row sums L^T: N columns after the O^T buffers
     auto tmem_o_of = [&](int si) -> uint32_t {
         return tmem + 2 * N + (L::kDoubleO ? (uint32_t)(si & 1) : 0u) * KS * N;
+    };
+    auto tmem_l_of = [&](int si) -> uint32_t {
+        return tmem + 2 * N + (L::kDoubleO ? 2u : 1u) * KS * N +
+               (L::kDoubleO ? (uint32_t)(si & 1) : 0u) * N;
     };
 
     if (warp == 0) {
@@ -869,13 +912,17 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
                                              : tc::idesc_bf16_f32(128, N, true, false);
             const uint32_t q_base = tc::smem_u32(s_q);
             const uint32_t p_base = tc::smem_u32(s_p);
+            // ONES as a K-major operand whose every 8-row group reads the same
+            // 8 rows of ones (stride 0), so the product is the column sums of
+            // P^T, the same in every lane of L^T.
+            const uint64_t ones_desc = tc::sdesc_sw128(tc::smem_u32(smem + L::kOffOnes), 16, 0);
             SegIter it;
-            it.init(p, sk);
+            it.init(p, sk, my_rg);
             Segment sg;
             bool alive = true;
             uint32_t mcnt = 0, gt = 0;   // stages consumed, tiles before this segment
             int si = 0;
-            while (alive && it.next(p, upr, plan.row_groups, sg)) {
+            while (alive && it.next(p, upo, plan.row_groups, sg)) {
                 const int n = sg.x1 - sg.x0;
                 if (!wait_or_abort(F8 ? &qs_ready[si & 1] : q_full, F8 ? (si >> 1) & 1 : si & 1,
                                    abort_flag, p.dev_status)) {
@@ -884,6 +931,7 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
                 }
                 tc::tc_fence_after();
                 const uint32_t tmem_o = tmem_o_of(si);
+                const uint32_t tmem_l = tmem_l_of(si);
                 int spec_stage = 0;   // stage holding the special tile's K and V rows
                 const bool sp0 = order_tile(sg, sg.x0) == sg.special;   // segment leads with it
                 for (int step = 0; step <= n && alive; ++step) {
@@ -998,6 +1046,18 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
                             ++mcnt;
                         }
                         if (!alive) break;
+                        // Row sums of the same P: L^T += ONES . P^T over the tile's keys.
+                        if (special) {
+                            tc::mma_bf16_ss(tmem_l, ones_desc, tc::sdesc_sw128(p_base, 16, 1024),
+                                            idesc_qk, x > 0);
+                        } else {
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint64_t pp = tc::sdesc_sw128(
+                                    p_base + (kk / 4) * L::kPBlock + (kk % 4) * 32, 16, 1024);
+                                tc::mma_bf16_ss(tmem_l, ones_desc, pp, idesc_qk, (x > 0 || kk > 0));
+                            }
+                        }
                         tc::mma_commit(o_done);
                     }
                 }
@@ -1012,17 +1072,22 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
         }
     } else if (warp < 6) {
         // ------------------------------------------------------------ softmax
+        // Thread t owns key t of each tile (TMEM lane t).  Per-row state lives
+        // in shared memory (running maxima) and tensor memory (row sums, L^T),
+        // so a thread holds only 16 rows' scores at a time whatever N is.
         const int q4 = warp & 3;              // TMEM lane quadrant this warp may access
         const int t = q4 * 32 + lane;         // key of the tile / d within an O block
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         SegIter it;
-        it.init(p, sk);
+        it.init(p, sk, my_rg);
         Segment sg;
         bool alive = true;
         uint32_t gt = 0, cnt_base = 0;       // tiles and stages before this segment
         int si = 0;                          // segments before this one
-        float *s_mrow = red + 12 * N;        // a finished segment's row maxima
-        float *s_lrow = red + 13 * N;        // and row sums
+        float *red_max = red + L::kRedMax;   // [4 warps][N] maxima of each warp's 32 keys
+        float *s_m = red + L::kRedM;         // running row maxima of the current segment
+        float *s_alpha = red + L::kRedAlpha; // this tile's rescale factor per row
+        float *s_mrow = red + L::kRedMrow;   // a finished segment's row maxima
         // The epilogue of a finished segment, run once the next segment's first
         // tile is under way (or at once with a single O^T buffer).
         struct PendingEpi {
@@ -1031,81 +1096,63 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
             int si, b, c, pos0, row0, rows_here;
             long long start;
         } pend{};
-        constexpr int kLdPair = N >= 32 ? 2 : 1;   // TMEM loads issued per wait
-        constexpr bool kSkipMax = N <= 16;         // skip the row-max reduction when idle
         auto write_segment = [&](const PendingEpi &pe) {
             const uint32_t tmo = tmem_o_of(pe.si);
-            if (pe.whole) {
-                // The segment saw every key of its rows: normalise and write.
-                // Row r = j * group + h' goes to out[b][j][c * group + h'].
-                float inv_l[N];
-#pragma unroll
-                for (int r = 0; r < N; ++r) inv_l[r] = p.out_scale / s_lrow[r];
-#pragma unroll
-                for (int ob = 0; ob < KS; ++ob) {
-                    float *obase = p.out +
-                                   (((size_t)pe.b * p.k + pe.pos0) * p.q_heads +
-                                    (size_t)pe.c * p.group) * D + ob * 128 + t;
-                    int jr = 0, hp = 0;
-#pragma unroll
-                    for (int cb = 0; cb < N / 16; cb += kLdPair) {
-                        // two 16-column loads in flight before one wait
-                        uint32_t r16[kLdPair][16];
-#pragma unroll
-                        for (int h = 0; h < kLdPair; ++h)
-                            tc::tmem_ld16(tmo + ob * N + lane_off + (cb + h) * 16, r16[h]);
-                        tc::tmem_ld_wait();
-#pragma unroll
-                        for (int h = 0; h < kLdPair; ++h) {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const int r = (cb + h) * 16 + e;
-                                if (r < pe.rows_here)
-                                    obase[((size_t)jr * p.q_heads + hp) * D] =
-                                        __uint_as_float(r16[h][e]) * inv_l[r];
-                                if (++hp == p.group) {
-                                    hp = 0;
-                                    ++jr;
-                                }
-                            }
-                        }
-                    }
-                }
-                return;
-            }
-            // A piece of a split unit: its partial goes to this CTA's slot
-            // (0: the range's first segment, 1: its last).
+            const uint32_t tml = tmem_l_of(pe.si);
+            // A piece of a split unit goes to this CTA's partial slot (0: the
+            // range's first segment, 1: its last).
             const int slot = pe.start == sk->s ? 0 : 1;
             const size_t base = ((size_t)blockIdx.x * 2 + slot) * N;
-            if (t == 0) {
+#pragma unroll 1
+            for (int cb = 0; cb < N / 16; ++cb) {
+                // row sums of these 16 rows (every lane of L^T holds them)
+                uint32_t l16[16];
+                tc::tmem_ld16(tml + lane_off + cb * 16, l16);
+                uint32_t o16[KS][16];
 #pragma unroll
-                for (int r = 0; r < N; ++r)
-                    if (r < pe.rows_here) p.part_ml[base + r] = make_float2(s_mrow[r], s_lrow[r]);
-            }
+                for (int ob = 0; ob < KS; ++ob)
+                    tc::tmem_ld16(tmo + ob * N + lane_off + cb * 16, o16[ob]);
+                tc::tmem_ld_wait();
+                if (pe.whole) {
+                    // The segment saw every key of its rows: normalise and write.
+                    // Row r = j * group + h' goes to out[b][j][c * group + h'].
+                    int jr = (cb * 16) / p.group, hp = (cb * 16) - jr * p.group;
 #pragma unroll
-            for (int ob = 0; ob < KS; ++ob) {
+                    for (int e = 0; e < 16; ++e) {
+                        const int r = cb * 16 + e;
+                        if (r < pe.rows_here) {
+                            const float inv = p.out_scale / __uint_as_float(l16[e]);
+                            float *o = p.out + (((size_t)pe.b * p.k + pe.pos0 + jr) * p.q_heads +
+                                                (size_t)pe.c * p.group + hp) * D + t;
 #pragma unroll
-                for (int cb = 0; cb < N / 16; cb += kLdPair) {
-                    uint32_t r16[kLdPair][16];
+                            for (int ob = 0; ob < KS; ++ob)
+                                o[ob * 128] = __uint_as_float(o16[ob][e]) * inv;
+                        }
+                        if (++hp == p.group) {
+                            hp = 0;
+                            ++jr;
+                        }
+                    }
+                } else {
 #pragma unroll
-                    for (int h = 0; h < kLdPair; ++h)
-                        tc::tmem_ld16(tmo + ob * N + lane_off + (cb + h) * 16, r16[h]);
-                    tc::tmem_ld_wait();
+                    for (int e = 0; e < 16; ++e) {
+                        const int r = cb * 16 + e;
+                        if (r < pe.rows_here) {
+                            if (t == 0)
+                                p.part_ml[base + r] =
+                                    make_float2(s_mrow[r], __uint_as_float(l16[e]));
 #pragma unroll
-                    for (int h = 0; h < kLdPair; ++h) {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int r = (cb + h) * 16 + e;
-                            if (r < pe.rows_here)
+                            for (int ob = 0; ob < KS; ++ob)
                                 p.part_o[(base + r) * D + ob * 128 + t] =
-                                    __uint_as_float(r16[h][e]) * p.out_scale;
+                                    __uint_as_float(o16[ob][e]) * p.out_scale;
                         }
                     }
                 }
             }
         };
-        while (alive && it.next(p, upr, plan.row_groups, sg)) {
+        while (alive && it.next(p, upo, plan.row_groups, sg)) {
             const uint32_t tmem_o = tmem_o_of(si);
+            const uint32_t tmem_l = tmem_l_of(si);
             const int n = sg.x1 - sg.x0;
             if (t == 0 && sg.x0 == 0 && !plan.unit_mode) {
                 // The unit's entry for the merge launch: where it starts in
@@ -1156,37 +1203,17 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
                     break;
                 }
             }
-            float m_run[N], l_part[N];
-#pragma unroll
-            for (int r = 0; r < N; ++r) {
-                m_run[r] = -INFINITY;
-                l_part[r] = 0.f;
-            }
             int idx = 0;
             for (; idx < n; ++idx) {
                 const uint32_t tile = gt + idx;
                 const int i = order_tile(sg, sg.x0 + idx);
-                // warp-uniform: the TMEM load below is warp-collective
+                // warp-uniform: the TMEM loads below are warp-collective
                 const bool w_ok = __all_sync(kFull, alive && wait_or_abort(&s_full[tile & 1],
                                                                            (tile >> 1) & 1,
                                                                            abort_flag,
                                                                            p.dev_status));
                 const uint32_t tmem_s = tmem + (tile & 1) * N;
-                float x[N];
-                if (w_ok) {
-                    tc::tc_fence_after();
-#pragma unroll
-                    for (int cb = 0; cb < N / 16; ++cb) {
-                        uint32_t r16[16];
-                        tc::tmem_ld16(tmem_s + lane_off + cb * 16, r16);
-                        tc::tmem_ld_wait();
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) x[cb * 16 + e] = __uint_as_float(r16[e]);
-                    }
-                } else {
-#pragma unroll
-                    for (int r = 0; r < N; ++r) x[r] = 0.f;
-                }
+                if (w_ok) tc::tc_fence_after();
                 // Position of key t of tile i and which rows may see it.
                 KeyInfo ki;
                 if (i == new_tile) {
@@ -1219,109 +1246,142 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
                     if (jlo < jhi)
                         rowmask = low_bits((int)jhi * p.group) & ~low_bits((int)jlo * p.group);
                 }
-                float tmax[N];
-                bool need = false;   // a score past its row's running maximum + slack
+                // Scores of rows 16 cb .. 16 cb + 15 (log2 units), -inf where the
+                // row may not see the key.  A 16-row tile is one chunk: its scores
+                // and row maxima stay in registers across both passes below.
+                auto load_chunk = [&](int cb, float (&v)[16]) {
+                    uint32_t r16[16];
+                    tc::tmem_ld16(tmem_s + lane_off + cb * 16, r16);
+                    tc::tmem_ld_wait();
 #pragma unroll
-                for (int r = 0; r < N; ++r) {
-                    x[r] = ((rowmask >> r) & 1ull) ? x[r] * (F8 ? qsc[r] : p.scale_log2)
-                                                   : -INFINITY;
-                    if constexpr (kSkipMax) need |= x[r] > m_run[r] + kRescaleSlack;
-                }
-                // The running maximum of a row moves only when the tile's maximum
+                    for (int e = 0; e < 16; ++e) {
+                        const int r = cb * 16 + e;
+                        v[e] = ((rowmask >> r) & 1ull)
+                                   ? __uint_as_float(r16[e]) * (F8 ? qsc[r] : p.scale_log2)
+                                   : -INFINITY;
+                    }
+                };
+                constexpr bool kOneChunk = N == 16;
+                float x1[16];
+                if (kOneChunk && w_ok) load_chunk(0, x1);
+                // A row's running maximum is replaced only when a tile's maximum
                 // exceeds it by more than kRescaleSlack (log2 units; P stays below
                 // 2^kRescaleSlack and O^T is rescaled only when a maximum really
-                // moves).  With 16 rows, one predicated barrier tells all 128
-                // threads whether any row of this tile does; only then are the
-                // tile's row maxima reduced (a warp transpose-reduction, then
-                // across the 4 warps in shared memory).  Either way the result is
-                // the same.  (With more rows the extra registers cost more than the
-                // skipped reduction saves: always reduce.)
-                const bool reduce =
-                    !kSkipMax || named_bar_softmax_any(need || !w_ok || *abort_flag);
-                float alpha[N];
+                // moves).  Pass 1 asks whether any score of this tile does (a
+                // segment's first tile always sets the maxima); one predicated
+                // barrier tells all 128 threads, and only then are the tile's row
+                // maxima reduced (a warp transpose-reduction per 16 rows, then
+                // across the 4 warps by one thread per row).
+                bool need = idx == 0;
+                if (!need && w_ok) {
+#pragma unroll 1
+                    for (int cb = 0; cb < N / 16; ++cb) {
+                        float v[16];
+                        if (kOneChunk) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) v[e] = x1[e];
+                        } else {
+                            load_chunk(cb, v);
+                        }
+#pragma unroll
+                        for (int e = 0; e < 16; e += 4) {
+                            const float4 m4 = *reinterpret_cast<const float4 *>(s_m + cb * 16 + e);
+                            need |= (v[e] > m4.x + kRescaleSlack) | (v[e + 1] > m4.y + kRescaleSlack) |
+                                    (v[e + 2] > m4.z + kRescaleSlack) | (v[e + 3] > m4.w + kRescaleSlack);
+                        }
+                    }
+                }
                 bool rescale = false;
-                if (reduce) {
+                if (named_bar_softmax_any(need || !w_ok || *abort_flag)) {
+#pragma unroll 1
+                    for (int cb = 0; cb < N / 16; ++cb) {
+                        float v[16];
+                        if (w_ok && kOneChunk) {
 #pragma unroll
-                    for (int r = 0; r < N; ++r) tmax[r] = x[r];
-                    const int rb = warp_transpose_reduce<N, true>(tmax, lane);
-                    float *red_max = red + (idx & 1) * 4 * N;
-                    constexpr int kHeld = N >= 32 ? N / 32 : 1;
+                            for (int e = 0; e < 16; ++e) v[e] = x1[e];
+                        } else if (w_ok) {
+                            load_chunk(cb, v);
+                        } else {
 #pragma unroll
-                    for (int e = 0; e < kHeld; ++e) red_max[q4 * N + rb + e] = tmax[e];
+                            for (int e = 0; e < 16; ++e) v[e] = -INFINITY;
+                        }
+                        const int rb = warp_transpose_reduce<16, true>(v, lane);
+                        red_max[q4 * N + cb * 16 + rb] = v[0];
+                    }
                     if (named_bar_softmax_any(!w_ok || *abort_flag)) {
                         alive = false;
                         break;
                     }
-#pragma unroll
-                    for (int r = 0; r < N; r += 4) {
-                        float4 a0 = *reinterpret_cast<const float4 *>(red_max + 0 * N + r);
-                        float4 a1 = *reinterpret_cast<const float4 *>(red_max + 1 * N + r);
-                        float4 a2 = *reinterpret_cast<const float4 *>(red_max + 2 * N + r);
-                        float4 a3 = *reinterpret_cast<const float4 *>(red_max + 3 * N + r);
-                        tmax[r + 0] = fmaxf(fmaxf(a0.x, a1.x), fmaxf(a2.x, a3.x));
-                        tmax[r + 1] = fmaxf(fmaxf(a0.y, a1.y), fmaxf(a2.y, a3.y));
-                        tmax[r + 2] = fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z));
-                        tmax[r + 3] = fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w));
-                    }
-#pragma unroll
-                    for (int r = 0; r < N; ++r) {
-                        const float mn = tmax[r] > m_run[r] + kRescaleSlack ? tmax[r] : m_run[r];
+                    bool moved = false;
+                    if (t < N) {
+                        const float tmax = fmaxf(fmaxf(red_max[t], red_max[N + t]),
+                                                 fmaxf(red_max[2 * N + t], red_max[3 * N + t]));
+                        const float m_old = idx == 0 ? -INFINITY : s_m[t];
+                        const float mn = tmax > m_old + kRescaleSlack ? tmax : m_old;
                         const float ms = mn == -INFINITY ? 0.f : mn;
-                        alpha[r] = fast_exp2(m_run[r] - ms);
-                        const float pr = fast_exp2(x[r] - ms);
-                        l_part[r] = l_part[r] * alpha[r] + pr;
-                        x[r] = pr;
-                        rescale |= (mn != m_run[r]) && (m_run[r] != -INFINITY);
-                        m_run[r] = mn;
+                        s_alpha[t] = fast_exp2(m_old - ms);
+                        s_m[t] = mn;
+                        moved = mn != m_old && m_old != -INFINITY;
                     }
-                } else {
-                    // every maximum stays: alpha = 1
-#pragma unroll
-                    for (int r = 0; r < N; ++r) {
-                        const float ms = m_run[r] == -INFINITY ? 0.f : m_run[r];
-                        const float pr = fast_exp2(x[r] - ms);
-                        l_part[r] += pr;
-                        x[r] = pr;
-                        alpha[r] = 1.f;
-                    }
+                    rescale = named_bar_softmax_any(moved);
                 }
                 // PV of the previous tile (of this segment or the one before)
-                // must be done before P and O are touched.
+                // must be done before P, O^T and L^T are touched.
                 if (tile > 0) {
                     alive = __all_sync(kFull, wait_or_abort(o_done, (tile - 1) & 1, abort_flag,
                                                             p.dev_status));
                     tc::tc_fence_after();
                 }
                 if (alive) {
-                    // P^T as a K-major operand: row r, key t (two 64-key blocks).
-                    uint8_t *pblk = s_p + (t / 64) * L::kPBlock;
-                    const uint32_t col = t % 64;
-#pragma unroll
-                    for (int r = 0; r < N; ++r) {
-                        uint16_t h;
-                        if constexpr (F8)
-                            h = __half_as_ushort(__float2half_rn(x[r]));
-                        else
-                            h = __bfloat16_as_ushort(__float2bfloat16_rn(x[r]));
-                        *reinterpret_cast<uint16_t *>(pblk + tc::sw128_offset(r, col)) = h;
-                    }
                     if (idx > 0 && rescale) {
-#pragma unroll
-                        for (int ob = 0; ob < KS; ++ob) {
-#pragma unroll
-                            for (int cb = 0; cb < N / 16; ++cb) {
+                        // A row's maximum moved: scale its O^T column and row sum.
+#pragma unroll 1
+                        for (int cb = 0; cb < N / 16; ++cb) {
+#pragma unroll 1
+                            for (int ob = 0; ob <= KS; ++ob) {
                                 uint32_t r16[16];
-                                const uint32_t addr = tmem_o + ob * N + lane_off + cb * 16;
+                                const uint32_t addr =
+                                    (ob < KS ? tmem_o + ob * N : tmem_l) + lane_off + cb * 16;
                                 tc::tmem_ld16(addr, r16);
                                 tc::tmem_ld_wait();
 #pragma unroll
                                 for (int e = 0; e < 16; ++e)
                                     r16[e] = __float_as_uint(__uint_as_float(r16[e]) *
-                                                             alpha[cb * 16 + e]);
+                                                             s_alpha[cb * 16 + e]);
                                 tc::tmem_st16(addr, r16);
                             }
                         }
                         tc::tmem_st_wait();
+                    }
+                    // Pass 2: P = 2^(score - row maximum), as the K-major operand
+                    // P^T: row r, key t (two 64-key blocks).
+                    uint8_t *pblk = s_p + (t / 64) * L::kPBlock;
+                    const uint32_t col = t % 64;
+#pragma unroll 1
+                    for (int cb = 0; cb < N / 16; ++cb) {
+                        float v[16], m[16];
+                        if (kOneChunk) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) v[e] = x1[e];
+                        } else {
+                            load_chunk(cb, v);
+                        }
+#pragma unroll
+                        for (int e = 0; e < 16; e += 4)
+                            *reinterpret_cast<float4 *>(m + e) =
+                                *reinterpret_cast<const float4 *>(s_m + cb * 16 + e);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int r = cb * 16 + e;
+                            const float pr =
+                                fast_exp2(v[e] - (m[e] == -INFINITY ? 0.f : m[e]));
+                            uint16_t h;
+                            if constexpr (F8)
+                                h = __half_as_ushort(__float2half_rn(pr));
+                            else
+                                h = __bfloat16_as_ushort(__float2bfloat16_rn(pr));
+                            *reinterpret_cast<uint16_t *>(pblk + tc::sw128_offset(r, col)) = h;
+                        }
                     }
                     // Rows of the tile that hold no token of this request: zero their
                     // V rows so their contents cannot reach O through P = 0.
@@ -1455,22 +1515,11 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
             }
             if (!alive) break;
             // ------------------------------------------------ segment end
-            // Row sums over the 128 key lanes, then (max, sum) per row to
-            // shared memory for the epilogue.
-            const int rbl = warp_transpose_reduce<N, false>(l_part, lane);
-            float *red_sum = red + 2 * 4 * N;
-            constexpr int kHeldL = N >= 32 ? N / 32 : 1;
-#pragma unroll
-            for (int e = 0; e < kHeldL; ++e) red_sum[q4 * N + rbl + e] = l_part[e];
+            // The row maxima go to s_mrow for the epilogue (the row sums stay in
+            // this segment's L^T until then).
             alive = !named_bar_softmax_any(!alive || *abort_flag);
             if (!alive) break;
-            if (t == 0) {
-#pragma unroll
-                for (int r = 0; r < N; ++r) {
-                    s_lrow[r] = red_sum[r] + red_sum[N + r] + red_sum[2 * N + r] + red_sum[3 * N + r];
-                    s_mrow[r] = m_run[r];
-                }
-            }
+            if (t < N) s_mrow[t] = s_m[t];
             pend.on = true;
             pend.whole = sg.x0 == 0 && sg.x1 == sg.ntiles;
             pend.si = si;
@@ -1516,12 +1565,12 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
         if constexpr (F8) {
             const int t = threadIdx.x - kThreads;
             SegIter it;
-            it.init(p, sk);
+            it.init(p, sk, my_rg);
             Segment sg;
             bool alive = true;
             uint32_t ccnt = 0;   // raw stages widened so far
             int si = 0;
-            while (alive && it.next(p, upr, plan.row_groups, sg)) {
+            while (alive && it.next(p, upo, plan.row_groups, sg)) {
                 const int n = sg.x1 - sg.x0;
                 alive = __all_sync(kFull, wait_or_abort(q_full, si & 1, abort_flag, p.dev_status));
                 if (!alive) break;
@@ -1610,13 +1659,14 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
 // the rescaling an online softmax applies between key blocks; pieces with
 // l_s = 0 saw no visible key.  One CTA per (unit, row), one thread per 16
 // bytes of the row: the unit table says whether the unit was split and
-// where it starts; piece q sits in slot (g, 0/1) of CTA g = first CTA + q.  It starts before the attention grid
+// where it starts; piece q sits in slot 0 or 1 of the CTA holding range g =
+// first range + q (with the paired schedule, CTA 2g + the unit's row group).  It starts before the attention grid
 // ends (programmatic dependent launch) and waits for it with
 // griddepcontrol.wait, which also makes the grid's writes visible.
 template <int D>
 __global__ void __launch_bounds__(D / 4) attn_fixup_kernel(const AttnParams p, int upr,
                                                             int row_groups, int pos_per_group,
-                                                            int slot_rows, int slots) {
+                                                            int slot_rows, int slots, int paired) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int u = blockIdx.x, r = blockIdx.y;   // unit, row within its row group
     const int b = u / upr, ur = u % upr;
@@ -1647,8 +1697,9 @@ __global__ void __launch_bounds__(D / 4) attn_fixup_kernel(const AttnParams p, i
     }
     const int np = (int)(g_last - g_first + 1);
     auto piece_base = [&](int q) -> size_t {
-        const long long gq = g_first + q;
-        return ((size_t)gq * 2 + (u0 > gq * len ? 1 : 0)) * slot_rows;
+        const long long gq = g_first + q;                   // range holding piece q
+        const long long cta = paired ? 2 * gq + rg : gq;    // its CTA for this row group
+        return ((size_t)cta * 2 + (u0 > gq * len ? 1 : 0)) * slot_rows;
     };
     // weights 2^(m_q - M) / L of the pieces, by warp 0 (each lane reads the
     // (max, sum) pairs of pieces lane and lane + 32 once)
@@ -1720,6 +1771,7 @@ cudaError_t launch_tc(const AttnParams &p, const TcPlan &plan, const TcMaps &map
         if (e != cudaSuccess) return e;
         configured_devices[dev] = 1;
     }
+    if (plan.paired) grid &= ~1;   // CTAs come in pairs, one per row group
     kernel<<<grid, NR > 0 ? kThreads + kConvThreads : kThreads, L::kAlloc, stream>>>(p, plan, maps);
     count_launches(1);
     e = cudaGetLastError();
@@ -1738,7 +1790,7 @@ cudaError_t launch_tc(const AttnParams &p, const TcPlan &plan, const TcMaps &map
     cfg.numAttrs = 1;
     const int upr = p.kv_heads * plan.row_groups;
     e = cudaLaunchKernelEx(&cfg, attn_fixup_kernel<D>, p, upr, plan.row_groups,
-                           plan.pos_per_group, N, grid);
+                           plan.pos_per_group, N, plan.paired ? grid / 2 : grid, plan.paired);
     count_launches(1);
     return e;
 }
@@ -1781,6 +1833,7 @@ cudaError_t launch_attention_tc(const AttnParams &p, int grid, bool unit_mode, b
     plan.pos_per_group = n / p.group;
     if (plan.pos_per_group > p.k) plan.pos_per_group = p.k;
     plan.row_groups = (p.k + plan.pos_per_group - 1) / plan.pos_per_group;
+    plan.paired = (!unit_mode && plan.row_groups == 2 && grid >= 2) ? 1 : 0;
 
     TcMaps maps{};
     const uint64_t D = (uint64_t)p.head_dim;
