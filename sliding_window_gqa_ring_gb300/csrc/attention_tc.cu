@@ -1203,6 +1203,14 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
                     break;
                 }
             }
+            // 16-row tiles keep the segment's row maxima in registers; shared
+            // memory serves only the reductions.
+            constexpr bool kOneChunk = N == 16;
+            float mreg[kOneChunk ? 16 : 1];
+            if constexpr (kOneChunk) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) mreg[e] = -INFINITY;
+            }
             int idx = 0;
             for (; idx < n; ++idx) {
                 const uint32_t tile = gt + idx;
@@ -1256,12 +1264,10 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         const int r = cb * 16 + e;
-                        v[e] = ((rowmask >> r) & 1ull)
-                                   ? __uint_as_float(r16[e]) * (F8 ? qsc[r] : p.scale_log2)
-                                   : -INFINITY;
+                        const float sc = F8 ? qsc[r] : p.scale_log2;
+                        v[e] = ((rowmask >> r) & 1ull) ? __uint_as_float(r16[e]) * sc : -INFINITY;
                     }
                 };
-                constexpr bool kOneChunk = N == 16;
                 float x1[16];
                 if (kOneChunk && w_ok) load_chunk(0, x1);
                 // A row's running maximum is replaced only when a tile's maximum
@@ -1283,11 +1289,19 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
                         } else {
                             load_chunk(cb, v);
                         }
+                        if constexpr (kOneChunk) {
 #pragma unroll
-                        for (int e = 0; e < 16; e += 4) {
-                            const float4 m4 = *reinterpret_cast<const float4 *>(s_m + cb * 16 + e);
-                            need |= (v[e] > m4.x + kRescaleSlack) | (v[e + 1] > m4.y + kRescaleSlack) |
-                                    (v[e + 2] > m4.z + kRescaleSlack) | (v[e + 3] > m4.w + kRescaleSlack);
+                            for (int e = 0; e < 16; ++e) need |= v[e] > mreg[e] + kRescaleSlack;
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; e += 4) {
+                                const float4 m4 =
+                                    *reinterpret_cast<const float4 *>(s_m + cb * 16 + e);
+                                need |= (v[e] > m4.x + kRescaleSlack) |
+                                        (v[e + 1] > m4.y + kRescaleSlack) |
+                                        (v[e + 2] > m4.z + kRescaleSlack) |
+                                        (v[e + 3] > m4.w + kRescaleSlack);
+                            }
                         }
                     }
                 }
@@ -1324,6 +1338,12 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
                         moved = mn != m_old && m_old != -INFINITY;
                     }
                     rescale = named_bar_softmax_any(moved);
+                    if constexpr (kOneChunk) {
+#pragma unroll
+                        for (int e = 0; e < 16; e += 4)
+                            *reinterpret_cast<float4 *>(mreg + e) =
+                                *reinterpret_cast<const float4 *>(s_m + e);
+                    }
                 }
                 // PV of the previous tile (of this segment or the one before)
                 // must be done before P, O^T and L^T are touched.
@@ -1366,10 +1386,15 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
                         } else {
                             load_chunk(cb, v);
                         }
+                        if constexpr (kOneChunk) {
 #pragma unroll
-                        for (int e = 0; e < 16; e += 4)
-                            *reinterpret_cast<float4 *>(m + e) =
-                                *reinterpret_cast<const float4 *>(s_m + cb * 16 + e);
+                            for (int e = 0; e < 16; ++e) m[e] = mreg[e];
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; e += 4)
+                                *reinterpret_cast<float4 *>(m + e) =
+                                    *reinterpret_cast<const float4 *>(s_m + cb * 16 + e);
+                        }
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
                             const int r = cb * 16 + e;
