@@ -289,9 +289,12 @@ def config_attention_bytes(w):
     return total
 
 
-def median_call_us(fn, reps, flush, stream):
+def median_call_us(fn, reps, flush, stream, trimmed=None):
     """Median over reps of one call timed with CUDA events on `stream`, with
-    the L2 flushed (a write larger than L2) before each timed call."""
+    the L2 flushed (a write larger than L2) before each timed call.  CUDA event
+    timestamps on this GPU come in steps of about 2 us, so the mean of the
+    middle 80% of the samples (`trimmed`, a one-element list, if given) is
+    also recorded: its resolution is finer than one step."""
     import torch
     for _ in range(3):
         fn()
@@ -306,6 +309,11 @@ def median_call_us(fn, reps, flush, stream):
         e1.record(stream)
         torch.cuda.synchronize()
         times.append(e0.elapsed_time(e1) * 1e3)
+    if trimmed is not None:
+        ts = sorted(times)
+        cut = len(ts) // 10
+        mid = ts[cut:len(ts) - cut] or ts
+        trimmed.append(sum(mid) / len(mid))
     return statistics.median(times)
 
 
@@ -319,8 +327,9 @@ def run_configs(dev, reps, peak, peak_kind, ablation_reps):
     from sliding_window_gqa_ring_gb300 import ablation, carat, engine, synth
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    floor1 = median_call_us(lambda: carat.carat_launch_floor(False), reps, flush, stream)
-    floor2 = median_call_us(lambda: carat.carat_launch_floor(True), reps, flush, stream)
+    ft = []
+    floor1 = median_call_us(lambda: carat.carat_launch_floor(False), reps, flush, stream, ft)
+    floor2 = median_call_us(lambda: carat.carat_launch_floor(True), reps, flush, stream, ft)
     rows = []
     for w in (synth.sliding_single(), synth.sliding_batched(), synth.global_single(),
               synth.global_sweep(4), synth.global_sweep(15)):
@@ -352,15 +361,18 @@ def run_configs(dev, reps, peak, peak_kind, ablation_reps):
         n0 = carat.kernel_launches()
         attend()
         attn_launches = carat.kernel_launches() - n0
+        tm = []
         append_us = median_call_us(append, reps, flush, stream)
-        attn_us = median_call_us(attend, reps, flush, stream)
-        fused_us = median_call_us(fused, reps, flush, stream)
+        attn_us = median_call_us(attend, reps, flush, stream, tm)
+        fused_us = median_call_us(fused, reps, flush, stream, tm)
         nbytes = config_attention_bytes(w)
         floor = floor2 if attn_launches > 1 else floor1
         gbs = nbytes / (attn_us * 1e3)
         rows.append({"workload": w.name, "batch": w.batch, "proposal_count": w.proposal_count,
                      "attention_bytes": nbytes, "append_us": round(append_us, 2),
                      "attention_us": round(attn_us, 2), "fused_us": round(fused_us, 2),
+                     "attention_us_trimmed_mean": round(tm[0], 2),
+                     "fused_us_trimmed_mean": round(tm[1], 2),
                      "attention_gb_s": round(gbs, 1), "attention_frac": round(gbs / peak, 4),
                      "attention_launches": attn_launches,
                      "attention_floor_us": round(floor, 2),
@@ -376,7 +388,8 @@ def run_configs(dev, reps, peak, peak_kind, ablation_reps):
             torch.cuda.empty_cache()
     return {"workloads": rows,
             "launch_floor_us": {"one_empty_launch": round(floor1, 2),
-                                "empty_launch_then_dependent_launch": round(floor2, 2)},
+                                "empty_launch_then_dependent_launch": round(floor2, 2),
+                                "trimmed_means": [round(x, 2) for x in ft]},
             "peak_gb_s": peak, "peak_source": f"{peak_kind} hbm_gbs",
             "timing": (f"median of {reps} calls, CUDA events on the launching stream, L2 "
                        "flushed (512 MB write) before every timed call; floor = the same "
