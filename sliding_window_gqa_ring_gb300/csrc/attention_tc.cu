@@ -29,20 +29,22 @@
 // sliding window), CTA g simply takes unit g whole ("unit mode").  Otherwise
 // (stream-K): a unit's tiles are taken
 // in a fixed order (the small tile of this step's rows first).  All units'
-// tiles, request after request, form one flattened sequence of T tiles, and
+// tiles, request after request, form one flattened sequence of tiles, and
 // the grid -- one CTA per resident slot, so every CTA starts at once -- cuts
-// it into equal contiguous ranges of ceil(T / grid) tiles (stream-K).  A CTA
-// walks its range as segments, one per unit it touches, streaming K/V through
-// one stage ring without a break between segments.  A segment that covers a
-// whole unit writes the normalised output; the at most two others (the
-// range's first and last) write a partial (row max, row sum, unnormalised O)
-// to the workspace, and the CTA holding a unit's first tile records in a unit
-// table whether the unit was split.  A second launch (attn_fixup_kernel, one
-// CTA per (unit, row), started early by programmatic dependent launch and
-// waiting for this grid) merges the split units' pieces in parallel.  The
-// range is never shorter than 1/(kMaxPieces - 1) of the longest unit, so no
-// unit is cut into more than kMaxPieces pieces.  The CTAs never wait for one
-// another.
+// it into contiguous ranges of equal cost (stream-K), where a unit costs its
+// tiles plus a fixed charge for the segment boundary it causes, so a range
+// that touches more units gets fewer tiles.  A CTA walks its range as
+// segments, one per unit it touches, streaming K/V through one stage ring
+// without a break between segments.  A segment that covers a whole unit
+// writes the normalised output; the at most two others (the range's first
+// and last) write a partial (row max, row sum, unnormalised O) to the
+// workspace, and the CTA holding a unit's first tile records in a unit table
+// the range it starts in, how many ranges it spans and which partial slot
+// its first piece uses.  A second launch (attn_fixup_kernel, one CTA per
+// (unit, row), started early by programmatic dependent launch and waiting
+// for this grid) merges the split units' pieces in parallel.  Ranges are
+// long enough that no unit is cut into more than kMaxPieces pieces.  The CTAs
+// never wait for one another.
 //
 // Warp roles (192 threads):
 //   warp 0      computes the CTA's range (a scan over the requests' tile
@@ -165,7 +167,10 @@ struct SkShared {
     int b0, ur0, off0;            // first segment: request, unit within it, order offset
     int id0, ntiles0, special0;   // first request's id, tiles and special tile
     long long ctx0;               // first request's context length
-    long long s, e, len;          // tile range [s, e) of the flattened order; range length
+    long long s, e;               // tile range [s, e) of the flattened order
+    long long len;                // stream-K: cost of one range (tiles plus unit charges)
+    long long ucost0;             // cost position of the first segment's unit
+    int segc;                     // cost charged per unit, in tiles
 };
 static_assert(sizeof(SkShared) <= 128, "SkShared must fit the misc area");
 
@@ -185,6 +190,7 @@ struct Segment {
     int x0, x1;                // order indices [x0, x1) of the unit's tiles covered here
     long long start;           // flattened index of the segment's first tile
     long long unit_start;      // flattened index of the unit's first tile
+    long long unit_cost;       // cost position of the unit (see locate_range)
 };
 
 // Tile index of order index x: the special tile (this step's rows of a fused
@@ -202,10 +208,14 @@ struct SegIter {
     int b, ur, off;
     int id, ntiles, special;
     long long ctx;
-    int rg_fixed;   // paired schedule: this CTA's row group (else -1)
+    long long ucost;   // cost position of the current unit
+    int segc;          // cost charged per unit
+    int rg_fixed;      // paired schedule: this CTA's row group (else -1)
 
     __device__ void init(const AttnParams &p, const SkShared *sk, int rg = -1) {
         rg_fixed = rg;
+        ucost = sk->ucost0;
+        segc = sk->segc;
         pos = sk->s;
         end = sk->e;
         b = sk->b0;
@@ -240,10 +250,12 @@ struct SegIter {
         sg.x1 = off + len;
         sg.start = pos;
         sg.unit_start = pos - off;
+        sg.unit_cost = ucost;
         pos += len;
         off += len;
         if (off == ntiles && pos < end) {
             off = 0;
+            ucost += ntiles + segc;
             if (++ur == upr) {
                 ur = 0;
                 ntiles = 0;
@@ -270,14 +282,19 @@ __device__ __forceinline__ int warp_max_int(int v) {
 }
 
 // Warp 0: this CTA's tile range of the flattened order and where it starts.
-// Runs once per CTA from a cold instruction cache, so it is kept to two short
-// loops (32 requests per pass, the second pass re-reading through L2) rather
+// Ranges have equal cost, not equal tile counts: each unit is charged segc
+// tiles besides its own (a segment boundary writes an output or a partial,
+// reloads Q and refills the stage ring), so a range that touches several units
+// gets fewer tiles.  In cost positions, unit u (the u-th unit that has tiles)
+// starts at U_u = P_u + segc * u, P_u being the flattened index of its first
+// tile, and its tile o sits at U_u + segc + o; tile t belongs to range
+// floor(cost(t) / T), T the cost of one range (the last range takes the rest).
+// Runs once per CTA from a cold instruction cache, so it is kept to short
+// loops (32 requests per pass, the later passes re-reading through L2) rather
 // than unrolled code.
-// upr: units per request in the flattened order; the order is cut into
-// `ranges` ranges and this CTA takes range `rix`.
 __device__ __noinline__ void locate_range(const AttnParams &p, int upr, int lane, SkShared *sk,
-                                          int ranges, int rix) {
-    long long total = 0;
+                                          int ranges, int rix, int seg_cost) {
+    long long tiles = 0, units = 0;
     int nmax = 0;
 #pragma unroll 1
     for (int base = 0; base < p.batch; base += 32) {
@@ -288,73 +305,110 @@ __device__ __noinline__ void locate_range(const AttnParams &p, int upr, int lane
             long long ctx;
             v = request_tiles(p, b, &id, &ctx, &sp);
         }
-        total += v;
+        tiles += v;
+        units += v > 0 ? 1 : 0;
         nmax = max(nmax, v);
     }
-    total = warp_sum_ll(total) * upr;
+    tiles = warp_sum_ll(tiles) * upr;
+    units = warp_sum_ll(units) * upr;
     nmax = warp_max_int(nmax);
-    const long long grid = ranges;
-    long long len = (total + grid - 1) / grid;
-    const long long min_len = (nmax + kMaxPieces - 2) / (kMaxPieces - 1);
-    if (len < min_len) len = min_len;
-    if (len < 1) len = 1;
-    const long long s = (long long)rix * len;
-    const long long e = s + len < total ? s + len : total;
-    // First request whose tiles reach past s; its id, context length and
-    // special tile come from the lane that read it.
-    int b0 = 0, ur0 = 0, off0 = 0, id0 = 0, nt0 = 0, sp0 = -1;
-    long long ctx0 = 0;
-    if (s < e) {
-        long long cum = 0;
+    // A call with fewer tiles than ranges gives every tile its own range.
+    const int c = tiles >= ranges ? seg_cost : 0;
+    const long long cost = tiles + (long long)c * units;
+    long long T = (cost + ranges - 1) / ranges;
+    // at most kMaxPieces ranges touch one unit; no range is empty but the last
+    const long long min_T = (nmax + kMaxPieces - 3) / (kMaxPieces - 2);
+    if (T < min_T) T = min_T;
+    if (T < c + 1) T = c + 1;
+    // First tile whose cost position is >= X: its flattened index, request,
+    // unit within the request, offset in the unit and the unit's cost
+    // position (index = tiles when there is none).
+    struct Pos {
+        long long tile, ucost;
+        int b, ur, off, id, nt, sp;
+        long long ctx;
+    };
+    auto find = [&](long long X, Pos &r) -> bool {
+        long long cum_cost = 0, cum_tiles = 0;
 #pragma unroll 1
         for (int base = 0; base < p.batch; base += 32) {
             const int b = base + lane;
             int v = 0, id = 0, sp = -1;
             long long ctx = 0;
             if (b < p.batch) v = request_tiles(p, b, &id, &ctx, &sp);
-            const long long vt = (long long)v * upr;
-            long long inc = vt;
+            const long long vc = v > 0 ? (long long)upr * (v + c) : 0;
+            long long inc = vc;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const long long y = __shfl_up_sync(kFull, inc, o);
                 if (lane >= o) inc += y;
             }
-            const unsigned hit = __ballot_sync(kFull, cum + inc > s);
+            long long inct = (long long)upr * v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const long long y = __shfl_up_sync(kFull, inct, o);
+                if (lane >= o) inct += y;
+            }
+            const unsigned hit = __ballot_sync(kFull, cum_cost + inc > X);
             if (hit) {
                 const int src = __ffs(hit) - 1;
                 if (lane == src) {
-                    const long long roff = s - (cum + inc - vt);   // tiles into request b
-                    b0 = b;
-                    ur0 = (int)(roff / v);
-                    off0 = (int)(roff - (long long)ur0 * v);
-                    nt0 = v;
-                    id0 = id;
-                    ctx0 = ctx;
-                    sp0 = sp;
+                    const long long rem = X - (cum_cost + inc - vc);   // cost into request b
+                    const long long per = v + c;
+                    const int j = (int)(rem / per);
+                    const long long r2 = rem - (long long)j * per;
+                    const int o = r2 <= c ? 0 : (int)(r2 - c);
+                    r.tile = cum_tiles + inct - (long long)upr * v + (long long)j * v + o;
+                    r.ucost = cum_cost + inc - vc + (long long)j * per;
+                    r.b = b;
+                    r.ur = j;
+                    r.off = o;
+                    r.id = id;
+                    r.nt = v;
+                    r.sp = sp;
+                    r.ctx = ctx;
                 }
-                b0 = __shfl_sync(kFull, b0, src);
-                ur0 = __shfl_sync(kFull, ur0, src);
-                off0 = __shfl_sync(kFull, off0, src);
-                nt0 = __shfl_sync(kFull, nt0, src);
-                id0 = __shfl_sync(kFull, id0, src);
-                ctx0 = __shfl_sync(kFull, ctx0, src);
-                sp0 = __shfl_sync(kFull, sp0, src);
-                break;
+                r.tile = __shfl_sync(kFull, r.tile, src);
+                r.ucost = __shfl_sync(kFull, r.ucost, src);
+                r.b = __shfl_sync(kFull, r.b, src);
+                r.ur = __shfl_sync(kFull, r.ur, src);
+                r.off = __shfl_sync(kFull, r.off, src);
+                r.id = __shfl_sync(kFull, r.id, src);
+                r.nt = __shfl_sync(kFull, r.nt, src);
+                r.sp = __shfl_sync(kFull, r.sp, src);
+                r.ctx = __shfl_sync(kFull, r.ctx, src);
+                return true;
             }
-            cum += __shfl_sync(kFull, inc, 31);
+            cum_cost += __shfl_sync(kFull, inc, 31);
+            cum_tiles += __shfl_sync(kFull, inct, 31);
         }
+        return false;
+    };
+    Pos st{}, en{};
+    st.tile = en.tile = tiles;
+    const long long X0 = (long long)rix * T;
+    bool have = X0 < cost && find(X0, st);
+    if (have && rix + 1 < ranges && (long long)(rix + 1) * T < cost) {
+        // with no unit charge cost positions are tile indices: no second scan
+        if (c == 0)
+            en.tile = (long long)(rix + 1) * T;
+        else
+            find((long long)(rix + 1) * T, en);
     }
+    if (!have) st.tile = tiles;
     if (lane == 0) {
-        sk->s = s;
-        sk->e = e;
-        sk->len = len;
-        sk->b0 = b0;
-        sk->ur0 = ur0;
-        sk->off0 = off0;
-        sk->ntiles0 = nt0;
-        sk->special0 = sp0;
-        sk->id0 = id0;
-        sk->ctx0 = ctx0;
+        sk->s = st.tile;
+        sk->e = en.tile;
+        sk->len = T;
+        sk->segc = c;
+        sk->b0 = have ? st.b : 0;
+        sk->ur0 = have ? st.ur : 0;
+        sk->off0 = have ? st.off : 0;
+        sk->ntiles0 = have ? st.nt : 0;
+        sk->special0 = have ? st.sp : -1;
+        sk->id0 = have ? st.id : 0;
+        sk->ctx0 = have ? st.ctx : 0;
+        sk->ucost0 = have ? st.ucost : 0;
     }
     __syncwarp();
 }
@@ -370,6 +424,8 @@ __device__ void locate_unit(const AttnParams &p, int upr, int lane, SkShared *sk
         sk->s = 0;
         sk->e = nt;
         sk->len = nt > 0 ? nt : 1;
+        sk->ucost0 = 0;
+        sk->segc = 0;
         sk->b0 = b;
         sk->ur0 = blockIdx.x % upr;
         sk->off0 = 0;
@@ -835,7 +891,7 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
             locate_unit(p, upr, lane, sk);
         else
             locate_range(p, upo, lane, sk, paired ? gridDim.x / 2 : gridDim.x,
-                         paired ? blockIdx.x / 2 : blockIdx.x);
+                         paired ? blockIdx.x / 2 : blockIdx.x, L::kDoubleO ? 1 : 2);
         if (lane == 0) {
             // Start streaming before the block-wide barrier: this thread made
             // the barriers, and the first NS stages need no release.
@@ -1155,13 +1211,18 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
             const uint32_t tmem_l = tmem_l_of(si);
             const int n = sg.x1 - sg.x0;
             if (t == 0 && sg.x0 == 0 && !plan.unit_mode) {
-                // The unit's entry for the merge launch: where it starts in
-                // the flattened order and its tiles when it is split across
-                // CTAs, 0 tiles when this segment covers it whole.
+                // The unit's entry for the merge launch: the range holding its
+                // first tile, the number of ranges it spans (0 when this
+                // segment covers it whole) and the partial slot its first
+                // piece uses (0: first segment of its range, 1: last); later
+                // pieces each open their range (slot 0).
+                const int ranges = paired ? (int)gridDim.x / 2 : (int)gridDim.x;
+                const int rix = paired ? (int)blockIdx.x / 2 : (int)blockIdx.x;
+                long long r_last = (sg.unit_cost + sk->segc + sg.ntiles - 1) / sk->len;
+                if (r_last > ranges - 1) r_last = ranges - 1;
                 const bool whole = sg.x1 == sg.ntiles;
-                p.units[sg.unit] = make_int4((int)(sg.unit_start & 0xffffffffll),
-                                             (int)(sg.unit_start >> 32), whole ? 0 : sg.ntiles,
-                                             (int)sk->len);
+                p.units[sg.unit] = make_int4(rix, whole ? 0 : (int)(r_last - rix + 1),
+                                             sg.start == sk->s ? 0 : 1, 0);
             }
             const int b = sg.b, c = sg.c;
             const long long ctx = sg.ctx;
@@ -1705,26 +1766,21 @@ __global__ void __launch_bounds__(D / 4) attn_fixup_kernel(const AttnParams p, i
     const int pos0 = rg * pos_per_group;
     const int npos = min(pos_per_group, p.k - pos0);
     if (r >= npos * p.group) return;
-    const int nt = e.z;
-    if (nt == 0) return;                          // whole: already written
-    const long long u0 = (long long)(unsigned)e.x | ((long long)e.y << 32);
-    const long long len = e.w;
+    const int np = e.y;
+    if (np == 0) return;                          // whole: already written
+    const int g_first = e.x, first_slot = e.z;
     // An entry the attention grid did not write this time (it stopped on a
     // timeout before reaching the unit) is not used: its pieces could lie
     // outside the workspace.
-    const long long lpos = len >= 1 ? len : 1;
-    const long long g_first = u0 / lpos;
-    const long long g_last = (u0 + nt - 1) / lpos;
-    if ((len < 1) | (u0 < 0) | (nt < 0) | (g_last >= slots) |
-        (g_last - g_first >= kMaxPieces)) {
+    if ((g_first < 0) | (np < 1) | (np > kMaxPieces) | (g_first > slots - np) |
+        ((first_slot & ~1) != 0)) {
         if (threadIdx.x == 0) set_status(p.dev_status, CARAT_DEV_TIMEOUT);
         return;
     }
-    const int np = (int)(g_last - g_first + 1);
     auto piece_base = [&](int q) -> size_t {
-        const long long gq = g_first + q;                   // range holding piece q
-        const long long cta = paired ? 2 * gq + rg : gq;    // its CTA for this row group
-        return ((size_t)cta * 2 + (u0 > gq * len ? 1 : 0)) * slot_rows;
+        const int gq = g_first + q;                         // range holding piece q
+        const int cta = paired ? 2 * gq + rg : gq;          // its CTA for this row group
+        return ((size_t)cta * 2 + (q == 0 ? first_slot : 0)) * slot_rows;
     };
     // weights 2^(m_q - M) / L of the pieces, by warp 0 (each lane reads the
     // (max, sum) pairs of pieces lane and lane + 32 once)
