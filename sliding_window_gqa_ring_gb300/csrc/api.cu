@@ -45,6 +45,7 @@ bool supported_head_dim(int d) { return d == 256 || d == 512; }
 struct SplitPlan {
     bool unit_mode = false;    // one CTA per unit (else stream-K)
     bool fp8 = false;          // FP8 e4m3 rings
+    bool deep = false;         // a call with at most one tile per SM: one CTA per SM, deep ring
     int grid = 0;              // CTAs launched
     size_t ml_bytes = 0;
     size_t o_bytes = 0;
@@ -90,6 +91,14 @@ SplitPlan tc_plan(int batch, int group, int k, int kv_heads, int head_dim, long 
     // One CTA per unit when there are enough units and each is short.
     p.unit_mode = units >= slots_total && max_tiles <= 16;
     p.grid = p.unit_mode ? (int)units : slots_total;
+    // A stream-K call that cannot have more tiles than the GPU has SMs gives
+    // each busy CTA about one tile: a kernel with a ring deep enough for a
+    // whole tile's K and V loads them at once (one DRAM round trip, not two).
+    const int sms = device_sm_count();
+    if (!p.unit_mode && !fp8 && units * max_tiles <= sms && tc_has_deep_variant(head_dim, n)) {
+        p.deep = true;
+        p.grid = sms;
+    }
     const size_t slots = (size_t)slots_total * 2 * n;
     p.ml_bytes = align256(slots * sizeof(float2));
     p.o_bytes = align256(slots * (size_t)head_dim * sizeof(float));
@@ -143,7 +152,7 @@ SplitPlan global_plan(int batch, int proposal_count, int q_heads, int kv_heads, 
 }
 
 cudaError_t launch_attention(const AttnParams &p, const SplitPlan &plan, cudaStream_t stream) {
-    return launch_attention_tc(p, plan.grid, plan.unit_mode, plan.fp8, stream);
+    return launch_attention_tc(p, plan.grid, plan.unit_mode, plan.fp8, stream, plan.deep);
 }
 
 carat_status launch_status(cudaError_t e) { return e == cudaSuccess ? CARAT_OK : CARAT_ERR_CUDA; }

@@ -1906,8 +1906,12 @@ int tc_units_per_request(int group, int k, int kv_heads) {
     return kv_heads * ((k + ppg - 1) / ppg);
 }
 
+bool tc_has_deep_variant(int head_dim, int rows_per_tile) {
+    return head_dim == 256 && rows_per_tile == 16;
+}
+
 cudaError_t launch_attention_tc(const AttnParams &p, int grid, bool unit_mode, bool fp8,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, bool deep) {
     const int n = tc_rows_per_tile(p.group, p.k);
     TcPlan plan{};
     plan.unit_mode = unit_mode ? 1 : 0;
@@ -2002,6 +2006,9 @@ cudaError_t launch_attention_tc(const AttnParams &p, int grid, bool unit_mode, b
     // streaming; the others run one CTA per SM with the stage ring taking the
     // rest of shared memory.
     if (p.head_dim == 256) {
+        // a small call (at most one tile per SM): one CTA per SM with six
+        // stages, so a tile's K and V stages all load at once
+        if (n == 16 && deep) return launch_tc<256, 16, 6, 1>(p, plan, maps, grid, stream);
         if (n == 16) return launch_tc<256, 16, 3, 2>(p, plan, maps, grid, stream);
         if (n == 32) return launch_tc<256, 32, 6, 1>(p, plan, maps, grid, stream);
         return launch_tc<256, 64, 5, 1>(p, plan, maps, grid, stream);

@@ -208,6 +208,9 @@ bool tc_supported(int head_dim, int group, int k);
 bool tc_fp8_supported(int head_dim, int group, int k);   // FP8 e4m3 rings
 int tc_units_per_request(int group, int k, int kv_heads);
 cudaError_t launch_attention_tc(const AttnParams &p, int grid, bool unit_mode, bool fp8,
-                                cudaStream_t stream);
+                                cudaStream_t stream, bool deep = false);
+// Whether a one-CTA-per-SM kernel with a deep stage ring exists for this
+// shape (used for calls with at most one tile per SM).
+bool tc_has_deep_variant(int head_dim, int rows_per_tile);
 
 }  // namespace carat
