@@ -1953,8 +1953,9 @@ cudaError_t launch_attention_tc(const AttnParams &p, int grid, bool unit_mode, b
         const uint32_t boxq[4] = {64, (uint32_t)p.group, (uint32_t)plan.pos_per_group, 1};
         if (!make_bf16_tensor_map(&maps.q, p.q, 4, dimsq, stridesq, boxq, true))
             return cudaErrorInvalidValue;
-        // one CTA per SM: 3 f16 stages and 6 (or 4) raw stages in flight
-        if (n == 16) return launch_tc<256, 16, 3, 1, 6>(p, plan, maps, grid, stream);
+        // one CTA per SM: f16 stages the widening warps fill and raw stages in
+        // flight (16 rows: 5 and 3, the split measured best; else 3 and 6 or 4)
+        if (n == 16) return launch_tc<256, 16, 5, 1, 3>(p, plan, maps, grid, stream);
         if (n == 32) return launch_tc<256, 32, 3, 1, 6>(p, plan, maps, grid, stream);
         return launch_tc<256, 64, 3, 1, 4>(p, plan, maps, grid, stream);
     }

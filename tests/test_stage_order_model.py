@@ -166,7 +166,7 @@ def _random_segments(rng):
 
 # (NS, KS) of the bf16 instantiations and (NS, KS, NR) of the FP8 ones
 BF16 = [(3, 2), (6, 2), (5, 2), (4, 4), (5, 4)]
-FP8 = [(3, 2, 6), (3, 2, 4)]
+FP8 = [(5, 2, 3), (3, 2, 6), (3, 2, 4)]
 
 
 @pytest.mark.parametrize("NS,KS", BF16)
