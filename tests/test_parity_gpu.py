@@ -133,6 +133,17 @@ def test_global_sweep(orc, k, fused):
     _run_global(orc, synth.global_sweep(k), fused=fused)
 
 
+@pytest.mark.parametrize("k", [4, 15])
+def test_global_one_long_request(orc, k):
+    """One request with 32768 keys on 2 KV heads: each unit is cut into 37 to
+    53 stream-K pieces, more than 32, so every lane of the merge launch weighs
+    a second piece (15 proposals: paired row groups).  Every output element."""
+    w = synth.small(f"global_long_k{k}", seed=3100 + k, batch=1, proposal_count=k, q_heads=16,
+                    kv_heads=2, head_dim=512, key_counts=[32768], capacity=32768,
+                    outlier_fraction=0.01)
+    _run_global(orc, w, fill=float("nan"))
+
+
 @FUSED
 def test_mixed_step_sampled(orc, fused):
     """The mixed step's 6 layers on a sample of its 64 requests (the shortest,
