@@ -43,13 +43,14 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool supported_head_dim(int d) { return d == 256 || d == 512; }
 
 struct SplitPlan {
-    bool unit_mode = false;    // one CTA per unit (else stream-K)
+    bool unit_mode = false;    // whole units from a work counter (else stream-K)
     bool fp8 = false;          // FP8 e4m3 rings
     bool deep = false;         // a call with at most one tile per SM: one CTA per SM, deep ring
     int grid = 0;              // CTAs launched
     size_t ml_bytes = 0;
     size_t o_bytes = 0;
     size_t unit_bytes = 0;
+    size_t sched_bytes = 0;
     size_t total = 0;
 };
 
@@ -76,11 +77,12 @@ int device_sm_count() {
 }
 
 // Tensor-core path.  Units (request, KV head, row group) that fill every
-// resident CTA slot and are all short (at most 16 tiles of 128 keys) run one
-// CTA each.  Otherwise one CTA per resident slot runs the stream-K schedule;
-// each keeps two partial slots (the first and last segment of its range), and
-// each unit a 16-byte entry for the merge launch.  The workspace is sized for
-// stream-K either way.
+// resident CTA slot and are all short (at most 16 tiles of 128 keys) are
+// taken whole, one at a time, by one persistent CTA per resident slot from a
+// work counter in the workspace (unit mode).  Otherwise one CTA per resident
+// slot runs the stream-K schedule; each keeps two partial slots (the first
+// and last segment of its range), and each unit a 16-byte entry for the merge
+// launch.  The workspace holds both.
 SplitPlan tc_plan(int batch, int group, int k, int kv_heads, int head_dim, long long max_tiles,
                   bool fp8 = false) {
     SplitPlan p;
@@ -88,9 +90,14 @@ SplitPlan tc_plan(int batch, int group, int k, int kv_heads, int head_dim, long 
     const int n = tc_rows_per_tile(group, k);
     const int slots_total = tc_ctas_per_sm(head_dim, n, fp8) * device_sm_count();
     const long long units = (long long)batch * tc_units_per_request(group, k, kv_heads);
-    // One CTA per unit when there are enough units and each is short.
-    p.unit_mode = units >= slots_total && max_tiles <= 16;
-    p.grid = p.unit_mode ? (int)units : slots_total;
+    // Whole units when there are enough of them and each is short.  With
+    // bf16 caches one CTA per unit.  With FP8 caches (one CTA per SM, several
+    // units each) one persistent CTA per SM: CTA g starts with unit g and then
+    // takes the next unit the counter hands out as soon as it has issued its
+    // current unit's loads, so the next unit's keys stream in while the
+    // current one finishes.
+    p.unit_mode = units >= slots_total && max_tiles <= 16 && units < (1ll << 24);
+    p.grid = p.unit_mode && !fp8 ? (int)units : slots_total;
     // A stream-K call that cannot have more tiles than the GPU has SMs gives
     // each busy CTA about one tile: a kernel with a ring deep enough for a
     // whole tile's K and V loads them at once (one DRAM round trip, not two).
@@ -103,7 +110,8 @@ SplitPlan tc_plan(int batch, int group, int k, int kv_heads, int head_dim, long 
     p.ml_bytes = align256(slots * sizeof(float2));
     p.o_bytes = align256(slots * (size_t)head_dim * sizeof(float));
     p.unit_bytes = align256((size_t)batch * tc_units_per_request(group, k, kv_heads) * 16);
-    p.total = p.ml_bytes + p.o_bytes + p.unit_bytes;
+    p.sched_bytes = 256;
+    p.total = p.ml_bytes + p.o_bytes + p.unit_bytes + p.sched_bytes;
     return p;
 }
 
@@ -113,6 +121,9 @@ void set_split_fields(AttnParams &p, const SplitPlan &plan, void *workspace) {
     p.part_ml = reinterpret_cast<float2 *>(w);
     p.part_o = w ? reinterpret_cast<float *>(w + plan.ml_bytes) : nullptr;
     p.units = w ? reinterpret_cast<int4 *>(w + plan.ml_bytes + plan.o_bytes) : nullptr;
+    p.sched = w ? reinterpret_cast<unsigned long long *>(w + plan.ml_bytes + plan.o_bytes +
+                                                          plan.unit_bytes)
+                : nullptr;
 }
 
 int row_groups_for(int group, int k) {

@@ -26,7 +26,13 @@
 //
 // Schedule.  A unit is one (request, KV head, row group).  When there are at
 // least as many units as resident CTA slots and every unit is short (a
-// sliding window), CTA g simply takes unit g whole ("unit mode").  Otherwise
+// sliding window), units are taken whole ("unit mode"): with bf16 caches CTA
+// g simply takes unit g; with FP8 caches (one CTA per SM, several units each)
+// the grid is one persistent CTA per SM, CTA g starts with unit g, and once
+// its producer has issued a unit's loads it takes the next unit from a work
+// counter in the workspace (so that unit's keys stream in while the last one
+// finishes), publishing it to the other roles through a small queue in
+// shared memory; the launch's last CTA clears the counter.  Otherwise
 // (stream-K): a unit's tiles are taken
 // in a fixed order (the small tile of this step's rows first).  All units'
 // tiles, request after request, form one flattened sequence of tiles, and
@@ -44,7 +50,8 @@
 // (unit, row), started early by programmatic dependent launch and waiting
 // for this grid) merges the split units' pieces in parallel.  Ranges are
 // long enough that no unit is cut into more than kMaxPieces pieces.  The CTAs
-// never wait for one another.
+// never wait for one another (the unit queue's counter is an atomic add, never
+// a wait).
 //
 // Warp roles (192 threads):
 //   warp 0      computes the CTA's range (a scan over the requests' tile
@@ -70,6 +77,7 @@
 // Every wait is bounded (mbar_wait): on a timeout the CTA records
 // CARAT_DEV_TIMEOUT, stops issuing work, waits (bounded) for its own copies
 // and MMAs in flight, frees its TMEM and returns.
+#include <atomic>
 #include <cfloat>
 
 #include <cuda_bf16.h>
@@ -88,6 +96,7 @@ constexpr int kBoxBytes = 128 * 128;        // [128 keys][64 bf16]
 constexpr int kStageBytes = 2 * kBoxBytes;  // 128 keys x 128 d
 constexpr int kDispRows = 16;               // displaced rows loaded per tile (>= k - 1)
 constexpr int kMaxPieces = 64;              // CTAs one unit may be split across
+constexpr int kUnitQ = 4;                   // unit mode: queue slots of units taken
 constexpr int kDispBoxBytes = kDispRows * 128;
 constexpr int kThreads = 192;
 constexpr int kConvThreads = 128;           // FP8 caches: four more warps widen the stages
@@ -115,9 +124,9 @@ struct Layout {
     static constexpr int kRedQscale = 7 * N;
     static constexpr int kRedFloats = 7 * N + (NR > 0 ? 2 : 0) * N;
     static constexpr int kOffBar = kOffRed + kRedFloats * 4;
-    static constexpr int kNumBars = 2 * NS + 7 + 2 * NR + (NR > 0 ? 2 : 0);
+    static constexpr int kNumBars = 2 * NS + 7 + 2 * NR + (NR > 0 ? 2 + 2 * kUnitQ : 0);
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;   // SkShared
-    static constexpr int kBytes = kOffMisc + 128;
+    static constexpr int kBytes = kOffMisc + (NR > 0 ? 256 : 128);
     static constexpr int kAlloc = kBytes + 1024;       // base alignment slack
     // Two S^T buffers, then per segment an O^T buffer (KS blocks of N columns)
     // and a row-sum buffer L^T (N columns); two of each when they fit the 512
@@ -159,6 +168,14 @@ struct TcPlan {
     int paired;
 };
 
+// Unit mode: a unit the producer took, as every role needs it (request,
+// unit within it, ring or cache id, context length, tiles, special tile);
+// u = -1: no unit left.
+struct UnitDesc {
+    int u, b, ur, id, ntiles, special;
+    long long ctx;
+};
+
 // Per-CTA schedule, written by warp 0 before the block-wide barrier and read
 // by every role.
 struct SkShared {
@@ -171,8 +188,12 @@ struct SkShared {
     long long len;                // stream-K: cost of one range (tiles plus unit charges)
     long long ucost0;             // cost position of the first segment's unit
     int segc;                     // cost charged per unit, in tiles
+    // FP8 unit mode: the units taken, in order (only FP8 kernels reserve the
+    // space: the misc area is 128 bytes with bf16 caches, 256 with FP8)
+    UnitDesc uq[kUnitQ];
 };
-static_assert(sizeof(SkShared) <= 128, "SkShared must fit the misc area");
+static_assert(offsetof(SkShared, uq) <= 128 && sizeof(SkShared) <= 256,
+              "SkShared must fit the misc area");
 
 // Tiles of request b (0 when request_ok rejects it) and its special tile.
 __device__ __forceinline__ int request_tiles(const AttnParams &p, int b, int *id, long long *ctx,
@@ -225,6 +246,28 @@ struct SegIter {
         ctx = sk->ctx0;
         ntiles = sk->ntiles0;
         special = sk->special0;
+    }
+
+    // Unit mode: unit u, whole, is the next segment.
+    __device__ void set_unit(const AttnParams &p, int upr, int u) {
+        b = u / upr;
+        ur = u - b * upr;
+        ntiles = request_tiles(p, b, &id, &ctx, &special);
+        pos = 0;
+        end = ntiles;
+        off = 0;
+    }
+    // The same from the producer's description of it.
+    __device__ void set_unit(const volatile UnitDesc &d) {
+        b = d.b;
+        ur = d.ur;
+        id = d.id;
+        ctx = d.ctx;
+        ntiles = d.ntiles;
+        special = d.special;
+        pos = 0;
+        end = ntiles;
+        off = 0;
     }
 
     // upr: units per request in the flattened order (KV heads when paired).
@@ -413,8 +456,9 @@ __device__ __noinline__ void locate_range(const AttnParams &p, int upr, int lane
     __syncwarp();
 }
 
-// Warp 0, unit mode: this CTA's range is unit blockIdx.x, whole (its own
-// frame: tiles [0, n)); nothing is split, so no partials and no merges.
+// Warp 0, unit mode with bf16 caches: this CTA's range is unit blockIdx.x,
+// whole (its own frame: tiles [0, n)); nothing is split, so no partials and
+// no merges.
 __device__ void locate_unit(const AttnParams &p, int upr, int lane, SkShared *sk) {
     if (lane == 0) {
         const int b = blockIdx.x / upr;
@@ -435,6 +479,57 @@ __device__ void locate_unit(const AttnParams &p, int upr, int lane, SkShared *sk
         sk->ctx0 = ctx;
     }
     __syncwarp();
+}
+
+// Warp 0, unit mode with FP8 caches: every role's iterator starts empty; each
+// unit, whole, comes through the unit queue (unit blockIdx.x first, then the
+// ones the work counter hands out).  Nothing is split, so no partials and no
+// merges.
+__device__ void locate_unit_queue(SkShared *sk, int lane) {
+    if (lane == 0) {
+        sk->s = 0;
+        sk->e = 0;
+        sk->len = 1;
+        sk->ucost0 = 0;
+        sk->segc = 0;
+        sk->b0 = 0;
+        sk->ur0 = 0;
+        sk->off0 = 0;
+        sk->ntiles0 = 0;
+        sk->special0 = -1;
+        sk->id0 = 0;
+        sk->ctx0 = 0;
+    }
+    __syncwarp();
+}
+
+// Unit mode's work counter and count of finished CTAs: a 64-bit word whose
+// high 40 bits hold the launch's epoch and low 24 bits the count; a word
+// holding another epoch (left by an earlier launch, or never written) counts
+// as 0.  Adds one and returns the count before the addition, or -1 if the
+// word never settled.  One atomic add in the common case (a compare-and-swap
+// loop would serialise the CTAs that finish a unit at about the same time,
+// one round trip to L2 each).  A caller that finds the word stale replaces
+// the stale value, whatever it has become, by (epoch, 1) and takes count 0,
+// unless another caller installed the epoch first, in which case it adds
+// again.  Each caller adds to a stale word at most once per installation, so
+// the replacement loop ends; the epoch is installed once, so every count is
+// returned once.
+__device__ long long tagged_increment(unsigned long long *w, unsigned long long epoch) {
+#pragma unroll 1
+    for (int tries = 0; tries < 64; ++tries) {
+        const unsigned long long old = atomicAdd(w, 1ull);
+        if ((old >> 24) == epoch) return (long long)(old & 0xffffffull);
+        unsigned long long cur = old + 1;
+#pragma unroll 1
+        for (int k = 0; k < 65536; ++k) {
+            const unsigned long long seen = atomicCAS(w, cur, (epoch << 24) + 1);
+            if (seen == cur) return 0;
+            if ((seen >> 24) == epoch) break;
+            cur = seen;
+        }
+    }
+    return -1;
 }
 
 // Four e4m3 values (first in the low byte) -> four f16 values, two per word
@@ -623,11 +718,12 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
     attn_tc_kernel(const AttnParams p, const TcPlan plan, const __grid_constant__ TcMaps maps) {
     using L = Layout<D, N, NS, NR>;
     constexpr int KS = L::KS;
-    // FP8 caches: the producer fills raw e4m3 stages, the softmax warps
+    // FP8 caches: the producer fills raw e4m3 stages, the widening warps
     // convert each into an f16 stage (exactly: every e4m3 value is an f16
-    // value, and one conversion instruction widens two of them), rewrite each
-    // segment's Q as f16 with a power-of-two scale per row, and write P as
-    // f16; the tensor core then runs the same products with f16 operands.
+    // value, and one conversion instruction widens two of them) and rewrite
+    // each segment's Q as f16 with a power-of-two scale per row, the softmax
+    // warps write P as f16; the tensor core then runs the same products with
+    // f16 operands.
     constexpr bool F8 = NR > 0;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int upr = p.kv_heads * plan.row_groups;   // units per request
@@ -652,9 +748,12 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
     uint64_t *raw_full = s_full + 7;     // [NR] FP8: e4m3 stage landed
     uint64_t *raw_empty = raw_full + NR; // [NR] FP8: e4m3 stage converted
     uint64_t *qs_ready = raw_empty + NR; // [2] FP8: a segment's Q rewritten (segments alternate)
+    uint64_t *uq_full = qs_ready + (NR > 0 ? 2 : 0);   // [kUnitQ] unit mode: slot written
+    uint64_t *uq_empty = uq_full + kUnitQ;             // [kUnitQ] unit mode: slot read by all
     uint8_t *s_raw = smem + L::kOffRaw;
     SkShared *sk = reinterpret_cast<SkShared *>(smem + L::kOffMisc);
     volatile int *abort_flag = &sk->abort_flag;
+    volatile UnitDesc *unit_q = sk->uq;
     float *red = reinterpret_cast<float *>(smem + L::kOffRed);
     float *s_qscale = red + L::kRedQscale;   // FP8: row score scales of two segments (even, odd)
     uint8_t *s_q = smem + L::kOffQ;
@@ -670,7 +769,7 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
     // (thread 0): the segment being loaded and the next stage load to issue.
     SegIter pit;
     Segment ps{};
-    bool p_have = false, p_qdone = false, alive_p = true;
+    bool p_have = false, p_qdone = false, alive_p = true, p_units_done = false;
     int ppart = 0, pks = 0, psi = 0;
     uint32_t qcnt = 0;   // Q copies issued
     uint32_t cnt = 0;
@@ -698,10 +797,57 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
     // range runs out; a stage is reused only after the MMA released it.  With
     // first_only the producer stops at the end of the first segment (the
     // next segment's Q waits for MMAs that start after the block barrier).
+    // Unit mode: the CTA's next unit with tiles -- unit blockIdx.x first, then
+    // the ones the work counter hands out (gridDim.x + count) -- set as the
+    // producer's next segment and published in the unit queue for the other
+    // roles, or -1 (published too) when none is left.  Its slot is reused once
+    // every role has read what it held kUnitQ units before.
+    auto next_unit = [&]() -> bool {
+        if (p_units_done) return false;
+        const int total = p.batch * upr;
+        const int slot = psi % kUnitQ;
+        if (psi >= kUnitQ && !wait_or_abort(&uq_empty[slot], ((psi / kUnitQ) & 1) ^ 1,
+                                            abort_flag, p.dev_status)) {
+            alive_p = false;
+            return false;
+        }
+        auto grab = [&]() -> int {
+            const long long c = tagged_increment(&p.sched[0], p.sched_epoch);
+            if (c < 0) {
+                set_status(p.dev_status, CARAT_DEV_TIMEOUT);
+                return total;
+            }
+            return (int)min((long long)gridDim.x + c, (long long)total);
+        };
+        int u = psi == 0 ? (int)blockIdx.x : grab();
+        while (u < total) {
+            pit.set_unit(p, upr, u);
+            if (pit.ntiles > 0) break;
+            u = grab();
+        }
+        volatile UnitDesc &d = unit_q[slot];
+        if (u >= total) {
+            u = -1;
+            p_units_done = true;
+        } else {
+            d.b = pit.b;
+            d.ur = pit.ur;
+            d.id = pit.id;
+            d.ctx = pit.ctx;
+            d.ntiles = pit.ntiles;
+            d.special = pit.special;
+        }
+        d.u = u;
+        tc::mbar_arrive(&uq_full[slot]);
+        return u >= 0;
+    };
     auto produce = [&](uint32_t limit, bool first_only) {
         while (alive_p && cnt < limit) {
             if (!p_have) {
                 if (first_only && psi > 0) return;
+                if constexpr (F8) {
+                    if (plan.unit_mode && !next_unit()) return;
+                }
                 if (!pit.next(p, upo, plan.row_groups, ps)) return;
                 p_have = true;
                 p_qdone = false;
@@ -848,6 +994,18 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
         }
     };
 
+    // Unit mode, every role but the producer: the k-th unit this CTA takes
+    // (the k-th the producer published), set as the iterator's next segment.
+    // 1: a unit; 0: no unit left; -1: the wait gave up.
+    auto take_unit = [&](SegIter &it, int k) -> int {
+        const int slot = k % kUnitQ;
+        if (!wait_or_abort(&uq_full[slot], (k / kUnitQ) & 1, abort_flag, p.dev_status)) return -1;
+        const int u = unit_q[slot].u;
+        if (u >= 0) it.set_unit(unit_q[slot]);
+        tc::mbar_arrive(&uq_empty[slot]);
+        return u >= 0 ? 1 : 0;
+    };
+
     // ------------------------------------------------------------ prologue
     // The merge launch that follows a stream-K launch may start as soon as
     // every CTA of this grid is running; it waits for this grid to finish.
@@ -881,14 +1039,24 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
             }
             tc::mbar_init(q_empty, 1);
             tc::mbar_init(fin, 1);
+            for (int i = 0; i < (F8 ? kUnitQ : 0); ++i) {
+                // read by the MMA thread, the 128 softmax threads and the 128
+                // widening threads
+                tc::mbar_init(&uq_full[i], 1);
+                tc::mbar_init(&uq_empty[i], 1 + 128 + kConvThreads);
+            }
             sk->abort_flag = 0;
             tc::fence_mbar_init();
             // K/V rows are read once, except by a pair, where the second read
             // should find them in L2
             pol = paired ? tc::l2_evict_normal_policy() : tc::l2_evict_first_policy();
         }
-        if (plan.unit_mode)
-            locate_unit(p, upr, lane, sk);
+        if (plan.unit_mode) {
+            if constexpr (F8)
+                locate_unit_queue(sk, lane);
+            else
+                locate_unit(p, upr, lane, sk);
+        }
         else
             locate_range(p, upo, lane, sk, paired ? gridDim.x / 2 : gridDim.x,
                          paired ? blockIdx.x / 2 : blockIdx.x, L::kDoubleO ? 1 : 2);
@@ -978,7 +1146,16 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
             bool alive = true;
             uint32_t mcnt = 0, gt = 0;   // stages consumed, tiles before this segment
             int si = 0;
-            while (alive && it.next(p, upo, plan.row_groups, sg)) {
+            // FP8 unit mode: the next unit the producer published, whole
+            auto unit_next = [&]() -> bool {
+                if (plan.unit_mode) {
+                    const int tu = take_unit(it, si);
+                    if (tu < 0) alive = false;
+                    if (tu <= 0) return false;
+                }
+                return it.next(p, upo, plan.row_groups, sg);
+            };
+            while (alive && (F8 ? unit_next() : it.next(p, upo, plan.row_groups, sg))) {
                 const int n = sg.x1 - sg.x0;
                 if (!wait_or_abort(F8 ? &qs_ready[si & 1] : q_full, F8 ? (si >> 1) & 1 : si & 1,
                                    abort_flag, p.dev_status)) {
@@ -1206,7 +1383,20 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
                 }
             }
         };
-        while (alive && it.next(p, upo, plan.row_groups, sg)) {
+        // FP8 unit mode: the next unit the producer published, whole (every
+        // thread took the same unit unless a wait gave up)
+        auto unit_next = [&]() -> bool {
+            if (plan.unit_mode) {
+                const int tu = take_unit(it, si);
+                if (named_bar_softmax_any(tu < 0)) {
+                    alive = false;
+                    return false;
+                }
+                if (tu == 0) return false;
+            }
+            return it.next(p, upo, plan.row_groups, sg);
+        };
+        while (alive && (F8 ? unit_next() : it.next(p, upo, plan.row_groups, sg))) {
             const uint32_t tmem_o = tmem_o_of(si);
             const uint32_t tmem_l = tmem_l_of(si);
             const int n = sg.x1 - sg.x0;
@@ -1656,7 +1846,16 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
             bool alive = true;
             uint32_t ccnt = 0;   // raw stages widened so far
             int si = 0;
-            while (alive && it.next(p, upo, plan.row_groups, sg)) {
+            while (alive) {
+                if (plan.unit_mode) {
+                    const int tu = take_unit(it, si);
+                    if (!__all_sync(kFull, tu >= 0)) {
+                        alive = false;
+                        break;
+                    }
+                    if (tu == 0) break;
+                }
+                if (!it.next(p, upo, plan.row_groups, sg)) break;
                 const int n = sg.x1 - sg.x0;
                 alive = __all_sync(kFull, wait_or_abort(q_full, si & 1, abort_flag, p.dev_status));
                 if (!alive) break;
@@ -1731,7 +1930,17 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
         __syncwarp();
         tc::tmem_dealloc(tmem, L::kTmemCols);
     }
-
+    if (F8 && plan.unit_mode && threadIdx.x == 0) {
+        // This CTA took its last unit; the launch's last CTA to get here
+        // clears the work counter and this count for the next launch (its
+        // epoch may be the same: a replayed graph).
+        __threadfence();
+        if (tagged_increment(&p.sched[1], p.sched_epoch) == (long long)gridDim.x - 1) {
+            __threadfence();
+            atomicExch(&p.sched[0], 0ull);
+            atomicExch(&p.sched[1], 0ull);
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -1910,8 +2119,23 @@ bool tc_has_deep_variant(int head_dim, int rows_per_tile) {
     return head_dim == 256 && rows_per_tile == 16;
 }
 
-cudaError_t launch_attention_tc(const AttnParams &p, int grid, bool unit_mode, bool fp8,
+// A new epoch (40 bits, never 0) per unit-mode launch: a launch's first
+// increment of the work counter or the done count replaces a word tagged
+// with another epoch, whatever the workspace held before.
+static unsigned long long next_unit_epoch() {
+    static std::atomic<unsigned long long> counter{0};
+    unsigned long long e = 0;
+    while (e == 0) e = (counter.fetch_add(1, std::memory_order_relaxed) + 1) & ((1ull << 40) - 1);
+    return e;
+}
+
+cudaError_t launch_attention_tc(const AttnParams &p_call, int grid, bool unit_mode, bool fp8,
                                 cudaStream_t stream, bool deep) {
+    AttnParams p = p_call;
+    if (unit_mode && fp8) {
+        if (!p.sched) return cudaErrorInvalidValue;
+        p.sched_epoch = next_unit_epoch();
+    }
     const int n = tc_rows_per_tile(p.group, p.k);
     TcPlan plan{};
     plan.unit_mode = unit_mode ? 1 : 0;

@@ -35,11 +35,16 @@ struct AttnParams {
     // two slots per CTA of a stream-K grid, [grid][2][rows per tile].
     float2 *part_ml;
     float *part_o;
-    // Stream-K schedule: per (request, KV head, row group) unit, its
-    // first tile's flattened index (x: low, y: high 32 bits), its tile count
-    // when split across CTAs (z; 0 when one CTA covered it) and the range
-    // length (w), for the merge launch.
+    // Stream-K schedule: per (request, KV head, row group) unit, the range
+    // holding its first tile (x), the ranges it spans (y; 0 when one CTA
+    // covered it whole) and the partial slot of its first piece (z), for the
+    // merge launch.
     int4 *units;
+    // Unit mode: the work counter handing out units (word 0) and the count of
+    // CTAs done (word 1), each tagged with the launch's epoch in its high 40
+    // bits; the last CTA of a launch clears both.
+    unsigned long long *sched;
+    unsigned long long sched_epoch;
     int *dev_status;
     int num_ids;                // rings / caches available
     int batch, k, q_heads, kv_heads, head_dim, group, rows;

@@ -56,21 +56,25 @@ def test_workspace_queries(lib):
     # Tensor-core path: two partial slots (rows per tile x head_dim floats, and
     # a (max, sum) pair per row) for each CTA of the persistent grid -- two
     # CTAs per SM for 16-row tiles at head_dim 256, 152 SMs when no GPU is
-    # present -- plus one 16-byte merge entry per (request, KV head, row group).
+    # present -- plus one 16-byte merge entry per (request, KV head, row group)
+    # and 256 bytes for unit mode's work counter.
     def a256(x):
         return (x + 255) // 256 * 256
 
-    def expected(batch, rows_per_tile, head_dim, ctas_per_sm, units_per_request):
-        slots = ctas_per_sm * 152 * 2 * rows_per_tile
-        return a256(slots * 8) + a256(slots * head_dim * 4) + a256(batch * units_per_request * 16)
+    import torch
+    sms = (torch.cuda.get_device_properties(0).multi_processor_count
+           if torch.cuda.is_available() else 152)
 
-    if lib.carat_swa_workspace_bytes(56, 1, 16, 8, 256, 1024) == expected(56, 16, 256, 2, 8):
-        assert lib.carat_swa_workspace_bytes(1, 1, 16, 8, 256, 1024) == expected(1, 16, 256, 2, 8)
-        # 8 query heads per KV head x 15 proposals: 64-row tiles, two row groups
-        assert (lib.carat_global_workspace_bytes(8, 15, 16, 2, 512, 32768)
-                == expected(8, 64, 512, 1, 2 * 2))
-    else:
-        pytest.skip("a GPU with another SM count is visible")
+    def expected(batch, rows_per_tile, head_dim, ctas_per_sm, units_per_request):
+        slots = ctas_per_sm * sms * 2 * rows_per_tile
+        return (a256(slots * 8) + a256(slots * head_dim * 4)
+                + a256(batch * units_per_request * 16) + 256)
+
+    assert lib.carat_swa_workspace_bytes(56, 1, 16, 8, 256, 1024) == expected(56, 16, 256, 2, 8)
+    assert lib.carat_swa_workspace_bytes(1, 1, 16, 8, 256, 1024) == expected(1, 16, 256, 2, 8)
+    # 8 query heads per KV head x 15 proposals: 64-row tiles, two row groups
+    assert (lib.carat_global_workspace_bytes(8, 15, 16, 2, 512, 32768)
+            == expected(8, 64, 512, 1, 2 * 2))
     assert lib.carat_swa_workspace_bytes(0, 1, 16, 8, 256, 1024) == 0
     assert lib.carat_swa_workspace_bytes(1, 1, 16, 8, 128, 1024) == 0       # unsupported D
     assert lib.carat_global_workspace_bytes(1, 17, 16, 2, 512, 1024) == 0   # too many proposals

@@ -22,6 +22,11 @@ with their special tile), and checks that every role reaches its end:
   softmax    per tile waits for S (QK done) and for the previous tile's PV,
              then publishes P (bf16: first waits for the tile's V stages, whose
              rows without a token it zeroes).
+  unit queue (FP8 unit mode, kq slots) the producer publishes each segment's
+             unit before its Q and stages, into a slot every other role has
+             read kq units before; the MMA thread, the softmax warps and the
+             widening warps each take the segment's unit from the queue before
+             their first step of it.
 
 The same model with a ring too small for a whole V tile must deadlock, so the
 check can see one.  (The model is kept with the kernel's stage order: a change
@@ -50,9 +55,20 @@ def _parts(n, special_first):
     return out
 
 
-def runs_to_end(segs, NS, KS, NR=0):
-    """True when every role finishes; NR > 0 models the FP8 kernel."""
+def runs_to_end(segs, NS, KS, NR=0, kq=None):
+    """True when every role finishes; NR > 0 models the FP8 kernel, kq the
+    unit queue's slots (None: no queue)."""
     f8 = NR > 0
+    published = set()                   # units the producer published
+    taken = {"mma": -1, "soft": -1, "widen": -1 if f8 else len(segs)}   # last unit taken
+
+    def take(role, si):
+        if kq is None or taken[role] >= si:
+            return True
+        if si not in published:
+            return False
+        taken[role] = si
+        return True
     early_special = NS == KS
     # stages in load order: (segment, tile, kind) with kind K, V or S (special)
     stages = []
@@ -91,6 +107,11 @@ def runs_to_end(segs, NS, KS, NR=0):
         # producer
         while prod < len(stages):
             si = stages[prod][0]
+            if kq is not None and si not in published:
+                if si >= kq and min(taken.values()) < si - kq:
+                    break
+                published.add(si)
+                moved = True
             if si not in q_loaded:
                 if si > 0 and (si - 1, last[si - 1]) not in qk:
                     break
@@ -106,6 +127,8 @@ def runs_to_end(segs, NS, KS, NR=0):
             # widening warps: Q of each segment, then its stages in order
             while widen < len(stages):
                 si = stages[widen][0]
+                if not take("widen", si):
+                    break
                 if wq <= si:
                     if si not in q_loaded:
                         break
@@ -125,7 +148,7 @@ def runs_to_end(segs, NS, KS, NR=0):
         while mp < len(mma):
             op, si, x = mma[mp]
             if op == "Q":
-                if si not in q_ready:
+                if not take("mma", si) or si not in q_ready:
                     break
             elif op == "QK":
                 key = (si, x, "S") if (si, x) in special else (si, x, "K")
@@ -147,6 +170,8 @@ def runs_to_end(segs, NS, KS, NR=0):
         # softmax
         while sp_ < len(soft):
             si, x = soft[sp_]
+            if not take("soft", si):
+                break
             if (si, x) not in qk:
                 break
             if sp_ > 0 and soft[sp_ - 1] not in pv:
@@ -185,6 +210,15 @@ def test_fp8_stage_order_finishes(NS, KS, NR):
         assert runs_to_end(segs, NS, KS, NR), (NS, KS, NR, segs)
 
 
+@pytest.mark.parametrize("NS,KS,NR", FP8)
+def test_fp8_unit_queue_finishes(NS, KS, NR):
+    # FP8 unit mode: each segment a whole unit taken through the 4-slot queue
+    rng = random.Random(7000 + 1000 * NS + 10 * KS + NR)
+    for _ in range(1500):
+        segs = [(rng.randint(1, 9), True) for _ in range(rng.randint(1, 8))]
+        assert runs_to_end(segs, NS, KS, NR, kq=4), (NS, KS, NR, segs)
+
+
 def test_model_sees_a_deadlock():
     # a bf16 ring of one stage cannot hold a 2-stage V tile whose rows the
     # softmax zeroes before the PV product that would free it
@@ -194,3 +228,6 @@ def test_model_sees_a_deadlock():
     # the widening warps free each raw slot as they go)
     assert not runs_to_end([(3, False)], 1, 2, 4)
     assert runs_to_end([(3, False)], 3, 2, 1)
+    # a unit queue with no slot never publishes a unit
+    assert not runs_to_end([(3, True), (2, True)], 5, 2, 3, kq=0)
+    assert runs_to_end([(3, True), (2, True)], 5, 2, 3, kq=1)
