@@ -111,12 +111,46 @@ def test_fp8_sliding_batched(orc):
 def test_fp8_mixed_step_sliding_layer(orc):
     w = synth.mixed_step()[0]
     # every request's attention against the oracle would take minutes on the
-    # host: a contiguous subset of the 64 requests (still 8 x 64 = 512 units
-    # on the GPU, one CTA each) is compared
+    # host: a contiguous subset of 12 of the 64 requests (96 units, fewer than
+    # the 152 CTAs: the stream-K schedule) is compared; test_fp8_sliding_batched
+    # and test_fp8_unit_queue_skips_rejected_requests cover the unit queue
     sub = synth.small("fp8_mixed_sub", seed=w.seed, batch=12, proposal_count=w.proposal_count,
                       q_heads=w.q_heads, kv_heads=w.kv_heads, head_dim=w.head_dim,
                       key_counts=w.key_counts[:12], window=w.window)
     _run(orc, sub)
+
+
+def test_fp8_unit_queue_skips_rejected_requests(orc):
+    """24 requests x 8 KV heads = 192 units over 152 persistent CTAs that take
+    whole units from the work counter.  Requests rejected on the device (a
+    negative context length, a ring id out of range) put no unit in the queue,
+    get NaN outputs and set the status bits; every other request comes out bit
+    for bit as in a call where all requests are valid, which matches the
+    oracle."""
+    kcs = [100 + 173 * i for i in range(24)]          # rings not full, full, wrapped
+    w = synth.small("fp8_queue", seed=5400, batch=24, proposal_count=4, q_heads=16, kv_heads=8,
+                    head_dim=256, key_counts=kcs, window=1024)
+    layer, inp, _, _ = _run(orc, w)                   # every request against the oracle
+    ref = layer.attend(inp.queries, inp.context_lengths).cpu().numpy()
+    torch.cuda.synchronize()
+    assert carat.carat_get_device_status(clear=True) == 0
+    bad_ctx = inp.context_lengths.clone()
+    bad_ctx[[3, 17]] = -5
+    ids = torch.arange(24, dtype=torch.int32, device="cuda")
+    ids[[0, 8, 23]] = 99                              # 24 rings: out of range
+    out = layer.attend(inp.queries, bad_ctx, ring_ids=ids).cpu().numpy()
+    status = carat.carat_get_device_status(clear=True)
+    assert status & carat.CARAT_DEV_BAD_CONTEXT and status & carat.CARAT_DEV_BAD_CACHE_ID
+    assert not status & carat.CARAT_DEV_TIMEOUT
+    for b in range(24):
+        if b in (0, 3, 8, 17, 23):
+            assert np.isnan(out[b]).all(), b
+        else:
+            assert np.array_equal(out[b], ref[b]), b
+    # the next call on the same workspace starts the counter afresh
+    again = layer.attend(inp.queries, inp.context_lengths).cpu().numpy()
+    assert np.array_equal(again, ref)
+    assert carat.carat_get_device_status(clear=True) == 0
 
 
 FP8_EDGES = {

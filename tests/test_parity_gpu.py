@@ -307,6 +307,38 @@ def test_bad_device_values_flagged():
     assert carat.carat_get_device_status(clear=True) & carat.CARAT_DEV_BAD_CONTEXT
 
 
+def test_unit_mode_skips_rejected_requests(orc):
+    """40 requests x 8 KV heads = 320 units, more than the 304 CTA slots: one
+    CTA per unit.  Rejected requests (negative context length, ring id out of
+    range) get NaN outputs and status bits; every other request comes out bit
+    for bit as in a call where all requests are valid, which matches the
+    oracle."""
+    kcs = [60 + 101 * i for i in range(40)]
+    w = synth.small("unit_bad", seed=4100, batch=40, proposal_count=4, q_heads=16, kv_heads=8,
+                    head_dim=256, key_counts=kcs, window=1024)
+    layer = engine.SlidingLayer(40, window=1024, max_proposals=4, scale=w.scale)
+    inp = engine.stage_sliding(w, 0, layer)
+    layer.append(inp.k_new, inp.v_new, inp.context_lengths)
+    ref = layer.attend(inp.queries, inp.context_lengths).cpu().numpy()
+    refs = _oracle_requests(orc, w, 0, inp, list(range(40)), w.window)
+    for b in range(40):
+        assert_close(ref[b], refs[b], f"unit mode request {b}")
+    carat.carat_get_device_status(clear=True)
+    bad_ctx = inp.context_lengths.clone()
+    bad_ctx[[5, 31]] = -1
+    ids = torch.arange(40, dtype=torch.int32, device="cuda")
+    ids[[0, 20, 39]] = 40
+    out = layer.attend(inp.queries, bad_ctx, ring_ids=ids).cpu().numpy()
+    status = carat.carat_get_device_status(clear=True)
+    assert status & carat.CARAT_DEV_BAD_CONTEXT and status & carat.CARAT_DEV_BAD_CACHE_ID
+    assert not status & carat.CARAT_DEV_TIMEOUT
+    for b in range(40):
+        if b in (0, 5, 20, 31, 39):
+            assert np.isnan(out[b]).all(), b
+        else:
+            assert np.array_equal(out[b], ref[b]), b
+
+
 def test_ring_ids_indirection(orc):
     """Requests mapped to rings in a shuffled order give the same outputs."""
     w = synth.small("ids", seed=4100, batch=4, proposal_count=4, q_heads=16, kv_heads=8,
