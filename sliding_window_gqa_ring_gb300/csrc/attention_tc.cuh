@@ -1348,6 +1348,7 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
         } pend{};
         float *red_lsum = red + L::kRedLsum;  // LP: [4 warps][N] row sums over each warp's keys
         float *s_l = red + L::kRedL;          // LP: a finished segment's row sums
+        float *s_inv = red_lsum;              // LP: out_scale / row sum (after the reduction)
         auto write_segment = [&](const PendingEpi &pe) {
             const uint32_t tmo = tmem_o_of(pe.si);
             const uint32_t tml = tmem_l_of(pe.si);
@@ -1368,9 +1369,13 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
                     red_lsum[q4 * N + cb * 16 + rb] = v[0];
                 }
                 named_bar_softmax_any(false);
-                if (t < N)
+                if (t < N) {
                     s_l[t] = (red_lsum[t] + red_lsum[N + t]) +
                              (red_lsum[2 * N + t] + red_lsum[3 * N + t]);
+                    // the factor a whole segment's output row is scaled by,
+                    // divided once here rather than by every thread
+                    s_inv[t] = p.out_scale / s_l[t];
+                }
                 named_bar_softmax_any(false);
             }
             // A piece of a split unit goes to this CTA's partial slot (0: the
@@ -1397,7 +1402,7 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
                         const int r = cb * 16 + e;
                         if (r < pe.rows_here) {
                             const float inv =
-                                p.out_scale / (LP ? s_l[r] : __uint_as_float(l16[e]));
+                                LP ? s_inv[r] : p.out_scale / __uint_as_float(l16[e]);
                             float *o = p.out + (((size_t)pe.b * p.k + pe.pos0 + jr) * p.q_heads +
                                                 (size_t)pe.c * p.group + hp) * D + t;
 #pragma unroll
