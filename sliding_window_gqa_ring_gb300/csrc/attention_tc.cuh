@@ -1349,6 +1349,7 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
         float *red_lsum = red + L::kRedLsum;  // LP: [4 warps][N] row sums over each warp's keys
         float *s_l = red + L::kRedL;          // LP: a finished segment's row sums
         float *s_inv = red_lsum;              // LP: out_scale / row sum (after the reduction)
+        int *s_off = reinterpret_cast<int *>(red_lsum + N);   // LP: a row's output offset
         auto write_segment = [&](const PendingEpi &pe) {
             const uint32_t tmo = tmem_o_of(pe.si);
             const uint32_t tml = tmem_l_of(pe.si);
@@ -1373,8 +1374,12 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
                     s_l[t] = (red_lsum[t] + red_lsum[N + t]) +
                              (red_lsum[2 * N + t] + red_lsum[3 * N + t]);
                     // the factor a whole segment's output row is scaled by,
-                    // divided once here rather than by every thread
+                    // divided once here rather than by every thread, and the
+                    // row's offset in the output (row t = j * group + h' goes
+                    // to out[b][pos0 + j][c * group + h'])
                     s_inv[t] = p.out_scale / s_l[t];
+                    const int jr = t / p.group;
+                    s_off[t] = (jr * p.q_heads + (t - jr * p.group)) * D;
                 }
                 named_bar_softmax_any(false);
             }
@@ -1393,7 +1398,22 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
                 for (int ob = 0; ob < KS; ++ob)
                     tc::tmem_ld16(tmo + ob * N + lane_off + cb * 16, o16[ob]);
                 tc::tmem_ld_wait();
-                if (pe.whole) {
+                if (LP && pe.whole) {
+                    // The segment saw every key of its rows: normalise and write.
+                    float *obase = p.out + (((size_t)pe.b * p.k + pe.pos0) * p.q_heads +
+                                            (size_t)pe.c * p.group) * D + t;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int r = cb * 16 + e;
+                        if (r < pe.rows_here) {
+                            const float inv = s_inv[r];
+                            float *o = obase + s_off[r];
+#pragma unroll
+                            for (int ob = 0; ob < KS; ++ob)
+                                o[ob * 128] = __uint_as_float(o16[ob][e]) * inv;
+                        }
+                    }
+                } else if (pe.whole) {
                     // The segment saw every key of its rows: normalise and write.
                     // Row r = j * group + h' goes to out[b][j][c * group + h'].
                     int jr = (cb * 16) / p.group, hp = (cb * 16) - jr * p.group;
@@ -1401,8 +1421,7 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
                     for (int e = 0; e < 16; ++e) {
                         const int r = cb * 16 + e;
                         if (r < pe.rows_here) {
-                            const float inv =
-                                LP ? s_inv[r] : p.out_scale / __uint_as_float(l16[e]);
+                            const float inv = p.out_scale / __uint_as_float(l16[e]);
                             float *o = p.out + (((size_t)pe.b * p.k + pe.pos0 + jr) * p.q_heads +
                                                 (size_t)pe.c * p.group + hp) * D + t;
 #pragma unroll
