@@ -1350,39 +1350,42 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
         float *s_l = red + L::kRedL;          // LP: a finished segment's row sums
         float *s_inv = red_lsum;              // LP: out_scale / row sum (after the reduction)
         int *s_off = reinterpret_cast<int *>(red_lsum + N);   // LP: a row's output offset
+        // LP: lane t of a finished segment's L^T holds the row sums over the
+        // keys thread t owned; add them up over the 128 lanes (a warp
+        // transpose-reduction per 16 rows, then across the four warps by one
+        // thread per row), with each row's output factor and offset.  Run at
+        // the segment's end, while its last PV product is still on the tensor
+        // core: the softmax threads alone write L^T.
+        auto reduce_row_sums = [&](int seg) {
+            const uint32_t tml = tmem_l_of(seg);
+#pragma unroll 1
+            for (int cb = 0; cb < N / 16; ++cb) {
+                uint32_t l16[16];
+                tc::tmem_ld16(tml + lane_off + cb * 16, l16);
+                tc::tmem_ld_wait();
+                float v[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(l16[e]);
+                const int rb = warp_transpose_reduce<16, false>(v, lane);
+                red_lsum[q4 * N + cb * 16 + rb] = v[0];
+            }
+            named_bar_softmax_any(false);
+            if (t < N) {
+                s_l[t] = (red_lsum[t] + red_lsum[N + t]) +
+                         (red_lsum[2 * N + t] + red_lsum[3 * N + t]);
+                // the factor a whole segment's output row is scaled by, divided
+                // once here rather than by every thread, and the row's offset in
+                // the output (row t = j * group + h' goes to
+                // out[b][pos0 + j][c * group + h'])
+                s_inv[t] = p.out_scale / s_l[t];
+                const int jr = t / p.group;
+                s_off[t] = (jr * p.q_heads + (t - jr * p.group)) * D;
+            }
+            named_bar_softmax_any(false);
+        };
         auto write_segment = [&](const PendingEpi &pe) {
             const uint32_t tmo = tmem_o_of(pe.si);
             const uint32_t tml = tmem_l_of(pe.si);
-            if constexpr (LP) {
-                // Lane t of L^T holds the row sums over the keys thread t
-                // owned: add them up over the 128 lanes (a warp transpose-
-                // reduction per 16 rows, then across the four warps by one
-                // thread per row).
-#pragma unroll 1
-                for (int cb = 0; cb < N / 16; ++cb) {
-                    uint32_t l16[16];
-                    tc::tmem_ld16(tml + lane_off + cb * 16, l16);
-                    tc::tmem_ld_wait();
-                    float v[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(l16[e]);
-                    const int rb = warp_transpose_reduce<16, false>(v, lane);
-                    red_lsum[q4 * N + cb * 16 + rb] = v[0];
-                }
-                named_bar_softmax_any(false);
-                if (t < N) {
-                    s_l[t] = (red_lsum[t] + red_lsum[N + t]) +
-                             (red_lsum[2 * N + t] + red_lsum[3 * N + t]);
-                    // the factor a whole segment's output row is scaled by,
-                    // divided once here rather than by every thread, and the
-                    // row's offset in the output (row t = j * group + h' goes
-                    // to out[b][pos0 + j][c * group + h'])
-                    s_inv[t] = p.out_scale / s_l[t];
-                    const int jr = t / p.group;
-                    s_off[t] = (jr * p.q_heads + (t - jr * p.group)) * D;
-                }
-                named_bar_softmax_any(false);
-            }
             // A piece of a split unit goes to this CTA's partial slot (0: the
             // range's first segment, 1: its last).
             const int slot = pe.start == sk->s ? 0 : 1;
@@ -1891,6 +1894,7 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
             pend.row0 = row0;
             pend.rows_here = rows_here;
             pend.start = sg.start;
+            if constexpr (LP) reduce_row_sums(si);
             gt += n;
             cnt_base += stages_before(2 * n);
             ++si;
