@@ -198,6 +198,7 @@ struct SkShared {
     long long len;                // stream-K: cost of one range (tiles plus unit charges)
     long long ucost0;             // cost position of the first segment's unit
     int segc;                     // cost charged per unit, in tiles
+    int special_last;             // the units' special tiles come last (see order_tile)
     // FP8 unit mode: the units taken, in order (only FP8 kernels reserve the
     // space: the misc area is 128 bytes with bf16 caches, 256 with FP8)
     UnitDesc uq[kUnitQ];
@@ -219,6 +220,7 @@ struct Segment {
     long long ctx;
     int ntiles, special;       // tiles of the unit and its special tile (-1: none)
     int x0, x1;                // order indices [x0, x1) of the unit's tiles covered here
+    bool special_last;         // the special tile comes last (else first)
     long long start;           // flattened index of the segment's first tile
     long long unit_start;      // flattened index of the unit's first tile
     long long unit_cost;       // cost position of the unit (see locate_range)
@@ -226,9 +228,12 @@ struct Segment {
 
 // Tile index of order index x: the special tile (this step's rows of a fused
 // append, or the displaced rows of a sliding verify; always the last tile
-// index) comes first.  It takes a single stage, held until its PV product.
+// index) comes first, or, in unit mode with a ring deeper than one V tile,
+// last (the natural order), so that a unit ends with its smallest PV product
+// rather than a whole tile's.  It takes a single stage, held until its PV
+// product.
 __device__ __forceinline__ int order_tile(const Segment &sg, int x) {
-    if (sg.special >= 0) return x == 0 ? sg.special : x - 1;
+    if (sg.special >= 0 && !sg.special_last) return x == 0 ? sg.special : x - 1;
     return x;
 }
 
@@ -242,11 +247,13 @@ struct SegIter {
     long long ucost;   // cost position of the current unit
     int segc;          // cost charged per unit
     int rg_fixed;      // paired schedule: this CTA's row group (else -1)
+    bool special_last; // the special tile comes last in each unit's order
 
     __device__ void init(const AttnParams &p, const SkShared *sk, int rg = -1) {
         rg_fixed = rg;
         ucost = sk->ucost0;
         segc = sk->segc;
+        special_last = sk->special_last != 0;
         pos = sk->s;
         end = sk->e;
         b = sk->b0;
@@ -290,6 +297,7 @@ struct SegIter {
         sg.ctx = ctx;
         sg.ntiles = ntiles;
         sg.special = special;
+        sg.special_last = special_last;
         if (rg_fixed >= 0) {
             sg.c = ur;
             sg.rg = rg_fixed;
@@ -1063,6 +1071,9 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
             // K/V rows are read once, except by a pair, where the second read
             // should find them in L2
             pol = paired ? tc::l2_evict_normal_policy() : tc::l2_evict_first_policy();
+            // Whole units whose ring holds a whole V tile besides the special
+            // tile's stage end with the special tile (see order_tile).
+            sk->special_last = (plan.unit_mode && NS > KS) ? 1 : 0;
         }
         if (plan.unit_mode) {
             if constexpr (F8)
@@ -1502,7 +1513,9 @@ __global__ void __launch_bounds__(NR > 0 ? kThreads + kConvThreads : kThreads, M
             const int base_slot = (ring && p.fused) ? (int)(ctx % p.window) : 0;
             // Segment-local index of the special tile (-1: not in this
             // segment): its K part takes one stage and its V part none.
-            const int xs = (sg.special >= 0 && sg.x0 == 0) ? 0 : -1;
+            const int xs = sg.special < 0 ? -1
+                           : sg.special_last ? (sg.x1 == sg.ntiles ? sg.ntiles - 1 - sg.x0 : -1)
+                                             : (sg.x0 == 0 ? 0 : -1);
             // Stages the producer issued for the segment's parts before part P.
             auto stages_before = [&](int P) -> uint32_t {
                 uint32_t st = (uint32_t)P * KS;

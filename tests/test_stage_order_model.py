@@ -37,8 +37,9 @@ import random
 import pytest
 
 
-def _parts(n, special_first):
-    """Parts of a segment of n tiles in load order: (tile x, is_v, special)."""
+def _parts(n, special_first, last=False):
+    """Parts of a segment of n tiles in load order: (tile x, is_v, special); the
+    special tile is order index 0, or n - 1 with `last`."""
     out = []
     for P in range(2 * n):
         if P == 0:
@@ -48,17 +49,18 @@ def _parts(n, special_first):
         else:
             x = (P - 1) // 2 + (1 if (P - 1) % 2 == 0 else 0)
             v = (P - 1) % 2 == 1
-        sp = special_first and x == 0
+        sp = special_first and x == (n - 1 if last else 0)
         if sp and v:
             continue
         out.append((x, v, sp))
     return out
 
 
-def runs_to_end(segs, NS, KS, NR=0, kq=None):
+def runs_to_end(segs, NS, KS, NR=0, kq=None, spec_last=False):
     """True when every role finishes; NR > 0 models the FP8 kernel, kq the
     unit queue's slots (None: no queue)."""
     f8 = NR > 0
+    early_special_ok = not spec_last    # a leading special tile's PV may come at step 0
     published = set()                   # units the producer published
     taken = {"mma": -1, "soft": -1, "widen": -1 if f8 else len(segs)}   # last unit taken
 
@@ -69,18 +71,18 @@ def runs_to_end(segs, NS, KS, NR=0, kq=None):
             return False
         taken[role] = si
         return True
-    early_special = NS == KS
+    early_special = NS == KS and early_special_ok
     # stages in load order: (segment, tile, kind) with kind K, V or S (special)
     stages = []
     for si, (n, sp) in enumerate(segs):
-        for x, v, s in _parts(n, sp):
+        for x, v, s in _parts(n, sp, spec_last):
             kind = "S" if s else ("V" if v else "K")
             stages += [(si, x, kind)] * (1 if s else KS)
     by_part = {}
     for j, (si, x, kind) in enumerate(stages):
         by_part.setdefault((si, x, kind), []).append(j)
     last = {si: n - 1 for si, (n, sp) in enumerate(segs)}
-    special = {(si, 0) for si, (n, sp) in enumerate(segs) if sp}
+    special = {(si, n - 1 if spec_last else 0) for si, (n, sp) in enumerate(segs) if sp}
 
     loaded, landed_ring, released = set(), set(), set()   # ring the MMA reads
     raw_free = set()                                       # FP8: raw slots freed
@@ -219,6 +221,23 @@ def test_fp8_unit_queue_finishes(NS, KS, NR):
         assert runs_to_end(segs, NS, KS, NR, kq=4), (NS, KS, NR, segs)
 
 
+@pytest.mark.parametrize("NS,KS", [(3, 2), (6, 2), (5, 2)])
+def test_bf16_special_last_finishes(NS, KS):
+    # unit mode with a ring deeper than one V tile: the special tile last
+    rng = random.Random(9000 + 10 * NS + KS)
+    for _ in range(1500):
+        segs = [(rng.randint(1, 9), rng.random() < 0.8)]
+        assert runs_to_end(segs, NS, KS, spec_last=True), (NS, KS, segs)
+
+
+@pytest.mark.parametrize("NS,KS,NR", [(5, 2, 3)])
+def test_fp8_special_last_with_unit_queue_finishes(NS, KS, NR):
+    rng = random.Random(9100 + NS)
+    for _ in range(1500):
+        segs = [(rng.randint(1, 9), rng.random() < 0.8) for _ in range(rng.randint(1, 8))]
+        assert runs_to_end(segs, NS, KS, NR, kq=4, spec_last=True), (NS, KS, NR, segs)
+
+
 def test_model_sees_a_deadlock():
     # a bf16 ring of one stage cannot hold a 2-stage V tile whose rows the
     # softmax zeroes before the PV product that would free it
@@ -228,6 +247,10 @@ def test_model_sees_a_deadlock():
     # the widening warps free each raw slot as they go)
     assert not runs_to_end([(3, False)], 1, 2, 4)
     assert runs_to_end([(3, False)], 3, 2, 1)
+    # the special tile last needs a ring deeper than one V tile: its stage is
+    # held to its PV product, after the last V tile's
+    assert not runs_to_end([(3, True)], 2, 2, spec_last=True)
+    assert runs_to_end([(3, True)], 3, 2, spec_last=True)
     # a unit queue with no slot never publishes a unit
     assert not runs_to_end([(3, True), (2, True)], 5, 2, 3, kq=0)
     assert runs_to_end([(3, True), (2, True)], 5, 2, 3, kq=1)
