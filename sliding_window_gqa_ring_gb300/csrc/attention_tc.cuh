@@ -32,9 +32,10 @@
 // its producer has issued a unit's loads it takes the next unit from a work
 // counter in the workspace (so that unit's keys stream in while the last one
 // finishes), publishing it to the other roles through a small queue in
-// shared memory; the launch's last CTA clears the counter.  Otherwise
-// (stream-K): a unit's tiles are taken
-// in a fixed order (the small tile of this step's rows first).  All units'
+// shared memory; the launch's last CTA clears the counter.  A whole unit's
+// small special tile comes last when the stage ring holds a whole V tile
+// besides it (see order_tile).  Otherwise (stream-K): a unit's tiles are
+// taken in a fixed order (the small special tile first).  All units'
 // tiles, request after request, form one flattened sequence of tiles, and
 // the grid -- one CTA per resident slot, so every CTA starts at once -- cuts
 // it into contiguous ranges of equal cost (stream-K), where a unit costs its
@@ -111,7 +112,8 @@ struct TcMaps {
 struct TcPlan {
     int row_groups;
     int pos_per_group;    // proposal positions per row group
-    int unit_mode;        // 1: CTA g takes unit g whole (grid = units); 0: stream-K
+    int unit_mode;        // 1: whole units (bf16: CTA g takes unit g, grid = units;
+                          // FP8: persistent CTAs and the unit queue); 0: stream-K
     // stream-K with two row groups: CTAs 2r and 2r + 1 walk the same range r
     // of the (request, KV head) order, one row group each, so each K/V tile is
     // read by both at about the same time and the second read comes from L2

@@ -204,8 +204,10 @@ cudaError_t launch_ring_rollback(const AppendParams &p, const int32_t *accepted,
 // Tensor-core path (attention_tc.cu): rows per tile (16, 32 or 64) for a
 // group size and proposal count, CTAs resident per SM, whether the shape is
 // supported, (request, KV head, row group) units per request, and the launch
-// over tiles of 128 keys on `grid` CTAs: one CTA per unit (unit_mode, grid =
-// units) or the persistent stream-K schedule (grid = resident slots).
+// over tiles of 128 keys on `grid` CTAs: whole units (unit_mode: one CTA per
+// unit with bf16 caches, grid = units; persistent CTAs taking units from a
+// work counter with FP8 caches, grid = resident slots) or the persistent
+// stream-K schedule (grid = resident slots).
 constexpr int kTcTileKeys = 128;
 int tc_rows_per_tile(int group, int k);
 int tc_ctas_per_sm(int head_dim, int rows_per_tile, bool fp8);
