@@ -14,7 +14,9 @@ needed between steps.  Timed steps repeat the same step at fixed positions (same
 work every step).
 
 The line's `configs` key times the single-layer workloads one call at a time
-(L2 flushed before each call): the single-request sliding decode (key count
+(L2 flushed before each call; the attention call also with the kernel's code
+put back in the caches by an untimed call on other, small data): the
+single-request sliding decode (key count
 1500), the batched sliding decode (56 requests), the single-request global
 verify (6005 keys, 4 proposals) and the 8-request global verify sweeps (4 and
 15 proposals), with the launch floor and the pages' unfused design of the
@@ -289,12 +291,15 @@ def config_attention_bytes(w):
     return total
 
 
-def median_call_us(fn, reps, flush, stream, trimmed=None):
+def median_call_us(fn, reps, flush, stream, trimmed=None, warm=None):
     """Median over reps of one call timed with CUDA events on `stream`, with
     the L2 flushed (a write larger than L2) before each timed call.  CUDA event
     timestamps on this GPU come in steps of about 2 us, so the mean of the
     middle 80% of the samples (`trimmed`, a one-element list, if given) is
-    also recorded: its resolution is finer than one step."""
+    also recorded: its resolution is finer than one step.  `warm`, if given,
+    runs untimed between the flush and the call (a call of the same kernel on
+    other, small data: the kernel's code is back in the caches, the timed
+    call's data is not)."""
     import torch
     for _ in range(3):
         fn()
@@ -302,6 +307,8 @@ def median_call_us(fn, reps, flush, stream, trimmed=None):
     times = []
     for _ in range(reps):
         flush.zero_()
+        if warm is not None:
+            warm()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -331,8 +338,8 @@ def run_configs(dev, reps, peak, peak_kind, ablation_reps):
     floor1 = median_call_us(lambda: carat.carat_launch_floor(False), reps, flush, stream, ft)
     floor2 = median_call_us(lambda: carat.carat_launch_floor(True), reps, flush, stream, ft)
     rows = []
-    for w in (synth.sliding_single(), synth.sliding_batched(), synth.global_single(),
-              synth.global_sweep(4), synth.global_sweep(15)):
+
+    def staged(w):
         if w.window:
             layer = engine.SlidingLayer(w.batch, window=w.window, q_heads=w.q_heads,
                                         kv_heads=w.kv_heads, head_dim=w.head_dim,
@@ -346,7 +353,23 @@ def run_configs(dev, reps, peak, peak_kind, ablation_reps):
                                        device=dev)
             inp = engine.stage_global(w, 0, layer, keep_history=False)
         inp.host.clear()
+        return layer, inp
+
+    for w in (synth.sliding_single(), synth.sliding_batched(), synth.global_single(),
+              synth.global_sweep(4), synth.global_sweep(15)):
+        layer, inp = staged(w)
         out = torch.empty(inp.queries.shape, dtype=torch.float32, device=dev)
+        # the same shapes (so the same kernel and schedule) over 130 keys a
+        # request, on memory of its own: its call before a timed one puts
+        # the kernel's code back in the caches without the timed call's data
+        ws = synth.small(w.name + "_warm", seed=w.seed + 7, batch=w.batch,
+                         proposal_count=w.proposal_count, q_heads=w.q_heads,
+                         kv_heads=w.kv_heads, head_dim=w.head_dim,
+                         key_counts=[max(130, w.proposal_count)] * w.batch, window=w.window,
+                         capacity=w.capacity, scale=w.scale)
+        wlayer, winp = staged(ws)
+        wlayer.append(winp.k_new, winp.v_new, winp.context_lengths)
+        wout = torch.empty(winp.queries.shape, dtype=torch.float32, device=dev)
 
         def append():
             layer.append(inp.k_new, inp.v_new, inp.context_lengths)
@@ -361,10 +384,14 @@ def run_configs(dev, reps, peak, peak_kind, ablation_reps):
         n0 = carat.kernel_launches()
         attend()
         attn_launches = carat.kernel_launches() - n0
+        def warm_attend():
+            wlayer.attend(winp.queries, winp.context_lengths, out=wout)
+
         tm = []
         append_us = median_call_us(append, reps, flush, stream)
         attn_us = median_call_us(attend, reps, flush, stream, tm)
         fused_us = median_call_us(fused, reps, flush, stream, tm)
+        attn_warm_us = median_call_us(attend, reps, flush, stream, tm, warm=warm_attend)
         nbytes = config_attention_bytes(w)
         floor = floor2 if attn_launches > 1 else floor1
         gbs = nbytes / (attn_us * 1e3)
@@ -374,12 +401,14 @@ def run_configs(dev, reps, peak, peak_kind, ablation_reps):
                      "attention_us_trimmed_mean": round(tm[0], 2),
                      "fused_us_trimmed_mean": round(tm[1], 2),
                      "attention_gb_s": round(gbs, 1), "attention_frac": round(gbs / peak, 4),
+                     "attention_us_code_warm": round(attn_warm_us, 2),
+                     "attention_us_code_warm_trimmed_mean": round(tm[2], 2),
                      "attention_launches": attn_launches,
                      "attention_floor_us": round(floor, 2),
                      "attention_excess_over_floor_us": round(attn_us - floor, 2),
                      "attention_frac_excluding_floor": round(
                          nbytes / max(attn_us - floor, 1e-3) / 1e3 / peak, 4)})
-        del layer, inp, out
+        del layer, inp, out, wlayer, winp, wout
         torch.cuda.empty_cache()
     abl = []
     if ablation_reps > 0:
@@ -395,7 +424,9 @@ def run_configs(dev, reps, peak, peak_kind, ablation_reps):
                        "flushed (512 MB write) before every timed call; floor = the same "
                        "timing of carat_launch_floor (one empty launch, or two with the "
                        "second a programmatic dependent launch, matching the call's launch "
-                       "count)"),
+                       "count); attention_us_code_warm: the same, with an untimed call of "
+                       "the same kernel on small data of its own between the flush and "
+                       "the timed call (code in the caches, data not)"),
             "ablation_unfused_global_verify": abl}
 
 
