@@ -209,6 +209,36 @@ def test_global_edges(orc, case, fused):
     _run_global(orc, w, fill=float("nan"), fused=fused)
 
 
+# Unit mode (whole units, one CTA per unit) with 32- and 64-row tiles, where
+# the ring holds more than one V tile besides the special tile's stage (so a
+# unit ends with its special tile): every output element against the oracle.
+# N(0,1) keys without outlier rows: with them, these 1.5-2.6 million outputs
+# put 1-3 elements 1.4-2.6e-3 beyond the implementation bound (P rounded to
+# bf16 in a sharp softmax), the same with the special tile first; the sweeps
+# and edge cases keep the outlier rows.
+UNIT_MODE_WIDE = {
+    # name: (batch, k, q heads, kv heads, head dim, window, capacity)
+    "sliding_k15_rows32": (20, 15, 16, 8, 256, 1024, 0),     # 160 units, 152 CTAs per wave
+    "sliding_k16_rows64": (20, 16, 32, 8, 256, 1024, 0),     # 4 heads x 16 positions
+    "global_k4_rows32": (80, 4, 16, 2, 512, 0, 1024),        # 160 units, capacity 1024
+}
+
+
+@FUSED
+@pytest.mark.parametrize("name", sorted(UNIT_MODE_WIDE))
+def test_unit_mode_wide_tiles(orc, name, fused):
+    batch, k, hq, hkv, d, window, cap = UNIT_MODE_WIDE[name]
+    span = window if window else cap
+    kcs = [k + (i * 997) % (3 * span if window else span - k) for i in range(batch)]
+    w = synth.small(f"unit_{name}", seed=3200 + batch + k, batch=batch, proposal_count=k,
+                    q_heads=hq, kv_heads=hkv, head_dim=d, key_counts=kcs, window=window,
+                    capacity=cap)
+    if window:
+        _run_sliding(orc, w, fill=float("nan"), fused=fused)
+    else:
+        _run_global(orc, w, fill=float("nan"), fused=fused)
+
+
 def _probe_values(n_keys, d, marks):
     """V rows marking chosen positions in chosen columns; K all zero so every
     visible key gets the same weight and the output counts positions."""

@@ -221,7 +221,7 @@ def test_fp8_unit_queue_finishes(NS, KS, NR):
         assert runs_to_end(segs, NS, KS, NR, kq=4), (NS, KS, NR, segs)
 
 
-@pytest.mark.parametrize("NS,KS", [(3, 2), (6, 2), (5, 2)])
+@pytest.mark.parametrize("NS,KS", [(3, 2), (6, 2), (5, 2), (5, 4)])
 def test_bf16_special_last_finishes(NS, KS):
     # unit mode with a ring deeper than one V tile: the special tile last
     rng = random.Random(9000 + 10 * NS + KS)
