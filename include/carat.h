@@ -400,7 +400,12 @@ int carat_pool_stats(carat_pool *pool, int32_t *out4);
  *   value is widened exactly to f16 on chip; k_scale scales the scores and
  *   v_scale the output.  head_dim 256 only (CARAT_ERR_UNSUPPORTED else).  The
  *   workspace it needs is at most carat_swa_workspace_bytes for the same
- *   sizes.  Other arguments, limits and device-side error handling as in
+ *   sizes.  When the call's units (request, KV head) outnumber the SMs, one
+ *   CTA per SM takes whole units from a work counter in the workspace: each
+ *   call tags the counter with a new epoch (so the workspace still needs no
+ *   initialisation, whatever it held) and the call's last CTA clears it;
+ *   concurrent calls on one workspace are as unsupported as for every other
+ *   call.  Other arguments, limits and device-side error handling as in
  *   carat_swa_attention.
  */
 carat_status carat_ring_append_fp8(void *k_ring, void *v_ring, int num_rings,
